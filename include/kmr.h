@@ -1,0 +1,249 @@
+/*
+ * kmr.h — C ABI of the GB300 int4 weight-only, group-wise decode-step library.
+ *
+ * The method: one greedy decode step of a Qwen3-style text decoder whose
+ * attention and MLP linears are stored as int4 codes with a bf16 scale and
+ * zero per group of 128 inputs, while embeddings, the tied LM head and the
+ * norms stay bf16 ("kaminari — a single-GPU Qwen3-VL inference engine,
+ * explained", §07 int4 sidecar quantization; §04 Request lifecycle, decode).
+ *
+ * Conventions for every entry point
+ *   - Return value: KMR_OK (0) or a negative KMR_ERR_* code; arguments are
+ *     checked on the host before anything is launched, and a failed check
+ *     launches nothing.
+ *   - Device pointers are raw CUDA device addresses on the current device;
+ *     host pointers are ordinary process memory.  The library never frees or
+ *     keeps a pointer the caller passes, except where stated.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Device work is asynchronous on that stream unless the entry
+ *     point says it synchronises.
+ *   - Kernels that detect bad per-row state at run time (a slot id out of
+ *     range, an unfinished row whose cache_position is outside [0, max_len))
+ *     skip that row and record the first such error in a device error word
+ *     that kmr_model_sync_status() / kmr_last_device_error() return.
+ *   - No kernel traps; every device wait is bounded and reports
+ *     KMR_ERR_DEVICE_TIMEOUT instead of hanging.
+ *
+ * Packed int4 layout ("KMR4", version 1; the library's own, not torchao's)
+ *   Canonical input: q uint8 [N, K] row-major with values 0..15 (row n =
+ *   output feature, column k = input feature), s and z bf16 [N, K / 128].
+ *   The dense weight is W[n, k] = (q[n, k] - 8) * s[n, k/128] + z[n, k/128].
+ *   Packing:
+ *     W_ks  = the K-slice width: the largest multiple of 128 that divides K
+ *             and is <= 1024;  KSL = K / W_ks slices per row tile.
+ *     Rows are grouped in tiles of 8 (N is padded to a multiple of 8 with
+ *     q = 8, s = z = 0, i.e. zero weights).  With KMR_PACK_GATE_UP the
+ *     canonical rows [gate (N/2); up (N/2)] are reordered so that packed tile
+ *     t holds gate rows 4t..4t+3 followed by up rows 4t..4t+3.
+ *     The matrix is a sequence of units (tile t, slice j), unit index
+ *     t * KSL + j, each UNIT_BYTES = 4 * W_ks + W_ks / 4 bytes:
+ *       bytes [0, 4*W_ks): 8 rows of W_ks/2 bytes; row r of the tile at
+ *         r * W_ks/2.  Within a row, 32-bit little-endian word i covers the
+ *         8 inputs k = j*W_ks + 8i + e, e = 0..7, with the nibble of e at
+ *         bit offset {0, 16, 4, 20, 8, 24, 12, 28}[e].
+ *       bytes [4*W_ks, UNIT_BYTES): 8 rows x (W_ks/128) groups of
+ *         (s bf16, z bf16), little-endian, row-major.
+ *   kmr_packed_size() = ceil(N/8) * KSL * UNIT_BYTES
+ *                     = ceil(N/8)*8 * (K/2 + 4*K/128) bytes.
+ */
+#ifndef KMR_H_
+#define KMR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ status */
+#define KMR_OK                   0
+#define KMR_ERR_INVALID_ARG     -1   /* null pointer, bad flag, bad scalar        */
+#define KMR_ERR_SHAPE           -2   /* unsupported or inconsistent dimensions    */
+#define KMR_ERR_SLOT_RANGE      -3   /* slot id outside [0, slots)                */
+#define KMR_ERR_CACHE_FULL      -4   /* unfinished row with cache_position >= max_len */
+#define KMR_ERR_NO_PACK         -5   /* a layer's int4 weights were never loaded  */
+#define KMR_ERR_CUDA            -6   /* a CUDA runtime call failed                */
+#define KMR_ERR_DEVICE_TIMEOUT  -7   /* a bounded device wait gave up             */
+#define KMR_ERR_BUFFER_SIZE     -8   /* a caller buffer is smaller than required  */
+#define KMR_ERR_BATCH           -9   /* batch outside [1, max_batch]              */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* kmr_status_string(int status);
+
+/* Library / layout version: returns 1 for the KMR4 v1 packed layout. */
+int kmr_layout_version(void);
+
+/* ------------------------------------------------------------------ packing */
+#define KMR_PACK_GATE_UP  1   /* interleave [gate; up] halves in blocks of 4 rows */
+
+/* Bytes of the packed form of an [N, K] int4 matrix with the given group
+ * (group must be 128; K a multiple of 128).  Returns 0 for unsupported shapes. */
+size_t kmr_packed_size(int N, int K, int group);
+
+/* Pack canonical q/s/z (layout above) into `packed` (packed_bytes >=
+ * kmr_packed_size).  on_device = 0: all pointers are host memory and the call
+ * is synchronous on the host.  on_device = 1: all pointers are device memory
+ * and the work is queued on `stream`.  Codes above 15 are rejected on the
+ * host path (KMR_ERR_INVALID_ARG); the device path masks them to 4 bits.
+ * Bit-exact: kmr_unpack_int4(kmr_pack_int4(x)) == x. */
+int kmr_pack_int4(const uint8_t* q, const uint16_t* s_bf16, const uint16_t* z_bf16,
+                  int N, int K, int group, int flags,
+                  void* packed, size_t packed_bytes, int on_device, void* stream);
+
+/* Inverse of kmr_pack_int4 (same flags, same pointer placement rules). */
+int kmr_unpack_int4(const void* packed, size_t packed_bytes, int N, int K, int group, int flags,
+                    uint8_t* q, uint16_t* s_bf16, uint16_t* z_bf16, int on_device, void* stream);
+
+/* ------------------------------------------------------------------ int4 GEMV */
+#define KMR_EPI_NONE      0   /* y[m, n]  = sum_k x[m, k] W[n, k]                       */
+#define KMR_EPI_RESIDUAL  1   /* y[m, n] += sum_k x[m, k] W[n, k]                       */
+#define KMR_EPI_SILU_MUL  2   /* packed with KMR_PACK_GATE_UP: y[m, j] = silu(g_j) * u_j,
+                                 j < N/2, g = rows [0, N/2), u = rows [N/2, N)         */
+
+/* Workspace bytes kmr_int4_gemv needs for M rows (device memory, zero-filled
+ * by the caller before its first use; every successful call leaves it zeroed). */
+size_t kmr_int4_gemv_workspace_size(int N, int K, int group, int M);
+
+/* Dequant-fused int4 GEMV / skinny GEMM ("kaminari", §07 int4 sidecar
+ * quantization: decoder linears weight-only int4; §06 The optimization
+ * ladder: decode is memory-bandwidth-bound, so the packed weights are
+ * streamed once and dequantised in registers).
+ *   packed  device, KMR4 layout of W [N, K] (flags as packed)
+ *   x       device fp32 [M, K] row-major, 1 <= M <= 16
+ *   y       device fp32 [M, N] (or [M, N/2] for KMR_EPI_SILU_MUL), row-major
+ *   The reduction order is fixed (no float atomics): results are bitwise
+ *   reproducible and a row's result does not depend on M. */
+int kmr_int4_gemv(const void* packed, int N, int K, int group, int flags,
+                  const float* x, int M, float* y, int epilogue,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------ attention */
+/* Workspace bytes kmr_decode_attn needs (device, zero-filled before first use,
+ * left zeroed by every successful call). */
+size_t kmr_decode_attn_workspace_size(int B, int n_q_heads, int n_kv_heads, int head_dim);
+
+/* GQA decode attention of one token per row over a static, slot-addressable
+ * bf16 KV cache ("The Ghost in the Batch", What Attention Does:
+ * out = softmax(q K^T / sqrt(d)) V, and the LSE-weighted merge of partial
+ * results; "kaminari", §03 StaticKVCache).  Split-KV: each (row, KV head)
+ * is cut into position chunks whose partial softmax states are merged in a
+ * fixed order; the split plan depends only on the row's own length.
+ *   q        device fp32 [B, n_q, d]
+ *   k_cache, v_cache  device bf16 [slots, n_kv, max_len, d] (one layer)
+ *   slot_ids device int32 [B]; cache_position device int32 [B]: row b attends
+ *            positions 0..cache_position[b] inclusive of slot slot_ids[b]
+ *   scale    softmax scale (1/sqrt(d) for the plain definition)
+ *   out      device fp32 [B, n_q, d]
+ *   Query head i reads KV head i / (n_q / n_kv).  head_dim must be 64 or 128.
+ *   Rows with a slot or position out of range are skipped (output zeros) and
+ *   set the error word read by kmr_last_device_error(). */
+int kmr_decode_attn(const float* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                    const int32_t* slot_ids, const int32_t* cache_position,
+                    int B, int n_q_heads, int n_kv_heads, int head_dim, int max_len, int slots,
+                    float scale, float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Error word of the standalone kernels (kmr_int4_gemv, kmr_decode_attn) on the
+ * current device: synchronises the device, returns the first recorded
+ * KMR_ERR_* (or KMR_OK) and clears it. */
+int kmr_last_device_error(void);
+
+/* ------------------------------------------------------------------ model */
+typedef struct kmr_model_config {
+    int hidden;            /* H                                    */
+    int n_q_heads;         /* query heads                          */
+    int n_kv_heads;        /* key/value heads (GQA)                */
+    int head_dim;          /* d: 64 or 128                         */
+    int intermediate;      /* I (MLP)                              */
+    int vocab;             /* V (tied embedding / LM head rows)    */
+    int n_layers;          /* L                                    */
+    int group;             /* int4 group along K: 128              */
+    float eps;             /* RMSNorm epsilon                      */
+    float rope_theta;      /* M-RoPE base                          */
+    int mrope_sections[3]; /* frequencies driven by T, H, W; sum = d/2 */
+    int qk_norm;           /* 1: per-head RMSNorm of q and k before the rotary embedding */
+    int eos_id;            /* token that finishes a row; -1: none  */
+    int pad_id;            /* token emitted by finished rows       */
+    int max_len;           /* static KV cache positions per slot   */
+    int slots;             /* physical cache rows                  */
+    int max_batch;         /* largest B a step may use (<= 16)     */
+} kmr_model_config;
+
+typedef struct kmr_model kmr_model;
+
+/* Create a model on the current device: allocates (once) the packed weights,
+ * the bf16 KV cache [L][slots][n_kv][max_len][d] for K and for V (zero-filled),
+ * and all step scratch.  No allocation happens per step ("kaminari", §03: the
+ * static cache is preallocated and mutated in place). */
+int kmr_model_create(const kmr_model_config* cfg, kmr_model** out);
+int kmr_model_destroy(kmr_model* m);
+
+/* Load one int4 linear of one layer from canonical host arrays (layout above).
+ * which: 0 = qkv [(nq+2nkv)d, H], 1 = o [H, nq d], 2 = gate_up [2I, H],
+ * 3 = down [H, I].  Fused rows follow qkv = [q; k; v], gate_up = [gate; up].
+ * Synchronous. */
+#define KMR_W_QKV 0
+#define KMR_W_O 1
+#define KMR_W_GATE_UP 2
+#define KMR_W_DOWN 3
+int kmr_model_set_linear(kmr_model* m, int layer, int which,
+                         const uint8_t* q, const uint16_t* s_bf16, const uint16_t* z_bf16);
+
+/* Load an RMSNorm weight (bf16 host array).  which: 0 = input [H],
+ * 1 = post-attention [H], 2 = q-norm [d], 3 = k-norm [d]; layer = -1 with
+ * which = 0 loads the final norm [H].  Synchronous. */
+#define KMR_N_INPUT 0
+#define KMR_N_POST 1
+#define KMR_N_Q 2
+#define KMR_N_K 3
+int kmr_model_set_norm(kmr_model* m, int layer, int which, const uint16_t* w_bf16);
+
+/* Load the tied bf16 embedding / LM head [V, H] from host memory.  Synchronous. */
+int kmr_model_set_embedding(kmr_model* m, const uint16_t* e_bf16);
+
+/* Write positions [0, length) of one layer's K and V cache rows of a slot
+ * from host bf16 arrays [n_kv, length, d] (a prefill stand-in).  Synchronous. */
+int kmr_model_set_kv(kmr_model* m, int layer, int slot, int length,
+                     const uint16_t* k_bf16, const uint16_t* v_bf16);
+
+/* Device pointers of one layer's K and V cache ([slots][n_kv][max_len][d] bf16). */
+int kmr_model_kv_pointers(kmr_model* m, int layer, void** k_cache, void** v_cache);
+
+/* One greedy decode step for B rows ("kaminari", §04 Request lifecycle,
+ * decode; §08 ContinuousBatchScheduler slots).  All pointers are device
+ * memory; the step state is read and advanced in place:
+ *   token_ids      int32 [B]    in: this step's token; out: the emitted token
+ *                               (argmax, lowest index on ties, or pad_id for
+ *                               rows finished before the step)
+ *   positions      int32 [3, B] in: M-RoPE (T, H, W) ids of this token;
+ *                               out: +1 for rows not finished before the step
+ *   cache_position int32 [B]    in: where this token's K/V are written (the row
+ *                               attends 0..cache_position); out: +1 likewise
+ *   slot_ids       int32 [B]    physical cache row of each batch row
+ *   finished       uint8 [B]    in/out: set when the emitted token is eos_id or
+ *                               the row has written position max_len - 1
+ *   logits         fp32 [B, V] or NULL: the final logits of every row
+ * A row finished before the step reads and writes no KV and does not advance.
+ * The step is a cached CUDA graph of the whole layer stack (captured on first
+ * use per pointer set and B); it is queued on `stream` without synchronising.
+ * Returns KMR_ERR_NO_PACK if any weight was never loaded. */
+int kmr_decode_step(kmr_model* m, int32_t* token_ids, int32_t* positions, int32_t* cache_position,
+                    const int32_t* slot_ids, uint8_t* finished, int B, float* logits, void* stream);
+
+/* The same step on HOST state arrays (same shapes and meaning): copies the
+ * state in, runs the step, copies the updated state back and synchronises
+ * `stream`.  logits (host fp32 [B, V]) may be NULL.  Per-row state is checked
+ * on the host first (KMR_ERR_SLOT_RANGE, KMR_ERR_CACHE_FULL). */
+int kmr_decode_step_host(kmr_model* m, int32_t* token_ids, int32_t* positions, int32_t* cache_position,
+                         const int32_t* slot_ids, uint8_t* finished, int B, float* logits, void* stream);
+
+/* Synchronise `stream`, then return and clear the model's device error word. */
+int kmr_model_sync_status(kmr_model* m, void* stream);
+
+/* Launches one step makes (kernels per step) for the given B, for accounting. */
+int kmr_model_kernels_per_step(const kmr_model* m, int B);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KMR_H_ */

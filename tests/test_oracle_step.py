@@ -1,0 +1,124 @@
+"""Invariants and special cases of the oracle's whole decode step (tiny model)."""
+import numpy as np
+import pytest
+
+from oracle import decoder as od
+from workloads import BF16_NAN, tiny_config, tiny_workload
+
+
+def _state(B=1, cpos=32, delta=0, tok=5, slot=0):
+    return (np.full(B, tok, np.int32), np.full((3, B), cpos + delta, np.int32),
+            np.full(B, cpos, np.int32), np.full(B, slot, np.int32), np.zeros(B, np.uint8))
+
+
+def test_zero_weights_reduce_to_embedding_dot():
+    """With every int4 linear zero (q=8, z=0) the residual stream stays E[tok]:
+    logits = E . rmsnorm(E[tok]) * w_final — a closed form of the tiny model."""
+    cfg = tiny_config()
+    o = od.OracleDecoder(cfg, seed=0)
+    zero = {}
+    for name, (N, K) in cfg.linear_shapes().items():
+        zero[name] = (np.full((N, K), 8, np.uint8), np.zeros((N, K // 128), np.uint16),
+                      np.zeros((N, K // 128), np.uint16))
+    o.syn.linear = lambda layer, name: zero[name]
+    o.prefill_cache(0, 32)
+    res = o.step(*_state(tok=77))
+    E = od.bf16_to_f64(o.syn.embedding())
+    x = E[77]
+    wf = od.bf16_to_f64(o.syn.norm(-1, "final"))
+    h = x / np.sqrt(np.mean(x * x) + cfg.eps) * wf
+    assert np.allclose(res.logits[0], E @ h, rtol=1e-12, atol=1e-15)
+
+
+def test_rows_are_independent_batch_invariance():
+    cfg = tiny_config(slots=3)
+    a = od.OracleDecoder(cfg, seed=0)
+    b = od.OracleDecoder(cfg, seed=0)
+    for s in range(3):
+        a.prefill_cache(s, 20 + 5 * s)
+        b.prefill_cache(s, 20 + 5 * s)
+    toks = np.array([3, 9, 100], np.int32)
+    cp = np.array([20, 25, 30], np.int32)
+    pos = np.stack([cp - 2, cp, cp + 1]).astype(np.int32)
+    full = a.step(toks, pos, cp, np.arange(3, dtype=np.int32), np.zeros(3, np.uint8))
+    one = b.step(toks[1:2], pos[:, 1:2], cp[1:2], np.array([1], np.int32), np.zeros(1, np.uint8))
+    assert np.allclose(full.logits[1], one.logits[0], rtol=1e-12, atol=1e-14)
+    assert full.next_ids[1] == one.next_ids[0]
+
+
+def test_step_writes_kv_only_at_cache_position_and_ignores_unfilled():
+    cfg = tiny_config()
+    clean = od.OracleDecoder(cfg, seed=0)
+    clean.prefill_cache(0, 32, fill=0)
+    nanfill = od.OracleDecoder(cfg, seed=0)
+    nanfill.prefill_cache(0, 32, fill=int(BF16_NAN))
+    before = [k.copy() for k in clean.K]
+    r1 = clean.step(*_state())
+    r2 = nanfill.step(*_state())
+    assert np.all(np.isfinite(r2.logits))
+    assert np.array_equal(r1.logits, r2.logits)       # positions > cache_position never read
+    for l in range(cfg.n_layers):
+        diff = np.argwhere(clean.K[l] != before[l])
+        assert diff.size and np.all(diff[:, 2] == 32)   # only position 32 changed
+
+
+def test_finished_row_emits_pad_and_does_not_advance():
+    cfg = tiny_config()
+    o = od.OracleDecoder(cfg, seed=0)
+    o.prefill_cache(0, 32)
+    kb = [k.copy() for k in o.K]
+    t, p, c, s, f = _state()
+    f[:] = 1
+    r = o.step(t, p, c, s, f)
+    assert r.next_ids[0] == cfg.pad_id and r.cache_position[0] == 32 and r.positions[0, 0] == 32
+    assert r.finished[0] == 1 and np.all(np.isnan(r.logits[0]))
+    assert all(np.array_equal(a, b) for a, b in zip(o.K, kb))
+
+
+def test_advance_eos_and_length_cap():
+    cfg = tiny_config()
+    o = od.OracleDecoder(cfg, seed=0)
+    o.prefill_cache(0, 32)
+    r = o.step(*_state())
+    assert r.cache_position[0] == 33 and np.all(r.positions[:, 0] == 33) and r.finished[0] == 0
+    assert r.next_ids[0] == od.argmax_lowest(r.logits[0])
+    # the same step with eos = the emitted token finishes the row
+    cfg2 = tiny_config(eos_id=int(r.next_ids[0]))
+    o2 = od.OracleDecoder(cfg2, seed=0)
+    o2.prefill_cache(0, 32)
+    assert o2.step(*_state()).finished[0] == 1
+    # writing the last cache position finishes the row (length cap)
+    o3 = od.OracleDecoder(cfg, seed=0)
+    o3.prefill_cache(0, cfg.max_len - 1)
+    r3 = o3.step(*_state(cpos=cfg.max_len - 1))
+    assert r3.finished[0] == 1 and r3.cache_position[0] == cfg.max_len
+    with pytest.raises(ValueError):
+        o3.step(*_state(cpos=cfg.max_len))
+
+
+def test_slot_indirection():
+    cfg = tiny_config(slots=4)
+    a = od.OracleDecoder(cfg, seed=0)
+    b = od.OracleDecoder(cfg, seed=0)
+    a.prefill_cache(0, 32)
+    # the same cache contents placed in physical slot 3
+    b.prefill_cache(3, 0)
+    for l in range(cfg.n_layers):
+        b.K[l][3] = a.K[l][0]
+        b.V[l][3] = a.V[l][0]
+    ra = a.step(*_state(slot=0))
+    rb = b.step(*_state(slot=3))
+    assert np.array_equal(ra.logits, rb.logits)
+
+
+def test_tiny_workload_greedy_16_steps_runs():
+    wl = tiny_workload()
+    o = od.OracleDecoder.for_workload(wl)
+    st = od.initial_state(wl)
+    toks = []
+    for _ in range(wl.steps):
+        r = o.step(*st)
+        toks.append(int(r.next_ids[0]))
+        st = (r.next_ids, r.positions, r.cache_position, st[3], r.finished)
+    assert len(toks) == 16 and all(0 <= t < wl.cfg.vocab for t in toks)
+    assert st[2][0] == 32 + 16
