@@ -1,0 +1,450 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark: int4 weight-only group-wise greedy decode of the
+28-layer 2B-shaped decoder on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--batch 1|4] [--impl kmr|reference]
+
+A step is one pass of the whole decode path (every layer's int4 QKV / O /
+gate_up / down GEMVs, q/k norm, M-RoPE, KV write and GQA attention, final
+norm, tied bf16 LM head, argmax and state advance) for the batch's rows.
+Workload (synthetic, seeded): batch 1 with 512 prefilled positions, 256
+greedy steps per generation (--batch 4: four continuous slots prefilled
+300/512/700/900, row 2 retired at step 64, row 3 length-capped at 1024,
+128 steps per generation).  The timed K steps run back to back as CUDA-graph
+replays; the state is rewound to the generation's start every generation.
+The per-step working set (1.4 GB of weights) is far larger than L2, so
+nothing survives in L2 between steps.
+
+Prints one JSON line (rank 0).  Multi-GPU: replicas only (the decode path
+does not shard); each rank runs its own model, time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "int4 decode tok/s @bs1/bs4 (2B-shaped); achieved HBM GB/s vs roofline"
+
+
+# ------------------------------------------------------------------ clocks during the timed region
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int = 0, interval_ms: int = 20):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms", str(interval_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = [r for t, r in self.rows if t0 - 0.05 <= t <= t1 + 0.05 and len(r) >= 9]
+        if not rows:
+            rows = [r for _, r in self.rows if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured (MEASURED_PEAKS.json)"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def profile_traffic(kernel_file: str, summary: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", summary)
+    src = os.path.join(ROOT, "int4_weight_only_group_gb300", "csrc", kernel_file)
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    text = open(path).read()
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    m_sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_tr or m_sha.group(1) != sha:
+        return None
+    return float(m_tr.group(1))
+
+
+# ------------------------------------------------------------------ workloads
+def workload(batch: int):
+    from workloads import full2b_b1_workload, full2b_b4_workload
+    return full2b_b1_workload() if batch == 1 else full2b_b4_workload()
+
+
+def tokens_per_generation(wl) -> int:
+    """Tokens the rows actually emit (non-pad) over one generation of wl.steps steps."""
+    total = 0
+    for b in range(wl.batch):
+        stop = wl.finish_at.get(b, wl.steps)
+        cap = wl.cfg.max_len - wl.prefill[b]
+        total += min(stop, cap, wl.steps)
+    return total
+
+
+def kv_bytes_per_generation(wl) -> int:
+    """KV bytes the attention moves over one generation (reads 0..pos-1, writes pos), all layers."""
+    c = wl.cfg
+    per_pos = c.n_layers * 2 * c.n_kv_heads * c.head_dim * 2
+    total = 0
+    for b in range(wl.batch):
+        n = min(wl.finish_at.get(b, wl.steps), c.max_len - wl.prefill[b], wl.steps)
+        total += per_pos * sum(wl.prefill[b] + t + 1 for t in range(n))
+    return total
+
+
+def weight_bytes(cfg) -> dict:
+    out = {}
+    for name, (N, K) in cfg.linear_shapes().items():
+        out[name] = N * (K // 2 + 4 * (K // 128))
+    out["lm_head"] = cfg.vocab * cfg.hidden * 2
+    out["norms"] = (cfg.n_layers * (2 * cfg.hidden + 2 * cfg.head_dim) + cfg.hidden) * 2
+    return out
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_kmr(args, rank: int, world: int) -> dict:
+    import torch
+    import int4_weight_only_group_gb300 as kmr
+    from int4_weight_only_group_gb300 import driver
+    from workloads import SyntheticModel
+    from workloads import initial_state
+
+    dev_index = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev_index)
+    wl = workload(args.batch)
+    cfg = wl.cfg
+    B = wl.batch
+    t_setup = time.time()
+    syn = SyntheticModel(cfg, wl.seed, memo=(rank == 0 and not args.no_cpu_baseline))
+    model = kmr.Model.from_config(cfg, max_batch=B)
+    driver.load_weights(model, syn, cfg.n_layers, cfg.qk_norm)
+    for b in range(B):
+        driver.load_kv(model, syn, cfg.n_layers, wl.slot_ids[b], wl.prefill[b])
+    setup_s = time.time() - t_setup
+
+    st0 = initial_state(wl)
+    dev = {k: torch.tensor(np.asarray(v), device="cuda") for k, v in
+           zip(("tok", "pos", "cpos", "slot", "fin"), st0)}
+    saved = {k: v.clone() for k, v in dev.items()}
+    stream = torch.cuda.current_stream()
+
+    def rewind():
+        for k in ("tok", "pos", "cpos", "fin"):
+            dev[k].copy_(saved[k])
+
+    def step(t_in_gen: int):
+        for row, at in wl.finish_at.items():
+            if at == t_in_gen:
+                dev["fin"][row] = 1
+        model.decode_step(dev["tok"], dev["pos"], dev["cpos"], dev["slot"], dev["fin"], B, None, stream)
+
+    for i in range(args.warmup):
+        step(i % wl.steps)
+    torch.cuda.synchronize()
+    assert model.sync_status(stream) == 0
+    rewind()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(dev_index) if rank == 0 else None
+    time.sleep(0.3 if clocks else 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    e0.record(stream)
+    gens = 0
+    for i in range(args.steps):
+        t = i % wl.steps
+        if t == 0 and i > 0:
+            rewind()
+            gens += 1
+        step(t)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = e0.elapsed_time(e1)
+    clk = None
+    if clocks:
+        time.sleep(0.1)
+        clocks.stop()
+        clk = clocks.summary(t0, t1)
+    assert model.sync_status(stream) == 0, "device error during the timed region"
+    full_gens, rem = divmod(args.steps, wl.steps)
+    tok_gen = tokens_per_generation(wl)
+    # tokens emitted in the timed steps (partial last generation counted exactly)
+    partial = 0
+    for b in range(B):
+        n = min(wl.finish_at.get(b, wl.steps), cfg.max_len - wl.prefill[b], wl.steps)
+        partial += min(n, rem)
+    tokens = full_gens * tok_gen + partial
+    kv_gen = kv_bytes_per_generation(wl)
+
+    if world > 1:
+        t = torch.tensor([elapsed_ms, tokens], dtype=torch.float64, device="cuda")
+        ts = [torch.zeros_like(t) for _ in range(world)]
+        torch.distributed.all_gather(ts, t)
+        elapsed_ms = max(float(x[0]) for x in ts)
+        tokens = sum(float(x[1]) for x in ts)
+    if rank != 0:
+        return {}
+
+    out = {"elapsed_ms": elapsed_ms, "tokens": tokens, "setup_s": setup_s, "clocks": clk,
+           "kernels_per_step": model.kernels_per_step(B), "kv_gen": kv_gen}
+    # ---- dominant kernel: the int4 GEMV, timed alone on rotating copies larger than L2
+    out["gemv"] = time_gemv(torch, kmr, syn, cfg, B)
+    # ---- end to end through the host-buffer C ABI call
+    out["e2e"] = time_e2e(torch, model, wl, st0, args.steps)
+    model.close()
+    if not args.no_cpu_baseline:
+        out["cpu"] = cpu_baseline(wl, syn)
+    return out
+
+
+def time_gemv(torch, kmr, syn, cfg, M: int) -> dict:
+    """Average CUDA-event duration of one int4 GEMV launch per projection shape, rotating
+    through distinct packed copies (> 2x L2 in total) so every launch streams from HBM."""
+    res = {}
+    stream = torch.cuda.current_stream()
+    for name, (N, K) in cfg.linear_shapes().items():
+        q, s, z = syn.linear(0, name)
+        flags = kmr.KMR_PACK_GATE_UP if name == "gate_up" else 0
+        size = kmr.kmr_packed_size(N, K, 128)
+        copies = max(4, int(np.ceil(300e6 / size)))
+        one = torch.empty(size, dtype=torch.uint8, device="cuda")
+        kmr.kmr_pack_int4(torch.from_numpy(q).cuda(), torch.from_numpy(s.view(np.int16)).cuda(),
+                          torch.from_numpy(z.view(np.int16)).cuda(), N, K, 128, flags, one, size, 1, stream)
+        bufs = [one] + [one.clone() for _ in range(copies - 1)]
+        x = torch.randn((M, K), device="cuda")
+        epi = kmr.KMR_EPI_SILU_MUL if name == "gate_up" else kmr.KMR_EPI_NONE
+        y = torch.zeros((M, N), device="cuda")
+        ws_b = kmr.kmr_int4_gemv_workspace_size(N, K, 128, M)
+        ws = torch.zeros(ws_b, dtype=torch.uint8, device="cuda")
+        for i in range(copies):
+            kmr.kmr_int4_gemv(bufs[i], N, K, 128, flags, x, M, y, epi, ws, ws_b, stream)
+        torch.cuda.synchronize()
+        reps = 200
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(reps):
+            kmr.kmr_int4_gemv(bufs[i % copies], N, K, 128, flags, x, M, y, epi, ws, ws_b, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1000.0 / reps
+        nbytes = size
+        res[name] = {"us": us, "bytes": nbytes, "gbs": nbytes / us / 1e3, "copies": copies}
+        del bufs, one
+    return res
+
+
+def time_e2e(torch, model, wl, st0, steps: int) -> dict:
+    """The same decode through kmr_decode_step_host: every step copies the step state in
+    from pinned host memory and the emitted tokens / state back, then synchronises."""
+    B = wl.batch
+    pin = {k: torch.from_numpy(np.array(v, copy=True)).pin_memory() for k, v in
+           zip(("tok", "pos", "cpos", "slot", "fin"), st0)}
+    arrs = {k: v.numpy() for k, v in pin.items()}
+    init = {k: v.copy() for k, v in arrs.items()}
+    n = min(steps, wl.steps)
+
+    def run(count):
+        for k in arrs:
+            arrs[k][...] = init[k]
+        for t in range(count):
+            for row, at in wl.finish_at.items():
+                if at == t:
+                    arrs["fin"][row] = 1
+            model.decode_step_host(arrs["tok"], arrs["pos"], arrs["cpos"], arrs["slot"], arrs["fin"], B, None,
+                                   torch.cuda.current_stream())
+
+    run(3)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    run(n)
+    dt = time.perf_counter() - t0
+    toks = 0
+    for b in range(B):
+        toks += min(wl.finish_at.get(b, wl.steps), wl.cfg.max_len - wl.prefill[b], n)
+    state_bytes = 25 * B   # tok, pos[3], cpos, slot (int32) + finished (uint8) per row
+    return {"value": toks / dt, "unit": "tok/s", "h2d_bytes_per_step": state_bytes,
+            "d2h_bytes_per_step": state_bytes, "steps": n}
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+def oracle_sample_time(wl, syn, layer_rows_frac: float, head_frac: float):
+    """Time one oracle layer (all of its math, on a row fraction of each linear) and a
+    vocab slice of the LM head; returns (s for the full step estimate, detail)."""
+    from oracle import decoder as od
+    cfg = wl.cfg
+    B = wl.batch
+    o = od.OracleDecoder(cfg, wl.seed, layers=1, syn=syn)
+    st = od.initial_state(wl)
+    for b in range(B):
+        o.prefill_cache(wl.slot_ids[b], wl.prefill[b])
+    x = od.bf16_to_f64(syn.embedding()[np.asarray(st[0])])
+    # weights drawn outside the timed region
+    for name in ("qkv", "o", "gate_up", "down"):
+        syn.linear(0, name)
+    t0 = time.perf_counter()
+    o._layer(0, x, st[1], st[2], st[3], st[4] == 0)
+    t_layer = time.perf_counter() - t0
+    nv = max(1, int(cfg.vocab * head_frac))
+    o.head_rows = slice(0, nv)
+    t0 = time.perf_counter()
+    o.logits_of(x)
+    t_head = time.perf_counter() - t0
+    full = t_layer * cfg.n_layers + t_head * cfg.vocab / nv
+    return full, {"t_layer_s": t_layer, "t_head_slice_s": t_head, "head_rows": nv}
+
+
+def cpu_baseline(wl, syn) -> dict:
+    full, det = oracle_sample_time(wl, syn, 1.0, 1.0 / 16)
+    tokens_per_step = tokens_per_generation(wl) / wl.steps
+    return {"value": tokens_per_step / full, "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"one full oracle layer (layer 0, all rows, attention included) x {wl.cfg.n_layers} "
+                      f"+ LM head on {det['head_rows']} of {wl.cfg.vocab} vocab rows scaled to the full vocab; "
+                      f"numpy float64 (BLAS threads = host cores); t_layer={det['t_layer_s']:.2f}s "
+                      f"t_head_slice={det['t_head_slice_s']:.2f}s",
+            "est_s_per_step": full}
+
+
+def run_reference(args) -> dict:
+    """The oracle as it stands, on the host cores, on this benchmark's workload: each step
+    is a bounded sample (one layer + a vocab slice of the head) scaled to a full step."""
+    from workloads import SyntheticModel
+    wl = workload(args.batch)
+    syn = SyntheticModel(wl.cfg, wl.seed, memo=True)
+    for i in range(args.warmup):
+        oracle_sample_time(wl, syn, 1.0, 1.0 / 64)
+    fulls = []
+    t0 = time.perf_counter()
+    budget_s = 150.0
+    for i in range(args.steps):
+        f, _ = oracle_sample_time(wl, syn, 1.0, 1.0 / 64)
+        fulls.append(f)
+        if time.perf_counter() - t0 > budget_s:
+            break
+    est = statistics.median(fulls)
+    tps = tokens_per_generation(wl) / wl.steps
+    value = tps / est
+    return {"metric": METRIC, "value": value, "unit": "tok/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": est * 1000.0, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "batch": wl.batch, "kv_max_len": wl.cfg.max_len},
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"per step: one oracle layer (all rows) x {wl.cfg.n_layers} + 1/64 of the "
+                                       f"LM head x 64; {len(fulls)} sampled steps (median), budget {budget_s:.0f}s"},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--batch", type=int, default=1, choices=(1, 4))
+    ap.add_argument("--impl", default="kmr", choices=("kmr", "reference"))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    r = run_kmr(args, rank, world)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+    wl = workload(args.batch)
+    cfg = wl.cfg
+    peaks = measured_peaks()
+    ms = r["elapsed_ms"] / args.steps
+    value = r["tokens"] / (r["elapsed_ms"] / 1000.0)
+    wb = weight_bytes(cfg)
+    step_weight_bytes = cfg.n_layers * (wb["qkv"] + wb["o"] + wb["gate_up"] + wb["down"]) + wb["lm_head"] + wb["norms"]
+    step_bytes = step_weight_bytes + r["kv_gen"] / wl.steps
+    g = r["gemv"]["gate_up"]
+    traffic = profile_traffic("kmr_gemv.cu", "int4_gemv_gate_up.md")
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int4w/bf16->f32", "data": "synthetic (seeded; shapes and distributions of the workload recipe)",
+        "config": {"workload": wl.name, "batch": wl.batch, "kv_max_len": cfg.max_len, "prefill": wl.prefill,
+                   "steps_per_generation": wl.steps, "l2": "inputs larger than L2 (1.4 GB of weights per step)",
+                   "parallelism": "replicas" if args.gpus > 1 else "single-gpu"},
+        "roofline": {"bound": "hbm", "kernel": "int4_gemv (gate_up shape, M=%d)" % wl.batch,
+                     "achieved": g["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": g["gbs"] / peaks["hbm_gbs"], "traffic": traffic,
+                     "peak_source": peaks["source"]},
+        "step_roofline": {"bytes_per_step": step_bytes, "achieved_gbs": step_bytes / (ms * 1e6),
+                          "frac": step_bytes / (ms * 1e6) / peaks["hbm_gbs"],
+                          "roofline_ms_per_step": step_bytes / (peaks["hbm_gbs"] * 1e6)},
+        "gemv_us": {k: round(v["us"], 2) for k, v in r["gemv"].items()},
+        "gemv_gbs": {k: round(v["gbs"], 1) for k, v in r["gemv"].items()},
+        "e2e": r["e2e"],
+        "gpu_launches": r["kernels_per_step"] * args.steps,
+        "clocks": r["clocks"],
+        "setup_s": round(r["setup_s"], 1),
+    }
+    if "cpu" in r:
+        line["cpu_baseline"] = r["cpu"]
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,812 @@
+// C ABI of the library (declared in kmr.h): argument checking, the model
+// object (packed weights, static KV cache, step scratch), the decode step as
+// a cached CUDA graph of programmatically-dependent kernel launches, and the
+// standalone GEMV / attention entry points.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
+#include "kmr_internal.cuh"
+
+namespace kmr {
+int pack_run(const uint8_t* q, const uint16_t* s, const uint16_t* z, int N, int K, int group, int flags,
+             void* packed, size_t packed_bytes, int on_device, cudaStream_t st);
+int unpack_run(const void* packed, size_t packed_bytes, int N, int K, int group, int flags, uint8_t* q, uint16_t* s,
+               uint16_t* z, int on_device, cudaStream_t st);
+cudaError_t gemv_set_attributes();
+cudaError_t head_set_attributes();
+cudaError_t attn_set_attributes();
+
+__device__ int g_standalone_err;
+
+int num_sms() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+int* standalone_error_word() {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_standalone_err) != cudaSuccess) return nullptr;
+    return static_cast<int*>(p);
+}
+
+cudaError_t ensure_kernel_attributes() {
+    static std::mutex mu;
+    static bool done[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (done[dev]) return cudaSuccess;
+    if ((e = gemv_set_attributes()) != cudaSuccess) return e;
+    if ((e = head_set_attributes()) != cudaSuccess) return e;
+    if ((e = attn_set_attributes()) != cudaSuccess) return e;
+    done[dev] = true;
+    return cudaSuccess;
+}
+
+// ------------------------------------------------------------------ GEMV launch helper
+struct GemvLaunch {
+    const uint8_t* w;
+    PackGeom g;
+    int in_kind;
+    const float* x;
+    const uint16_t* embed;
+    const int32_t* tokens;
+    int vocab;
+    float* x_out;
+    const uint16_t* norm_w;
+    float eps;
+    int epi;
+    float* y;
+    int ldy;
+};
+
+// Rows in passes of at most 8; returns the number of launches or a negative KMR code.
+static int enqueue_gemv(const GemvLaunch& a, int M, float* gpart, int* counters, int* err, cudaStream_t st,
+                        bool pdl, int sms) {
+    int launches = 0;
+    const int units = a.g.tiles * a.g.ksl;
+    const int grid = gemv_grid(units, sms);
+    for (int r0 = 0; r0 < M; r0 += kMaxMB) {
+        const int mr = (M - r0) < kMaxMB ? (M - r0) : kMaxMB;
+        const int MB = gemv_pick_mb(mr);
+        GemvParams p = {};
+        p.w = a.w;
+        p.N = a.g.N;
+        p.K = a.g.K;
+        p.wks = a.g.wks;
+        p.ksl = a.g.ksl;
+        p.tiles = a.g.tiles;
+        p.units = units;
+        p.unit_bytes = a.g.unit_bytes;
+        p.M = mr;
+        p.in_kind = a.in_kind;
+        p.x = a.x ? a.x + size_t(r0) * a.g.K : nullptr;
+        p.embed = a.embed;
+        p.tokens = a.tokens ? a.tokens + r0 : nullptr;
+        p.vocab = a.vocab;
+        p.x_out = a.x_out ? a.x_out + size_t(r0) * a.g.K : nullptr;
+        p.norm_w = a.norm_w;
+        p.eps = a.eps;
+        p.epi = a.epi;
+        p.y = a.y + size_t(r0) * a.ldy;
+        p.ldy = a.ldy;
+        p.gpart = gpart;
+        p.counters = counters;
+        p.err = err;
+        p.nstage = gemv_nstage(units, grid, a.g.unit_bytes);
+        if (launch_gemv(p, MB, grid, st, pdl || launches > 0) != cudaSuccess) return KMR_ERR_CUDA;
+        ++launches;
+    }
+    return launches;
+}
+
+}  // namespace kmr
+
+using namespace kmr;
+
+// ====================================================================== status / packing
+extern "C" const char* kmr_status_string(int s) {
+    switch (s) {
+        case KMR_OK: return "ok";
+        case KMR_ERR_INVALID_ARG: return "invalid argument";
+        case KMR_ERR_SHAPE: return "unsupported or inconsistent shape";
+        case KMR_ERR_SLOT_RANGE: return "slot id out of range";
+        case KMR_ERR_CACHE_FULL: return "cache position out of range for an unfinished row";
+        case KMR_ERR_NO_PACK: return "int4 weights not loaded";
+        case KMR_ERR_CUDA: return "CUDA runtime error";
+        case KMR_ERR_DEVICE_TIMEOUT: return "bounded device wait timed out";
+        case KMR_ERR_BUFFER_SIZE: return "buffer too small";
+        case KMR_ERR_BATCH: return "batch size out of range";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int kmr_layout_version(void) { return 1; }
+
+extern "C" size_t kmr_packed_size(int N, int K, int group) {
+    PackGeom g;
+    if (!pack_geom(N, K, group, &g)) return 0;
+    return (size_t)g.bytes;
+}
+
+extern "C" int kmr_pack_int4(const uint8_t* q, const uint16_t* s, const uint16_t* z, int N, int K, int group,
+                             int flags, void* packed, size_t packed_bytes, int on_device, void* stream) {
+    return pack_run(q, s, z, N, K, group, flags, packed, packed_bytes, on_device,
+                    static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int kmr_unpack_int4(const void* packed, size_t packed_bytes, int N, int K, int group, int flags,
+                               uint8_t* q, uint16_t* s, uint16_t* z, int on_device, void* stream) {
+    return unpack_run(packed, packed_bytes, N, K, group, flags, q, s, z, on_device,
+                      static_cast<cudaStream_t>(stream));
+}
+
+// ====================================================================== standalone GEMV
+static int gemv_grid_cap() { return num_sms(); }
+
+extern "C" size_t kmr_int4_gemv_workspace_size(int N, int K, int group, int M) {
+    PackGeom g;
+    if (!pack_geom(N, K, group, &g) || M < 1) return 0;
+    return gemv_workspace_bytes(gemv_grid(g.tiles * g.ksl, gemv_grid_cap()), g.tiles);
+}
+
+extern "C" int kmr_int4_gemv(const void* packed, int N, int K, int group, int flags, const float* x, int M,
+                             float* y, int epilogue, void* workspace, size_t workspace_bytes, void* stream) {
+    PackGeom g;
+    if (!packed || !x || !y || !workspace) return KMR_ERR_INVALID_ARG;
+    if (flags & ~KMR_PACK_GATE_UP) return KMR_ERR_INVALID_ARG;
+    if (!pack_geom(N, K, group, &g) || K > 8192) return KMR_ERR_SHAPE;
+    if (M < 1 || M > kMaxBatch) return KMR_ERR_BATCH;
+    if (epilogue == KMR_EPI_SILU_MUL) {
+        if (!(flags & KMR_PACK_GATE_UP) || N % 8 != 0) return KMR_ERR_INVALID_ARG;
+    } else if (epilogue != KMR_EPI_NONE && epilogue != KMR_EPI_RESIDUAL) {
+        return KMR_ERR_INVALID_ARG;
+    }
+    const int grid = gemv_grid(g.tiles * g.ksl, gemv_grid_cap());
+    if (workspace_bytes < gemv_workspace_bytes(grid, g.tiles)) return KMR_ERR_BUFFER_SIZE;
+    if (ensure_kernel_attributes() != cudaSuccess) return KMR_ERR_CUDA;
+    int* err = standalone_error_word();
+    if (!err) return KMR_ERR_CUDA;
+    float* gpart = static_cast<float*>(workspace);
+    int* counters = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + gemv_workspace_bytes(grid, 0));
+    GemvLaunch a = {};
+    a.w = static_cast<const uint8_t*>(packed);
+    a.g = g;
+    a.in_kind = IN_F32;
+    a.x = x;
+    a.epi = epilogue == KMR_EPI_NONE ? EPI_STORE : (epilogue == KMR_EPI_RESIDUAL ? EPI_RESID : EPI_SILU);
+    a.y = y;
+    a.ldy = epilogue == KMR_EPI_SILU_MUL ? N / 2 : N;
+    const int r = enqueue_gemv(a, M, gpart, counters, err, static_cast<cudaStream_t>(stream), false, gemv_grid_cap());
+    return r < 0 ? r : KMR_OK;
+}
+
+// ====================================================================== standalone attention
+extern "C" size_t kmr_decode_attn_workspace_size(int B, int nq, int nkv, int d) {
+    if (B < 1 || nq < 1 || nkv < 1 || nq % nkv) return 0;
+    return attn_workspace_bytes(B, nq, nkv, d, 32);
+}
+
+extern "C" int kmr_decode_attn(const float* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                               const int32_t* slot_ids, const int32_t* cache_position, int B, int nq, int nkv,
+                               int d, int max_len, int slots, float scale, float* out, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    if (!q || !k_cache || !v_cache || !slot_ids || !cache_position || !out || !workspace) return KMR_ERR_INVALID_ARG;
+    if (B < 1 || B > 65535) return KMR_ERR_BATCH;
+    if (nq < 1 || nkv < 1 || nq % nkv || (nq / nkv) > 4 || (nq / nkv) == 3) return KMR_ERR_SHAPE;
+    if ((d != 64 && d != 128) || max_len < 1 || slots < 1) return KMR_ERR_SHAPE;
+    if (!(scale == scale)) return KMR_ERR_INVALID_ARG;
+    if (workspace_bytes < attn_workspace_bytes(B, nq, nkv, d, 32)) return KMR_ERR_BUFFER_SIZE;
+    if (ensure_kernel_attributes() != cudaSuccess) return KMR_ERR_CUDA;
+    int* err = standalone_error_word();
+    if (!err) return KMR_ERR_CUDA;
+    AttnParams p = {};
+    p.in = q;
+    p.in_ld = nq * d;
+    p.fused = 0;
+    p.kc = const_cast<uint16_t*>(k_cache);
+    p.vc = const_cast<uint16_t*>(v_cache);
+    p.slot_ids = slot_ids;
+    p.cpos = cache_position;
+    p.B = B;
+    p.nq = nq;
+    p.nkv = nkv;
+    p.d = d;
+    p.S = max_len;
+    p.slots = slots;
+    p.scale = scale;
+    p.tsplit = attn_default_tsplit(nkv);
+    p.out = out;
+    p.part = static_cast<float*>(workspace);
+    p.counters = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) +
+                                        attn_workspace_bytes(B, nq, nkv, d, 32) - ((size_t(B) * nkv * 4 + 15) & ~size_t(15)));
+    p.err = err;
+    return launch_attn(p, static_cast<cudaStream_t>(stream), false) == cudaSuccess ? KMR_OK : KMR_ERR_CUDA;
+}
+
+extern "C" int kmr_last_device_error(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return KMR_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_standalone_err, sizeof(int)) != cudaSuccess) return KMR_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_standalone_err, &zero, sizeof(int)) != cudaSuccess) return KMR_ERR_CUDA;
+    return v;
+}
+
+// ====================================================================== model
+namespace {
+
+struct LayerW {
+    uint8_t* w[4] = {nullptr, nullptr, nullptr, nullptr};
+    PackGeom g[4];
+    uint16_t* norm[4] = {nullptr, nullptr, nullptr, nullptr};
+    bool wl[4] = {false, false, false, false};
+    bool nl[4] = {false, false, false, false};
+};
+
+struct GraphKey {
+    int B;
+    const void* p[6];
+    bool operator==(const GraphKey& o) const {
+        if (B != o.B) return false;
+        for (int i = 0; i < 6; ++i)
+            if (p[i] != o.p[i]) return false;
+        return true;
+    }
+};
+struct GraphEntry {
+    GraphKey key;
+    cudaGraphExec_t exec;
+    unsigned long long used;
+};
+
+}  // namespace
+
+struct kmr_model {
+    kmr_model_config cfg;
+    int device = 0;
+    int sms = 0;
+    int tsplit = 1;
+    std::vector<LayerW> layers;
+    uint16_t* embed = nullptr;
+    bool embed_loaded = false;
+    uint16_t* final_norm = nullptr;
+    bool final_loaded = false;
+    uint16_t* kc = nullptr;
+    uint16_t* vc = nullptr;
+    size_t kv_layer_elems = 0;
+    float* inv_freq = nullptr;
+    float* x_resid = nullptr;
+    float* qkv = nullptr;
+    float* attn_out = nullptr;
+    float* act = nullptr;
+    float* gpart = nullptr;
+    int* gcount = nullptr;
+    float* apart = nullptr;
+    int* acount = nullptr;
+    float* hbest_v = nullptr;
+    int* hbest_i = nullptr;
+    int* hcount = nullptr;
+    int* err = nullptr;
+    // host-state staging for kmr_decode_step_host
+    uint8_t* d_state = nullptr;
+    uint8_t* h_state = nullptr;
+    float* d_logits = nullptr;
+    cudaStream_t cap = nullptr;
+    std::vector<GraphEntry> graphs;
+    unsigned long long tick = 0;
+    std::vector<void*> allocs;
+    std::mutex mu;
+};
+
+namespace {
+
+template <typename T>
+cudaError_t dalloc(kmr_model* m, T** p, size_t bytes) {
+    void* q = nullptr;
+    cudaError_t e = cudaMalloc(&q, bytes ? bytes : 16);
+    if (e != cudaSuccess) return e;
+    m->allocs.push_back(q);
+    *p = static_cast<T*>(q);
+    return cudaMemset(q, 0, bytes ? bytes : 16);
+}
+
+bool cfg_ok(const kmr_model_config& c) {
+    if (c.hidden <= 0 || c.n_q_heads <= 0 || c.n_kv_heads <= 0 || c.head_dim <= 0 || c.intermediate <= 0 ||
+        c.vocab <= 0 || c.n_layers <= 0)
+        return false;
+    if (c.group != 128) return false;
+    if (c.head_dim != 64 && c.head_dim != 128) return false;
+    if (c.n_q_heads % c.n_kv_heads) return false;
+    const int rep = c.n_q_heads / c.n_kv_heads;
+    if (rep != 1 && rep != 2 && rep != 4) return false;
+    if (c.hidden % 128 || c.intermediate % 128 || (c.n_q_heads * c.head_dim) % 128) return false;
+    if (c.hidden > 8192 || c.intermediate > 8192 || c.n_q_heads * c.head_dim > 8192) return false;
+    if (c.mrope_sections[0] < 0 || c.mrope_sections[1] < 0 || c.mrope_sections[2] < 0 ||
+        c.mrope_sections[0] + c.mrope_sections[1] + c.mrope_sections[2] != c.head_dim / 2)
+        return false;
+    if (!(c.eps >= 0.f) || !(c.rope_theta > 0.f)) return false;
+    if (c.max_len < 1 || c.slots < 1 || c.max_batch < 1 || c.max_batch > kMaxBatch) return false;
+    if (c.pad_id < 0 || c.pad_id >= c.vocab || c.eos_id < -1 || c.eos_id >= c.vocab) return false;
+    return true;
+}
+
+int linear_shape(const kmr_model_config& c, int which, int* N, int* K) {
+    switch (which) {
+        case KMR_W_QKV: *N = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim; *K = c.hidden; return 0;
+        case KMR_W_O: *N = c.hidden; *K = c.n_q_heads * c.head_dim; return 0;
+        case KMR_W_GATE_UP: *N = 2 * c.intermediate; *K = c.hidden; return 0;
+        case KMR_W_DOWN: *N = c.hidden; *K = c.intermediate; return 0;
+        default: return -1;
+    }
+}
+
+bool all_loaded(const kmr_model* m) {
+    if (!m->embed_loaded || !m->final_loaded) return false;
+    for (const LayerW& l : m->layers) {
+        for (int i = 0; i < 4; ++i)
+            if (!l.wl[i]) return false;
+        if (!l.nl[KMR_N_INPUT] || !l.nl[KMR_N_POST]) return false;
+        if (m->cfg.qk_norm && (!l.nl[KMR_N_Q] || !l.nl[KMR_N_K])) return false;
+    }
+    return true;
+}
+
+struct StepArgs {
+    int32_t* tok;
+    int32_t* pos;
+    int32_t* cpos;
+    const int32_t* slot;
+    uint8_t* fin;
+    float* logits;
+    int B;
+};
+
+// Queue the whole decode step (5 kernels per layer + the LM head) on `st`.
+int enqueue_step(kmr_model* m, const StepArgs& a, cudaStream_t st) {
+    const kmr_model_config& c = m->cfg;
+    const int B = a.B;
+    const int qd = c.n_q_heads * c.head_dim;
+    const int nqkv = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+    const int grid = m->sms;
+    bool pdl = false;   // the first kernel of the step has no kernel predecessor inside the graph
+    for (int l = 0; l < c.n_layers; ++l) {
+        LayerW& L = m->layers[l];
+        GemvLaunch g = {};
+        // fused QKV (+ input RMSNorm; layer 0 embeds the tokens)
+        g.w = L.w[KMR_W_QKV];
+        g.g = L.g[KMR_W_QKV];
+        g.in_kind = l == 0 ? IN_EMBED_NORM : IN_F32_NORM;
+        g.x = m->x_resid;
+        g.embed = m->embed;
+        g.tokens = a.tok;
+        g.vocab = c.vocab;
+        g.x_out = l == 0 ? m->x_resid : nullptr;
+        g.norm_w = L.norm[KMR_N_INPUT];
+        g.eps = c.eps;
+        g.epi = EPI_STORE;
+        g.y = m->qkv;
+        g.ldy = nqkv;
+        if (enqueue_gemv(g, B, m->gpart, m->gcount, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        pdl = true;
+        // attention (+ q/k norm, M-RoPE, KV write)
+        AttnParams ap = {};
+        ap.in = m->qkv;
+        ap.in_ld = nqkv;
+        ap.fused = 1;
+        ap.kc = m->kc + size_t(l) * m->kv_layer_elems;
+        ap.vc = m->vc + size_t(l) * m->kv_layer_elems;
+        ap.slot_ids = a.slot;
+        ap.cpos = a.cpos;
+        ap.positions = a.pos;
+        ap.pos_ld = B;
+        ap.finished = a.fin;
+        ap.qn_w = c.qk_norm ? L.norm[KMR_N_Q] : nullptr;
+        ap.kn_w = c.qk_norm ? L.norm[KMR_N_K] : nullptr;
+        ap.eps = c.eps;
+        ap.inv_freq = m->inv_freq;
+        ap.sec0 = c.mrope_sections[0];
+        ap.sec1 = c.mrope_sections[1];
+        ap.B = B;
+        ap.nq = c.n_q_heads;
+        ap.nkv = c.n_kv_heads;
+        ap.d = c.head_dim;
+        ap.S = c.max_len;
+        ap.slots = c.slots;
+        ap.scale = 1.0f / sqrtf(float(c.head_dim));
+        ap.tsplit = m->tsplit;
+        ap.out = m->attn_out;
+        ap.part = m->apart;
+        ap.counters = m->acount;
+        ap.err = m->err;
+        if (launch_attn(ap, st, pdl) != cudaSuccess) return KMR_ERR_CUDA;
+        // O projection + residual
+        g = GemvLaunch{};
+        g.w = L.w[KMR_W_O];
+        g.g = L.g[KMR_W_O];
+        g.in_kind = IN_F32;
+        g.x = m->attn_out;
+        g.epi = EPI_RESID;
+        g.y = m->x_resid;
+        g.ldy = c.hidden;
+        if (enqueue_gemv(g, B, m->gpart, m->gcount, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        // gate_up (+ post-attention RMSNorm) -> SiLU(gate) * up
+        g = GemvLaunch{};
+        g.w = L.w[KMR_W_GATE_UP];
+        g.g = L.g[KMR_W_GATE_UP];
+        g.in_kind = IN_F32_NORM;
+        g.x = m->x_resid;
+        g.norm_w = L.norm[KMR_N_POST];
+        g.eps = c.eps;
+        g.epi = EPI_SILU;
+        g.y = m->act;
+        g.ldy = c.intermediate;
+        if (enqueue_gemv(g, B, m->gpart, m->gcount, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        // down + residual
+        g = GemvLaunch{};
+        g.w = L.w[KMR_W_DOWN];
+        g.g = L.g[KMR_W_DOWN];
+        g.in_kind = IN_F32;
+        g.x = m->act;
+        g.epi = EPI_RESID;
+        g.y = m->x_resid;
+        g.ldy = c.hidden;
+        if (enqueue_gemv(g, B, m->gpart, m->gcount, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        (void)qd;
+    }
+    // final norm + LM head + argmax + finalize, in passes of at most 8 rows
+    for (int r0 = 0; r0 < B; r0 += kMaxMB) {
+        const int mr = (B - r0) < kMaxMB ? (B - r0) : kMaxMB;
+        const int MB = gemv_pick_mb(mr);
+        HeadParams hp = {};
+        hp.E = m->embed;
+        hp.V = c.vocab;
+        hp.K = c.hidden;
+        hp.tiles = (c.vocab + 7) / 8;
+        hp.M = mr;
+        hp.x = m->x_resid + size_t(r0) * c.hidden;
+        hp.norm_w = m->final_norm;
+        hp.eps = c.eps;
+        hp.logits = a.logits ? a.logits + size_t(r0) * c.vocab : nullptr;
+        hp.ldl = c.vocab;
+        hp.gbest_val = m->hbest_v;
+        hp.gbest_idx = m->hbest_i;
+        hp.counter = m->hcount;
+        hp.tokens = a.tok + r0;
+        hp.positions = a.pos + r0;
+        hp.pos_ld = B;
+        hp.cpos = a.cpos + r0;
+        hp.finished = a.fin + r0;
+        hp.eos = c.eos_id;
+        hp.pad = c.pad_id;
+        hp.max_len = c.max_len;
+        hp.err = m->err;
+        const int hgrid = grid < hp.tiles ? grid : hp.tiles;
+        const int tpc = (hp.tiles + hgrid - 1) / hgrid;
+        int nst = int((128 * 1024) / (size_t(8) * c.hidden * 2));
+        if (nst < 2) nst = 2;
+        if (nst > tpc) nst = tpc;
+        hp.nstage = nst;
+        if (launch_head(hp, MB, hgrid, st, true) != cudaSuccess) return KMR_ERR_CUDA;
+    }
+    return KMR_OK;
+}
+
+int get_graph(kmr_model* m, const StepArgs& a, cudaGraphExec_t* out) {
+    GraphKey key;
+    key.B = a.B;
+    key.p[0] = a.tok;
+    key.p[1] = a.pos;
+    key.p[2] = a.cpos;
+    key.p[3] = a.slot;
+    key.p[4] = a.fin;
+    key.p[5] = a.logits;
+    for (GraphEntry& e : m->graphs) {
+        if (e.key == key) {
+            e.used = ++m->tick;
+            *out = e.exec;
+            return KMR_OK;
+        }
+    }
+    cudaGraph_t graph = nullptr;
+    if (cudaStreamBeginCapture(m->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return KMR_ERR_CUDA;
+    const int rc = enqueue_step(m, a, m->cap);
+    const cudaError_t ec = cudaStreamEndCapture(m->cap, &graph);
+    if (rc != KMR_OK || ec != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        cudaGetLastError();
+        return rc != KMR_OK ? rc : KMR_ERR_CUDA;
+    }
+    cudaGraphExec_t exec = nullptr;
+    const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ei != cudaSuccess) return KMR_ERR_CUDA;
+    if (m->graphs.size() >= 8) {
+        size_t lru = 0;
+        for (size_t i = 1; i < m->graphs.size(); ++i)
+            if (m->graphs[i].used < m->graphs[lru].used) lru = i;
+        cudaGraphExecDestroy(m->graphs[lru].exec);
+        m->graphs.erase(m->graphs.begin() + lru);
+    }
+    m->graphs.push_back(GraphEntry{key, exec, ++m->tick});
+    *out = exec;
+    return KMR_OK;
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) cudaSetDevice(dev);
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+}  // namespace
+
+extern "C" int kmr_model_create(const kmr_model_config* cfg, kmr_model** out) {
+    if (!cfg || !out) return KMR_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!cfg_ok(*cfg)) return KMR_ERR_SHAPE;
+    kmr_model* m = new kmr_model();
+    m->cfg = *cfg;
+    const kmr_model_config& c = m->cfg;
+    auto fail = [&](int code) {
+        kmr_model_destroy(m);
+        return code;
+    };
+    if (cudaGetDevice(&m->device) != cudaSuccess) return fail(KMR_ERR_CUDA);
+    if (ensure_kernel_attributes() != cudaSuccess) return fail(KMR_ERR_CUDA);
+    m->sms = num_sms();
+    m->tsplit = attn_default_tsplit(c.n_kv_heads);
+    m->layers.resize(c.n_layers);
+    for (int l = 0; l < c.n_layers; ++l) {
+        for (int w = 0; w < 4; ++w) {
+            int N, K;
+            linear_shape(c, w, &N, &K);
+            if (!pack_geom(N, K, c.group, &m->layers[l].g[w])) return fail(KMR_ERR_SHAPE);
+            if (dalloc(m, &m->layers[l].w[w], (size_t)m->layers[l].g[w].bytes)) return fail(KMR_ERR_CUDA);
+        }
+        for (int n = 0; n < 4; ++n) {
+            const int len = n < 2 ? c.hidden : c.head_dim;
+            if (dalloc(m, &m->layers[l].norm[n], size_t(len) * 2)) return fail(KMR_ERR_CUDA);
+        }
+    }
+    const int B = c.max_batch;
+    const int nqkv = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+    size_t max_tiles = 0, max_grid = 1;
+    for (int w = 0; w < 4; ++w) {
+        const PackGeom& pg = m->layers[0].g[w];
+        max_tiles = std::max(max_tiles, size_t(pg.tiles));
+        max_grid = std::max(max_grid, size_t(gemv_grid(pg.tiles * pg.ksl, m->sms)));
+    }
+    m->kv_layer_elems = size_t(c.slots) * c.n_kv_heads * c.max_len * c.head_dim;
+    if (dalloc(m, &m->embed, size_t(c.vocab) * c.hidden * 2) || dalloc(m, &m->final_norm, size_t(c.hidden) * 2) ||
+        dalloc(m, &m->kc, m->kv_layer_elems * c.n_layers * 2) || dalloc(m, &m->vc, m->kv_layer_elems * c.n_layers * 2) ||
+        dalloc(m, &m->inv_freq, size_t(c.head_dim / 2) * 4) || dalloc(m, &m->x_resid, size_t(B) * c.hidden * 4) ||
+        dalloc(m, &m->qkv, size_t(B) * nqkv * 4) || dalloc(m, &m->attn_out, size_t(B) * c.n_q_heads * c.head_dim * 4) ||
+        dalloc(m, &m->act, size_t(B) * c.intermediate * 4) ||
+        dalloc(m, &m->gpart, max_grid * 2 * 8 * kMaxMB * 4) || dalloc(m, &m->gcount, max_tiles * 4) ||
+        dalloc(m, &m->apart, size_t(B) * c.n_q_heads * m->tsplit * (c.head_dim + 2) * 4) ||
+        dalloc(m, &m->acount, size_t(B) * c.n_kv_heads * 4) || dalloc(m, &m->hbest_v, size_t(m->sms) * kMaxMB * 4) ||
+        dalloc(m, &m->hbest_i, size_t(m->sms) * kMaxMB * 4) || dalloc(m, &m->hcount, 16) || dalloc(m, &m->err, 16) ||
+        dalloc(m, &m->d_state, size_t(B) * 32))
+        return fail(KMR_ERR_CUDA);
+    std::vector<float> inv(c.head_dim / 2);
+    for (int i = 0; i < c.head_dim / 2; ++i)
+        inv[i] = float(pow(double(c.rope_theta), -2.0 * double(i) / double(c.head_dim)));
+    if (cudaMemcpy(m->inv_freq, inv.data(), inv.size() * 4, cudaMemcpyHostToDevice)) return fail(KMR_ERR_CUDA);
+    if (cudaMallocHost(&m->h_state, size_t(B) * 32) != cudaSuccess) return fail(KMR_ERR_CUDA);
+    if (cudaStreamCreateWithFlags(&m->cap, cudaStreamNonBlocking) != cudaSuccess) return fail(KMR_ERR_CUDA);
+    if (cudaDeviceSynchronize() != cudaSuccess) return fail(KMR_ERR_CUDA);
+    *out = m;
+    return KMR_OK;
+}
+
+extern "C" int kmr_model_destroy(kmr_model* m) {
+    if (!m) return KMR_ERR_INVALID_ARG;
+    DeviceGuard dg(m->device);
+    cudaDeviceSynchronize();
+    for (GraphEntry& e : m->graphs) cudaGraphExecDestroy(e.exec);
+    for (void* p : m->allocs) cudaFree(p);
+    if (m->d_logits) cudaFree(m->d_logits);
+    if (m->h_state) cudaFreeHost(m->h_state);
+    if (m->cap) cudaStreamDestroy(m->cap);
+    delete m;
+    return KMR_OK;
+}
+
+extern "C" int kmr_model_set_linear(kmr_model* m, int layer, int which, const uint8_t* q, const uint16_t* s,
+                                    const uint16_t* z) {
+    if (!m || !q || !s || !z) return KMR_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= m->cfg.n_layers) return KMR_ERR_INVALID_ARG;
+    int N, K;
+    if (linear_shape(m->cfg, which, &N, &K)) return KMR_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(m->mu);
+    DeviceGuard dg(m->device);
+    LayerW& L = m->layers[layer];
+    const size_t nq = size_t(N) * K, ns = size_t(N) * (K / 128);
+    for (size_t i = 0; i < nq; ++i)
+        if (q[i] > 15) return KMR_ERR_INVALID_ARG;
+    uint8_t* dq = nullptr;
+    uint16_t* ds = nullptr;
+    uint16_t* dz = nullptr;
+    int rc = KMR_OK;
+    if (cudaMalloc(&dq, nq) || cudaMalloc(&ds, ns * 2) || cudaMalloc(&dz, ns * 2)) rc = KMR_ERR_CUDA;
+    if (rc == KMR_OK && (cudaMemcpy(dq, q, nq, cudaMemcpyHostToDevice) ||
+                         cudaMemcpy(ds, s, ns * 2, cudaMemcpyHostToDevice) ||
+                         cudaMemcpy(dz, z, ns * 2, cudaMemcpyHostToDevice)))
+        rc = KMR_ERR_CUDA;
+    if (rc == KMR_OK)
+        rc = pack_run(dq, ds, dz, N, K, 128, which == KMR_W_GATE_UP ? KMR_PACK_GATE_UP : 0, L.w[which],
+                      (size_t)L.g[which].bytes, 1, nullptr);
+    if (rc == KMR_OK && cudaDeviceSynchronize() != cudaSuccess) rc = KMR_ERR_CUDA;
+    cudaFree(dq);
+    cudaFree(ds);
+    cudaFree(dz);
+    if (rc == KMR_OK) L.wl[which] = true;
+    return rc;
+}
+
+extern "C" int kmr_model_set_norm(kmr_model* m, int layer, int which, const uint16_t* w) {
+    if (!m || !w) return KMR_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(m->mu);
+    DeviceGuard dg(m->device);
+    if (layer == -1) {
+        if (which != KMR_N_INPUT) return KMR_ERR_INVALID_ARG;
+        if (cudaMemcpy(m->final_norm, w, size_t(m->cfg.hidden) * 2, cudaMemcpyHostToDevice)) return KMR_ERR_CUDA;
+        m->final_loaded = true;
+        return KMR_OK;
+    }
+    if (layer < 0 || layer >= m->cfg.n_layers || which < 0 || which > 3) return KMR_ERR_INVALID_ARG;
+    const int len = which < 2 ? m->cfg.hidden : m->cfg.head_dim;
+    if (cudaMemcpy(m->layers[layer].norm[which], w, size_t(len) * 2, cudaMemcpyHostToDevice)) return KMR_ERR_CUDA;
+    m->layers[layer].nl[which] = true;
+    return KMR_OK;
+}
+
+extern "C" int kmr_model_set_embedding(kmr_model* m, const uint16_t* e) {
+    if (!m || !e) return KMR_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(m->mu);
+    DeviceGuard dg(m->device);
+    if (cudaMemcpy(m->embed, e, size_t(m->cfg.vocab) * m->cfg.hidden * 2, cudaMemcpyHostToDevice))
+        return KMR_ERR_CUDA;
+    m->embed_loaded = true;
+    return KMR_OK;
+}
+
+extern "C" int kmr_model_set_kv(kmr_model* m, int layer, int slot, int length, const uint16_t* k,
+                                const uint16_t* v) {
+    if (!m || (!k && length > 0) || (!v && length > 0)) return KMR_ERR_INVALID_ARG;
+    const kmr_model_config& c = m->cfg;
+    if (layer < 0 || layer >= c.n_layers) return KMR_ERR_INVALID_ARG;
+    if (slot < 0 || slot >= c.slots) return KMR_ERR_SLOT_RANGE;
+    if (length < 0 || length > c.max_len) return KMR_ERR_CACHE_FULL;
+    if (length == 0) return KMR_OK;
+    std::lock_guard<std::mutex> lk(m->mu);
+    DeviceGuard dg(m->device);
+    const size_t row = size_t(c.head_dim) * 2;
+    for (int h = 0; h < c.n_kv_heads; ++h) {
+        const size_t off = size_t(layer) * m->kv_layer_elems + ((size_t(slot) * c.n_kv_heads + h) * c.max_len) * c.head_dim;
+        if (cudaMemcpy(m->kc + off, k + size_t(h) * length * c.head_dim, row * length, cudaMemcpyHostToDevice) ||
+            cudaMemcpy(m->vc + off, v + size_t(h) * length * c.head_dim, row * length, cudaMemcpyHostToDevice))
+            return KMR_ERR_CUDA;
+    }
+    return KMR_OK;
+}
+
+extern "C" int kmr_model_kv_pointers(kmr_model* m, int layer, void** k, void** v) {
+    if (!m || !k || !v || layer < 0 || layer >= m->cfg.n_layers) return KMR_ERR_INVALID_ARG;
+    *k = m->kc + size_t(layer) * m->kv_layer_elems;
+    *v = m->vc + size_t(layer) * m->kv_layer_elems;
+    return KMR_OK;
+}
+
+extern "C" int kmr_decode_step(kmr_model* m, int32_t* tok, int32_t* pos, int32_t* cpos, const int32_t* slot,
+                               uint8_t* fin, int B, float* logits, void* stream) {
+    if (!m || !tok || !pos || !cpos || !slot || !fin) return KMR_ERR_INVALID_ARG;
+    if (B < 1 || B > m->cfg.max_batch) return KMR_ERR_BATCH;
+    if (!all_loaded(m)) return KMR_ERR_NO_PACK;
+    std::lock_guard<std::mutex> lk(m->mu);
+    DeviceGuard dg(m->device);
+    StepArgs a = {tok, pos, cpos, slot, fin, logits, B};
+    cudaGraphExec_t exec = nullptr;
+    const int rc = get_graph(m, a, &exec);
+    if (rc != KMR_OK) return rc;
+    return cudaGraphLaunch(exec, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KMR_OK : KMR_ERR_CUDA;
+}
+
+extern "C" int kmr_decode_step_host(kmr_model* m, int32_t* tok, int32_t* pos, int32_t* cpos, const int32_t* slot,
+                                    uint8_t* fin, int B, float* logits, void* stream) {
+    if (!m || !tok || !pos || !cpos || !slot || !fin) return KMR_ERR_INVALID_ARG;
+    const kmr_model_config& c = m->cfg;
+    if (B < 1 || B > c.max_batch) return KMR_ERR_BATCH;
+    if (!all_loaded(m)) return KMR_ERR_NO_PACK;
+    for (int b = 0; b < B; ++b) {
+        if (tok[b] < 0 || tok[b] >= c.vocab) return KMR_ERR_INVALID_ARG;
+        if (fin[b]) continue;
+        if (slot[b] < 0 || slot[b] >= c.slots) return KMR_ERR_SLOT_RANGE;
+        if (cpos[b] < 0 || cpos[b] >= c.max_len) return KMR_ERR_CACHE_FULL;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t* d_tok;
+    int32_t* d_pos;
+    int32_t* d_cpos;
+    int32_t* d_slot;
+    uint8_t* d_fin;
+    {
+        std::lock_guard<std::mutex> lk(m->mu);
+        DeviceGuard dg(m->device);
+        if (logits && !m->d_logits) {
+            void* p = nullptr;
+            if (cudaMalloc(&p, size_t(c.max_batch) * c.vocab * 4) != cudaSuccess) return KMR_ERR_CUDA;
+            m->d_logits = static_cast<float*>(p);
+        }
+        // state block: tok[Bmax] | pos[3][B] | cpos[Bmax] | slot[Bmax] | fin[Bmax]  (positions use row stride B)
+        const int Bm = c.max_batch;
+        uint8_t* h = m->h_state;
+        const size_t o_tok = 0, o_pos = size_t(Bm) * 4, o_cpos = o_pos + size_t(3) * Bm * 4,
+                     o_slot = o_cpos + size_t(Bm) * 4, o_fin = o_slot + size_t(Bm) * 4;
+        memcpy(h + o_tok, tok, size_t(B) * 4);
+        memcpy(h + o_pos, pos, size_t(3) * B * 4);
+        memcpy(h + o_cpos, cpos, size_t(B) * 4);
+        memcpy(h + o_slot, slot, size_t(B) * 4);
+        memcpy(h + o_fin, fin, size_t(B));
+        d_tok = reinterpret_cast<int32_t*>(m->d_state + o_tok);
+        d_pos = reinterpret_cast<int32_t*>(m->d_state + o_pos);
+        d_cpos = reinterpret_cast<int32_t*>(m->d_state + o_cpos);
+        d_slot = reinterpret_cast<int32_t*>(m->d_state + o_slot);
+        d_fin = m->d_state + o_fin;
+        const size_t total = o_fin + size_t(Bm);
+        if (cudaMemcpyAsync(m->d_state, h, total, cudaMemcpyHostToDevice, st) != cudaSuccess) return KMR_ERR_CUDA;
+        StepArgs a = {d_tok, d_pos, d_cpos, d_slot, d_fin, logits ? m->d_logits : nullptr, B};
+        cudaGraphExec_t exec = nullptr;
+        const int rc = get_graph(m, a, &exec);
+        if (rc != KMR_OK) return rc;
+        if (cudaGraphLaunch(exec, st) != cudaSuccess) return KMR_ERR_CUDA;
+        if (cudaMemcpyAsync(h, m->d_state, total, cudaMemcpyDeviceToHost, st) != cudaSuccess) return KMR_ERR_CUDA;
+        if (logits && cudaMemcpyAsync(logits, m->d_logits, size_t(B) * c.vocab * 4, cudaMemcpyDeviceToHost, st) !=
+                          cudaSuccess)
+            return KMR_ERR_CUDA;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return KMR_ERR_CUDA;
+        memcpy(tok, h + o_tok, size_t(B) * 4);
+        memcpy(pos, h + o_pos, size_t(3) * B * 4);
+        memcpy(cpos, h + o_cpos, size_t(B) * 4);
+        memcpy(fin, h + o_fin, size_t(B));
+    }
+    return KMR_OK;
+}
+
+extern "C" int kmr_model_sync_status(kmr_model* m, void* stream) {
+    if (!m) return KMR_ERR_INVALID_ARG;
+    DeviceGuard dg(m->device);
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KMR_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, m->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return KMR_ERR_CUDA;
+    if (v != 0 && cudaMemset(m->err, 0, sizeof(int)) != cudaSuccess) return KMR_ERR_CUDA;
+    return v;
+}
+
+extern "C" int kmr_model_kernels_per_step(const kmr_model* m, int B) {
+    if (!m || B < 1) return 0;
+    const int passes = (B + kMaxMB - 1) / kMaxMB;
+    return m->cfg.n_layers * (4 * passes + 1) + passes;
+}

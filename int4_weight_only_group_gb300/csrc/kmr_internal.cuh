@@ -1,0 +1,245 @@
+// Internal declarations shared by the library's translation units: device
+// helpers (mbarrier, bulk async copies, programmatic dependent launch, int4
+// magic-number dequantisation) and the kernel parameter blocks.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kmr.h"
+
+namespace kmr {
+
+constexpr int kThreads = 256;        // every compute kernel uses 8 warps
+constexpr int kTileRows = 8;         // rows per packed int4 tile / LM-head tile
+constexpr int kMaxMB = 8;            // rows of x per GEMV pass
+constexpr int kMaxBatch = 16;
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// Programmatic dependent launch: release the next kernel in the stream early,
+// and wait for the previous kernel's completion (and memory) before touching
+// anything it writes.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+// Bulk (non-tensor) async copy global -> shared, completion counted on an mbarrier.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* b) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(b))
+        : "memory");
+}
+// Same, with an L2 evict-first hint for data streamed exactly once (weights).
+__device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint32_t bytes, uint64_t* b,
+                                                uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(b)), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint32_t mbar_try_wait(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Bounded wait on an mbarrier phase.  Gives up after ~`limit_ns` (or 2^26
+// polls), records KMR_ERR_DEVICE_TIMEOUT and returns false; never traps.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, int* err,
+                                          uint64_t limit_ns = 2000000000ull) {
+    if (mbar_try_wait(b, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1; it < (1u << 26); ++it) {
+        if (mbar_try_wait(b, parity)) return true;
+        if ((it & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) break;
+    }
+    atomicCAS(err, 0, KMR_ERR_DEVICE_TIMEOUT);
+    return false;
+}
+
+__device__ __forceinline__ void set_error(int* err, int code) { atomicCAS(err, 0, code); }
+
+// (a & mask) | bits — one LOP3.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t mask, uint32_t bits) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(bits));
+    return d;
+}
+// acc += w.lo * x.lo + w.hi * x.hi with f16 products accumulated in f32.
+__device__ __forceinline__ void fma_f16x2_f32(float& acc, uint32_t w, uint32_t x) {
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a0, b0, %0;\n\tfma.rn.f32.f16 %0, a1, b1, %0;\n}"
+        : "+f"(acc)
+        : "r"(w), "r"(x));
+}
+// acc += w.lo * x.lo + w.hi * x.hi with bf16 products accumulated in f32.
+__device__ __forceinline__ void fma_bf16x2_f32(float& acc, uint32_t w, uint32_t x) {
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %0, a1, b1, %0;\n}"
+        : "+f"(acc)
+        : "r"(w), "r"(x));
+}
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t v) { return __uint_as_float(uint32_t(v) << 16); }
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return 0x7FC0;   // NaN
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return static_cast<uint16_t>(u >> 16);
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_sum(T v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// ------------------------------------------------------------------ packed layout
+struct PackGeom {
+    int N, K, wks, ksl, tiles, unit_bytes;
+    long long bytes;
+};
+// Returns false for unsupported shapes (group != 128, K not a multiple of 128).
+bool pack_geom(int N, int K, int group, PackGeom* g);
+
+// ------------------------------------------------------------------ GEMV
+enum InKind { IN_F32 = 0, IN_F32_NORM = 1, IN_EMBED_NORM = 2 };
+enum EpiKind { EPI_STORE = 0, EPI_RESID = 1, EPI_SILU = 2 };
+
+struct GemvParams {
+    const uint8_t* w;            // packed KMR4 units
+    int N, K, wks, ksl, tiles, units, unit_bytes;
+    int M;                       // rows in this pass (<= MB)
+    int in_kind;
+    const float* x;              // [M][K] fp32, row stride K (IN_F32*)
+    const uint16_t* embed;       // IN_EMBED_NORM: bf16 [V][K]
+    const int32_t* tokens;       //   token per row (ids outside [0, vocab) read row 0 and set KMR_ERR_INVALID_ARG)
+    int vocab;
+    float* x_out;                //   CTA 0 stores the embedded rows (fp32 [M][K]) here
+    const uint16_t* norm_w;      // bf16 [K] (IN_*_NORM)
+    float eps;
+    int epi;
+    float* y;                    // output, row stride ldy
+    int ldy;
+    float* gpart;                // [grid][2][8][MB] boundary-tile partial sums
+    int* counters;               // [tiles] arrivals per boundary tile (zero between launches)
+    int* err;
+    int nstage;                  // weight ring depth (units)
+};
+size_t gemv_smem_bytes(int MB, int K, int unit_bytes, int nstage, int units_per_cta);
+cudaError_t launch_gemv(const GemvParams& p, int MB, int grid, cudaStream_t st, bool pdl);
+int gemv_pick_mb(int M);
+// Persistent grid for a matrix of `units` units: one CTA per SM, more when a CTA
+// would otherwise hold more than 64 units (bounded shared memory per CTA).
+int gemv_grid(int units, int sms);
+int gemv_units_per_cta(int units, int grid);
+int gemv_nstage(int units, int grid, int unit_bytes);
+// workspace: gpart floats + counters ints, for grid CTAs and `tiles` tiles
+size_t gemv_workspace_bytes(int grid, int tiles);
+
+// ------------------------------------------------------------------ LM head
+struct HeadParams {
+    const uint16_t* E;           // bf16 [V][K]
+    int V, K, tiles;
+    int M;                       // rows in this pass (<= MB)
+    const float* x;              // residual rows fp32 [M][K]
+    const uint16_t* norm_w;
+    float eps;
+    float* logits;               // fp32 [M][ldl] or nullptr
+    int ldl;
+    float* gbest_val;            // [grid][MB]
+    int* gbest_idx;              // [grid][MB]
+    int* counter;                // one int (zero between launches)
+    // step state of these rows (finalize)
+    int32_t* tokens;
+    int32_t* positions;          // [3][pos_ld]
+    int pos_ld;
+    int32_t* cpos;
+    uint8_t* finished;
+    int eos, pad, max_len;
+    int* err;
+    int nstage;
+};
+size_t head_smem_bytes(int MB, int K, int nstage);
+cudaError_t launch_head(const HeadParams& p, int MB, int grid, cudaStream_t st, bool pdl);
+
+// ------------------------------------------------------------------ attention
+struct AttnParams {
+    const float* in;             // fused: raw qkv rows [B][in_ld]; plain: q rows [B][in_ld]
+    int in_ld;
+    int fused;
+    uint16_t* kc;                // bf16 [slots][nkv][S][d] (one layer)
+    uint16_t* vc;
+    const int32_t* slot_ids;
+    const int32_t* cpos;
+    const int32_t* positions;    // [3][pos_ld] (fused)
+    int pos_ld;
+    const uint8_t* finished;     // may be null (plain)
+    const uint16_t* qn_w;        // bf16 [d] or null (no q/k norm)
+    const uint16_t* kn_w;
+    float eps;
+    const float* inv_freq;       // [d/2]
+    int sec0, sec1;              // frequencies [0,sec0) follow T, [sec0, sec0+sec1) follow H, rest W
+    int B, nq, nkv, d, S, slots;
+    float scale;
+    int tsplit;                  // grid.x: largest number of splits per (row, kv head)
+    float* out;                  // [B][nq*d]
+    float* part;                 // [B][nkv][tsplit][rep][d+2]
+    int* counters;               // [B][nkv]
+    int* err;
+};
+size_t attn_smem_bytes(int d, int rep);
+cudaError_t launch_attn(const AttnParams& p, cudaStream_t st, bool pdl);
+size_t attn_workspace_bytes(int B, int nq, int nkv, int d, int tsplit);
+int attn_default_tsplit(int nkv);
+
+// ------------------------------------------------------------------ misc
+int num_sms();
+int* standalone_error_word();          // device address of the standalone-kernel error word
+cudaError_t ensure_kernel_attributes();
+
+}  // namespace kmr

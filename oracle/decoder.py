@@ -178,9 +178,9 @@ class OracleDecoder:
     """
 
     def __init__(self, cfg: ModelConfig, seed: int = 0, layers: Optional[int] = None,
-                 head_rows: Optional[slice] = None):
+                 head_rows: Optional[slice] = None, syn: Optional[SyntheticModel] = None):
         self.cfg = cfg
-        self.syn = SyntheticModel(cfg, seed)
+        self.syn = syn if syn is not None else SyntheticModel(cfg, seed)
         self.n_layers = cfg.n_layers if layers is None else layers
         self.head_rows = head_rows      # restrict the LM head to a vocab slice (bounded CPU samples)
         shape = (cfg.slots, cfg.n_kv_heads, cfg.max_len, cfg.head_dim)
@@ -283,9 +283,6 @@ class OracleDecoder:
 
 
 def initial_state(wl: Workload):
-    """(tokens, positions [3,B], cache_position, slot_ids, finished) at the first decode step."""
-    B = wl.batch
-    cpos = np.array(wl.prefill, dtype=np.int32)
-    pos = np.tile(cpos + np.array(wl.rope_delta, dtype=np.int32), (3, 1)).astype(np.int32)
-    return (np.array(wl.first_tokens, dtype=np.int32), pos, cpos,
-            np.array(wl.slot_ids, dtype=np.int32), np.zeros(B, dtype=np.uint8))
+    """The workload's first-step state (see workloads.initial_state)."""
+    from workloads import initial_state as _init
+    return _init(wl)

@@ -28,7 +28,7 @@ __all__ = [
     "ModelConfig", "tiny_config", "layer2b_config", "full2b_config",
     "f32_to_bf16_bits", "bf16_bits_to_f32", "SyntheticModel", "Workload",
     "tiny_workload", "layer2b_workload", "full2b_b1_workload", "full2b_b4_workload",
-    "BF16_NAN",
+    "BF16_NAN", "initial_state",
 ]
 
 BF16_NAN = np.uint16(0x7FC0)
@@ -126,13 +126,22 @@ class SyntheticModel:
     concatenations: qkv = [q; k; v], gate_up = [gate; up].
     """
 
-    def __init__(self, cfg: ModelConfig, seed: int = 0):
+    def __init__(self, cfg: ModelConfig, seed: int = 0, memo: bool = False):
         self.cfg = cfg
         self.seed = seed
+        self.memo = memo              # keep drawn linears (several consumers of one model)
         self._cache: Dict[str, object] = {}
 
     def linear(self, layer: int, name: str):
         key = f"L{layer}.{name}"
+        if self.memo and key in self._cache:
+            return self._cache[key]
+        out = self._draw_linear(key, name)
+        if self.memo:
+            self._cache[key] = out
+        return out
+
+    def _draw_linear(self, key: str, name: str):
         N, K = self.cfg.linear_shapes()[name]
         g = self.cfg.group
         assert K % g == 0
@@ -231,3 +240,14 @@ def full2b_b4_workload(seed: int = 0) -> Workload:
                     cfg, seed, batch=4, prefill=[300, 512, 700, 900], rope_delta=deltas,
                     slot_ids=[0, 1, 2, 3], first_tokens=_first_tokens(seed, 4, cfg.vocab, cfg.eos_id),
                     steps=128, finish_at={2: 64})
+
+
+def initial_state(wl: Workload):
+    """(tokens [B], positions [3, B], cache_position [B], slot_ids [B], finished [B]) at the
+    first decode step: the new token is written at the prefilled length and rotated at
+    that length plus the row's M-RoPE delta on all three axes."""
+    B = wl.batch
+    cpos = np.array(wl.prefill, dtype=np.int32)
+    pos = np.tile(cpos + np.array(wl.rope_delta, dtype=np.int32), (3, 1)).astype(np.int32)
+    return (np.array(wl.first_tokens, dtype=np.int32), pos, cpos,
+            np.array(wl.slot_ids, dtype=np.int32), np.zeros(B, dtype=np.uint8))
