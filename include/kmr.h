@@ -101,8 +101,10 @@ int kmr_unpack_int4(const void* packed, size_t packed_bytes, int N, int K, int g
 #define KMR_EPI_SILU_MUL  2   /* packed with KMR_PACK_GATE_UP: y[m, j] = silu(g_j) * u_j,
                                  j < N/2, g = rows [0, N/2), u = rows [N/2, N)         */
 
-/* Workspace bytes kmr_int4_gemv needs for M rows (device memory, zero-filled
- * by the caller before its first use; every successful call leaves it zeroed). */
+/* Workspace bytes kmr_int4_gemv needs for M rows (device memory).  The caller
+ * zero-fills it once before its first use; its last ceil(N/8)*4 bytes (rounded
+ * up to 16) are arrival counters that every successful call leaves zeroed, the
+ * rest is scratch.  Calls sharing one workspace must not overlap on the GPU. */
 size_t kmr_int4_gemv_workspace_size(int N, int K, int group, int M);
 
 /* Dequant-fused int4 GEMV / skinny GEMM ("kaminari", §07 int4 sidecar
@@ -119,8 +121,10 @@ int kmr_int4_gemv(const void* packed, int N, int K, int group, int flags,
                   void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------ attention */
-/* Workspace bytes kmr_decode_attn needs (device, zero-filled before first use,
- * left zeroed by every successful call). */
+/* Workspace bytes kmr_decode_attn needs (device memory).  The caller
+ * zero-fills it once before its first use; its last B*n_kv_heads*4 bytes
+ * (rounded up to 16) are arrival counters that every successful call leaves
+ * zeroed, the rest is scratch.  Calls sharing one workspace must not overlap. */
 size_t kmr_decode_attn_workspace_size(int B, int n_q_heads, int n_kv_heads, int head_dim);
 
 /* GQA decode attention of one token per row over a static, slot-addressable

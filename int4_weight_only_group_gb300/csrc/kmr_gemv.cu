@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, (MB <= 4 ? 2 : 1)) gemv_kernel(const
                     v[it][4] = b.x; v[it][5] = b.y; v[it][6] = b.z; v[it][7] = b.w;
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ss += v[it][e] * v[it][e];
+                for (int e = 0; e < 8; ++e) ss = __fmaf_rn(v[it][e], v[it][e], ss);
             }
         }
         float r = 1.f;
@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, (MB <= 4 ? 2 : 1)) gemv_kernel(const
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     float h = v[it][e];
-                    if (norm) h = h * r * bf16_to_f32(p.norm_w[sg * 8 + e]);
+                    if (norm) h = __fmul_rn(__fmul_rn(h, r), bf16_to_f32(p.norm_w[sg * 8 + e]));
                     v[it][e] = h;
                     amax = fmaxf(amax, fabsf(h));
                 }
@@ -215,12 +215,13 @@ __global__ void __launch_bounds__(kThreads, (MB <= 4 ? 2 : 1)) gemv_kernel(const
                 uint32_t hp[4];
 #pragma unroll
                 for (int e = 0; e < 8; e += 2) {
-                    const float f0 = v[it][e] * sigma * ((e & 2) ? 0.0625f : 1.f);
-                    const float f1 = v[it][e + 1] * sigma * ((e & 2) ? 0.0625f : 1.f);
+                    const float f0 = __fmul_rn(__fmul_rn(v[it][e], sigma), (e & 2) ? 0.0625f : 1.f);
+                    const float f1 = __fmul_rn(__fmul_rn(v[it][e + 1], sigma), (e & 2) ? 0.0625f : 1.f);
                     const __half a = __float2half_rn(f0), b = __float2half_rn(f1);
                     const float ra = __half2float(a), rb = __half2float(b);
-                    s1 += ra + rb;
-                    s2 += (e & 2) ? 16.f * (ra + rb) : (ra + rb);
+                    const float pr = __fadd_rn(ra, rb);
+                    s1 = __fadd_rn(s1, pr);
+                    s2 = __fadd_rn(s2, (e & 2) ? __fmul_rn(16.f, pr) : pr);
                     hp[e >> 1] = uint32_t(__half_as_ushort(a)) | (uint32_t(__half_as_ushort(b)) << 16);
                 }
                 *reinterpret_cast<uint4*>(xh + size_t(m) * K + size_t(sg) * 8) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
@@ -284,9 +285,10 @@ __global__ void __launch_bounds__(kThreads, (MB <= 4 ? 2 : 1)) gemv_kernel(const
                 dot_word<MB>(D, wq.z, xr, 2);
                 dot_word<MB>(D, wq.w, xr, 3);
                 const float sc = bf16_lo(sz), zc = bf16_hi(sz);
-                const float z8 = zc - 8.f * sc;
+                const float z8 = __fmaf_rn(-8.f, sc, zc);
 #pragma unroll
-                for (int m = 0; m < MB; ++m) acc[r][m] = (sc * (D[m] - c1[m]) + z8 * c2[m]) * is[m];
+                for (int m = 0; m < MB; ++m)
+                    acc[r][m] = __fmul_rn(__fmaf_rn(sc, __fsub_rn(D[m], c1[m]), __fmul_rn(z8, c2[m])), is[m]);
             }
         }
         // reduce-scatter the 8 row sums over the 32 lanes: lane l ends with row (l>>2)&7
@@ -385,12 +387,12 @@ __global__ void __launch_bounds__(kThreads, (MB <= 4 ? 2 : 1)) gemv_kernel(const
             const int jj = t * 4 + r;
             if (jj >= p.N / 2) continue;
             const float up = tval[size_t(tl) * RM + (r + 4) * MB + m];
-            p.y[size_t(m) * p.ldy + jj] = v / (1.f + expf(-v)) * up;
+            p.y[size_t(m) * p.ldy + jj] = __fmul_rn(__fdiv_rn(v, __fadd_rn(1.f, expf(-v))), up);
         } else {
             const int n = t * 8 + r;
             if (n >= p.N) continue;
             float* yp = p.y + size_t(m) * p.ldy + n;
-            if (p.epi == EPI_RESID) *yp += v;
+            if (p.epi == EPI_RESID) *yp = __fadd_rn(*yp, v);
             else *yp = v;
         }
     }

@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(const HeadParams 
             float ss = 0.f;
             for (int k = tid; k < K; k += kThreads) {
                 const float v = real ? p.x[size_t(m) * K + k] : 0.f;
-                ss += v * v;
+                ss = __fmaf_rn(v, v, ss);
             }
             ss = warp_sum(ss);
             consumers_sync();
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(const HeadParams 
             for (int w = 0; w < 8; ++w) tot += red2[w];
             const float r = rsqrtf(tot / float(K) + p.eps);
             for (int k = tid; k < K; k += kThreads) {
-                const float v = real ? p.x[size_t(m) * K + k] * r * bf16_to_f32(p.norm_w[k]) : 0.f;
+                const float v = real ? __fmul_rn(__fmul_rn(p.x[size_t(m) * K + k], r), bf16_to_f32(p.norm_w[k])) : 0.f;
                 xb[size_t(m) * K + k] = f32_to_bf16_rn(v);
             }
         }

@@ -69,7 +69,8 @@ def _gemv(torch, packed, N, K, x, epi=kmr.KMR_EPI_NONE, flags=0, y0=None):
     kmr.kmr_int4_gemv(packed, N, K, 128, flags, xd, M, y, epi, ws, ws_bytes, torch.cuda.current_stream())
     torch.cuda.synchronize()
     assert kmr.kmr_last_device_error() == 0
-    assert int(ws.sum().item()) == 0, "workspace must be left zeroed"
+    cnt_bytes = ((N + 7) // 8 * 4 + 15) // 16 * 16
+    assert int(ws[-cnt_bytes:].sum().item()) == 0, "arrival counters must be left zeroed"
     return y.cpu().numpy()
 
 
@@ -129,15 +130,22 @@ def test_int4_gemv_epilogues(torch):
 
 
 def test_int4_gemv_special_cases(torch):
+    # The kernel folds the 1024 magic offset, the -8 and the zero point in once per 32
+    # inputs (y = s (D - 1024 X') + (z - 8 s) X), so an all-zero weight row leaves a
+    # float32 cancellation residue of order 2^-24 * 1024 * |x'| per chunk: far below the
+    # 1e-2 bar, bounded here by 1e-4 * s * ||x||.
     N, K = 64, 1024
     q = np.full((N, K), 8, np.uint8)
     s = f32_to_bf16_bits(np.full((N, K // 128), 0.5, np.float32))
     z = np.zeros((N, K // 128), np.uint16)
     x = np.random.default_rng(0).standard_normal((3, K)).astype(np.float32)
-    assert np.all(_gemv(torch, _device_pack(torch, q, s, z), N, K, x) == 0.0)          # W = 0
+    bound = 1e-4 * 0.5 * np.linalg.norm(x, axis=1, keepdims=True)
+    y = _gemv(torch, _device_pack(torch, q, s, z), N, K, x)
+    assert np.all(np.abs(y) <= bound)                                                     # W = 0
     q[5, 777] = 9                                                                         # one code 9
     y = _gemv(torch, _device_pack(torch, q, s, z), N, K, x)
-    assert np.allclose(y[:, 5], 0.5 * x[:, 777], rtol=1e-3) and np.all(y[:, np.arange(N) != 5] == 0)
+    assert np.allclose(y[:, 5], 0.5 * x[:, 777], rtol=1e-3, atol=bound[:, 0].max())
+    assert np.all(np.abs(y[:, np.arange(N) != 5]) <= bound)
     assert np.all(_gemv(torch, _device_pack(torch, q, s, z), N, K, np.zeros((2, K), np.float32)) == 0.0)
 
 
