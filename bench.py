@@ -236,6 +236,9 @@ def run_kmr(args, rank: int, world: int) -> dict:
 
     out = {"elapsed_ms": elapsed_ms, "tokens": tokens, "setup_s": setup_s, "clocks": clk,
            "kernels_per_step": model.kernels_per_step(B), "kv_gen": kv_gen}
+    if args.skip_extras:
+        model.close()
+        return out
     # ---- dominant kernel: the int4 GEMV, timed alone on rotating copies larger than L2
     out["gemv"] = time_gemv(torch, kmr, syn, cfg, B)
     # ---- end to end through the host-buffer C ABI call
@@ -263,16 +266,14 @@ def time_gemv(torch, kmr, syn, cfg, M: int) -> dict:
         x = torch.randn((M, K), device="cuda")
         epi = kmr.KMR_EPI_SILU_MUL if name == "gate_up" else kmr.KMR_EPI_NONE
         y = torch.zeros((M, N), device="cuda")
-        ws_b = kmr.kmr_int4_gemv_workspace_size(N, K, 128, M)
-        ws = torch.zeros(ws_b, dtype=torch.uint8, device="cuda")
         for i in range(copies):
-            kmr.kmr_int4_gemv(bufs[i], N, K, 128, flags, x, M, y, epi, ws, ws_b, stream)
+            kmr.kmr_int4_gemv(bufs[i], N, K, 128, flags, x, M, y, epi, stream)
         torch.cuda.synchronize()
         reps = 200
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for i in range(reps):
-            kmr.kmr_int4_gemv(bufs[i % copies], N, K, 128, flags, x, M, y, epi, ws, ws_b, stream)
+            kmr.kmr_int4_gemv(bufs[i % copies], N, K, 128, flags, x, M, y, epi, stream)
         e1.record(stream)
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) * 1000.0 / reps
@@ -391,7 +392,11 @@ def main():
     ap.add_argument("--batch", type=int, default=1, choices=(1, 4))
     ap.add_argument("--impl", default="kmr", choices=("kmr", "reference"))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-extras", action="store_true",
+                    help="time only the decode steps (no standalone GEMV timing, e2e or CPU legs; for launch lists)")
     args = ap.parse_args()
+    if args.skip_extras:
+        args.no_cpu_baseline = True
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -409,6 +414,10 @@ def main():
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank != 0:
+        return
+    if args.skip_extras:
+        print(json.dumps({"ms_per_step": r["elapsed_ms"] / args.steps, "steps": args.steps,
+                          "kernels_per_step": r["kernels_per_step"]}))
         return
     wl = workload(args.batch)
     cfg = wl.cfg

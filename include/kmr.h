@@ -24,27 +24,30 @@
  *   - No kernel traps; every device wait is bounded and reports
  *     KMR_ERR_DEVICE_TIMEOUT instead of hanging.
  *
- * Packed int4 layout ("KMR4", version 1; the library's own, not torchao's)
+ * Packed int4 layout ("KMR4", version 2; the library's own, not torchao's)
  *   Canonical input: q uint8 [N, K] row-major with values 0..15 (row n =
  *   output feature, column k = input feature), s and z bf16 [N, K / 128].
  *   The dense weight is W[n, k] = (q[n, k] - 8) * s[n, k/128] + z[n, k/128].
- *   Packing:
- *     W_ks  = the K-slice width: the largest multiple of 128 that divides K
- *             and is <= 1024;  KSL = K / W_ks slices per row tile.
- *     Rows are grouped in tiles of 8 (N is padded to a multiple of 8 with
- *     q = 8, s = z = 0, i.e. zero weights).  With KMR_PACK_GATE_UP the
- *     canonical rows [gate (N/2); up (N/2)] are reordered so that packed tile
- *     t holds gate rows 4t..4t+3 followed by up rows 4t..4t+3.
- *     The matrix is a sequence of units (tile t, slice j), unit index
- *     t * KSL + j, each UNIT_BYTES = 4 * W_ks + W_ks / 4 bytes:
- *       bytes [0, 4*W_ks): 8 rows of W_ks/2 bytes; row r of the tile at
- *         r * W_ks/2.  Within a row, 32-bit little-endian word i covers the
- *         8 inputs k = j*W_ks + 8i + e, e = 0..7, with the nibble of e at
- *         bit offset {0, 16, 4, 20, 8, 24, 12, 28}[e].
- *       bytes [4*W_ks, UNIT_BYTES): 8 rows x (W_ks/128) groups of
- *         (s bf16, z bf16), little-endian, row-major.
- *   kmr_packed_size() = ceil(N/8) * KSL * UNIT_BYTES
- *                     = ceil(N/8)*8 * (K/2 + 4*K/128) bytes.
+ *   Packing (one 32-bit word per lane per 16x16 block: the A fragment of a
+ *   16x8x16 tensor-core product):
+ *     Rows are grouped in tiles of 16 (N is padded to a multiple of 16 with
+ *     q = 8, s = z = 0, i.e. zero weights).  With KMR_PACK_GATE_UP (N a
+ *     multiple of 16) the canonical rows [gate (N/2); up (N/2)] are reordered
+ *     so that packed tile t holds gate rows 8t..8t+7 then up rows 8t..8t+7.
+ *     A tile is K/128 consecutive groups of 1088 bytes; group gr of tile T
+ *     starts at T * (K/128) * 1088 + gr * 1088 and holds
+ *       bytes [0, 1024): for k-step ks = 0..7 (inputs k0 = 128 gr + 16 ks)
+ *         and lane l = 0..31 (g = l / 4, t = l % 4), the little-endian
+ *         32-bit word at (ks / 4) * 512 + l * 16 + (ks % 4) * 4 whose
+ *         nibbles are, by bit offset (row r of the tile, input k):
+ *            0: (g, k0+2t)     16: (g, k0+2t+1)
+ *            4: (g+8, k0+2t)   20: (g+8, k0+2t+1)
+ *            8: (g, k0+2t+8)   24: (g, k0+2t+9)
+ *           12: (g+8, k0+2t+8) 28: (g+8, k0+2t+9)
+ *       bytes [1024, 1088): for rows r = 0..15 of the tile, (s bf16, z bf16)
+ *         of group gr, little-endian, at 1024 + 4 r.
+ *   kmr_packed_size() = ceil(N/16) * (K/128) * 1088
+ *                     = ceil(N/16)*16 * (K/2 + 4*K/128) bytes.
  */
 #ifndef KMR_H_
 #define KMR_H_
@@ -71,11 +74,11 @@ extern "C" {
 /* Human-readable name of a status code (static string, never NULL). */
 const char* kmr_status_string(int status);
 
-/* Library / layout version: returns 1 for the KMR4 v1 packed layout. */
+/* Library / layout version: returns 2 for the KMR4 v2 packed layout. */
 int kmr_layout_version(void);
 
 /* ------------------------------------------------------------------ packing */
-#define KMR_PACK_GATE_UP  1   /* interleave [gate; up] halves in blocks of 4 rows */
+#define KMR_PACK_GATE_UP  1   /* interleave [gate; up] halves in blocks of 8 rows */
 
 /* Bytes of the packed form of an [N, K] int4 matrix with the given group
  * (group must be 128; K a multiple of 128).  Returns 0 for unsupported shapes. */
@@ -101,12 +104,6 @@ int kmr_unpack_int4(const void* packed, size_t packed_bytes, int N, int K, int g
 #define KMR_EPI_SILU_MUL  2   /* packed with KMR_PACK_GATE_UP: y[m, j] = silu(g_j) * u_j,
                                  j < N/2, g = rows [0, N/2), u = rows [N/2, N)         */
 
-/* Workspace bytes kmr_int4_gemv needs for M rows (device memory).  The caller
- * zero-fills it once before its first use; its last ceil(N/8)*4 bytes (rounded
- * up to 16) are arrival counters that every successful call leaves zeroed, the
- * rest is scratch.  Calls sharing one workspace must not overlap on the GPU. */
-size_t kmr_int4_gemv_workspace_size(int N, int K, int group, int M);
-
 /* Dequant-fused int4 GEMV / skinny GEMM ("kaminari", §07 int4 sidecar
  * quantization: decoder linears weight-only int4; §06 The optimization
  * ladder: decode is memory-bandwidth-bound, so the packed weights are
@@ -114,11 +111,11 @@ size_t kmr_int4_gemv_workspace_size(int N, int K, int group, int M);
  *   packed  device, KMR4 layout of W [N, K] (flags as packed)
  *   x       device fp32 [M, K] row-major, 1 <= M <= 16
  *   y       device fp32 [M, N] (or [M, N/2] for KMR_EPI_SILU_MUL), row-major
- *   The reduction order is fixed (no float atomics): results are bitwise
+ *   K <= 8192.  No workspace: each CTA owns whole 16-row tiles.  The
+ *   reduction order is fixed (no float atomics): results are bitwise
  *   reproducible and a row's result does not depend on M. */
 int kmr_int4_gemv(const void* packed, int N, int K, int group, int flags,
-                  const float* x, int M, float* y, int epilogue,
-                  void* workspace, size_t workspace_bytes, void* stream);
+                  const float* x, int M, float* y, int epilogue, void* stream);
 
 /* ------------------------------------------------------------------ attention */
 /* Workspace bytes kmr_decode_attn needs (device memory).  The caller

@@ -23,7 +23,7 @@ __all__ = [
     "KMR_PACK_GATE_UP", "KMR_EPI_NONE", "KMR_EPI_RESIDUAL", "KMR_EPI_SILU_MUL",
     "KMR_W_QKV", "KMR_W_O", "KMR_W_GATE_UP", "KMR_W_DOWN", "KMR_N_INPUT", "KMR_N_POST", "KMR_N_Q", "KMR_N_K",
     "ModelConfig", "kmr_status_string", "kmr_layout_version", "kmr_packed_size", "kmr_pack_int4",
-    "kmr_unpack_int4", "kmr_int4_gemv_workspace_size", "kmr_int4_gemv", "kmr_decode_attn_workspace_size",
+    "kmr_unpack_int4", "kmr_int4_gemv", "kmr_decode_attn_workspace_size",
     "kmr_decode_attn", "kmr_last_device_error", "Model",
 ]
 
@@ -81,8 +81,7 @@ _SIGNATURES = {
     "kmr_packed_size": (_SZ, [_I, _I, _I]),
     "kmr_pack_int4": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _SZ, _I, _P]),
     "kmr_unpack_int4": (_I, [_P, _SZ, _I, _I, _I, _I, _P, _P, _P, _I, _P]),
-    "kmr_int4_gemv_workspace_size": (_SZ, [_I, _I, _I, _I]),
-    "kmr_int4_gemv": (_I, [_P, _I, _I, _I, _I, _P, _I, _P, _I, _P, _SZ, _P]),
+    "kmr_int4_gemv": (_I, [_P, _I, _I, _I, _I, _P, _I, _P, _I, _P]),
     "kmr_decode_attn_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "kmr_decode_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _SZ, _P]),
     "kmr_last_device_error": (_I, []),
@@ -175,13 +174,9 @@ def kmr_unpack_int4(packed, packed_bytes, N, K, group, flags, q, s, z, on_device
                                  int(on_device), _stream(stream)), "kmr_unpack_int4")
 
 
-def kmr_int4_gemv_workspace_size(N, K, group, M) -> int:
-    return lib().kmr_int4_gemv_workspace_size(N, K, group, M)
-
-
-def kmr_int4_gemv(packed, N, K, group, flags, x, M, y, epilogue, workspace, workspace_bytes, stream=None) -> None:
-    _check(lib().kmr_int4_gemv(_ptr(packed), N, K, group, flags, _ptr(x), M, _ptr(y), epilogue, _ptr(workspace),
-                               workspace_bytes, _stream(stream)), "kmr_int4_gemv")
+def kmr_int4_gemv(packed, N, K, group, flags, x, M, y, epilogue, stream=None) -> None:
+    _check(lib().kmr_int4_gemv(_ptr(packed), N, K, group, flags, _ptr(x), M, _ptr(y), epilogue, _stream(stream)),
+           "kmr_int4_gemv")
 
 
 def kmr_decode_attn_workspace_size(B, nq, nkv, d) -> int:

@@ -76,11 +76,9 @@ struct GemvLaunch {
 };
 
 // Rows in passes of at most 8; returns the number of launches or a negative KMR code.
-static int enqueue_gemv(const GemvLaunch& a, int M, float* gpart, int* counters, int* err, cudaStream_t st,
-                        bool pdl, int sms) {
+static int enqueue_gemv(const GemvLaunch& a, int M, int* err, cudaStream_t st, bool pdl, int sms) {
     int launches = 0;
-    const int units = a.g.tiles * a.g.ksl;
-    const int grid = gemv_grid(units, sms);
+    const int grid = gemv_grid(a.g.tiles, sms);
     for (int r0 = 0; r0 < M; r0 += kMaxMB) {
         const int mr = (M - r0) < kMaxMB ? (M - r0) : kMaxMB;
         const int MB = gemv_pick_mb(mr);
@@ -88,11 +86,8 @@ static int enqueue_gemv(const GemvLaunch& a, int M, float* gpart, int* counters,
         p.w = a.w;
         p.N = a.g.N;
         p.K = a.g.K;
-        p.wks = a.g.wks;
-        p.ksl = a.g.ksl;
         p.tiles = a.g.tiles;
-        p.units = units;
-        p.unit_bytes = a.g.unit_bytes;
+        p.tile_bytes = a.g.tile_bytes;
         p.M = mr;
         p.in_kind = a.in_kind;
         p.x = a.x ? a.x + size_t(r0) * a.g.K : nullptr;
@@ -105,10 +100,8 @@ static int enqueue_gemv(const GemvLaunch& a, int M, float* gpart, int* counters,
         p.epi = a.epi;
         p.y = a.y + size_t(r0) * a.ldy;
         p.ldy = a.ldy;
-        p.gpart = gpart;
-        p.counters = counters;
         p.err = err;
-        p.nstage = gemv_nstage(units, grid, a.g.unit_bytes);
+        p.nstage = gemv_nstage(a.g.tiles, grid, a.g.tile_bytes);
         if (launch_gemv(p, MB, grid, st, pdl || launches > 0) != cudaSuccess) return KMR_ERR_CUDA;
         ++launches;
     }
@@ -136,7 +129,7 @@ extern "C" const char* kmr_status_string(int s) {
     }
 }
 
-extern "C" int kmr_layout_version(void) { return 1; }
+extern "C" int kmr_layout_version(void) { return 2; }
 
 extern "C" size_t kmr_packed_size(int N, int K, int group) {
     PackGeom g;
@@ -157,33 +150,21 @@ extern "C" int kmr_unpack_int4(const void* packed, size_t packed_bytes, int N, i
 }
 
 // ====================================================================== standalone GEMV
-static int gemv_grid_cap() { return num_sms(); }
-
-extern "C" size_t kmr_int4_gemv_workspace_size(int N, int K, int group, int M) {
-    PackGeom g;
-    if (!pack_geom(N, K, group, &g) || M < 1) return 0;
-    return gemv_workspace_bytes(gemv_grid(g.tiles * g.ksl, gemv_grid_cap()), g.tiles);
-}
-
 extern "C" int kmr_int4_gemv(const void* packed, int N, int K, int group, int flags, const float* x, int M,
-                             float* y, int epilogue, void* workspace, size_t workspace_bytes, void* stream) {
+                             float* y, int epilogue, void* stream) {
     PackGeom g;
-    if (!packed || !x || !y || !workspace) return KMR_ERR_INVALID_ARG;
+    if (!packed || !x || !y) return KMR_ERR_INVALID_ARG;
     if (flags & ~KMR_PACK_GATE_UP) return KMR_ERR_INVALID_ARG;
     if (!pack_geom(N, K, group, &g) || K > 8192) return KMR_ERR_SHAPE;
     if (M < 1 || M > kMaxBatch) return KMR_ERR_BATCH;
     if (epilogue == KMR_EPI_SILU_MUL) {
-        if (!(flags & KMR_PACK_GATE_UP) || N % 8 != 0) return KMR_ERR_INVALID_ARG;
+        if (!(flags & KMR_PACK_GATE_UP) || N % 16 != 0) return KMR_ERR_INVALID_ARG;
     } else if (epilogue != KMR_EPI_NONE && epilogue != KMR_EPI_RESIDUAL) {
         return KMR_ERR_INVALID_ARG;
     }
-    const int grid = gemv_grid(g.tiles * g.ksl, gemv_grid_cap());
-    if (workspace_bytes < gemv_workspace_bytes(grid, g.tiles)) return KMR_ERR_BUFFER_SIZE;
     if (ensure_kernel_attributes() != cudaSuccess) return KMR_ERR_CUDA;
     int* err = standalone_error_word();
     if (!err) return KMR_ERR_CUDA;
-    float* gpart = static_cast<float*>(workspace);
-    int* counters = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + gemv_workspace_bytes(grid, 0));
     GemvLaunch a = {};
     a.w = static_cast<const uint8_t*>(packed);
     a.g = g;
@@ -192,7 +173,7 @@ extern "C" int kmr_int4_gemv(const void* packed, int N, int K, int group, int fl
     a.epi = epilogue == KMR_EPI_NONE ? EPI_STORE : (epilogue == KMR_EPI_RESIDUAL ? EPI_RESID : EPI_SILU);
     a.y = y;
     a.ldy = epilogue == KMR_EPI_SILU_MUL ? N / 2 : N;
-    const int r = enqueue_gemv(a, M, gpart, counters, err, static_cast<cudaStream_t>(stream), false, gemv_grid_cap());
+    const int r = enqueue_gemv(a, M, err, static_cast<cudaStream_t>(stream), true, num_sms());
     return r < 0 ? r : KMR_OK;
 }
 
@@ -295,8 +276,6 @@ struct kmr_model {
     float* qkv = nullptr;
     float* attn_out = nullptr;
     float* act = nullptr;
-    float* gpart = nullptr;
-    int* gcount = nullptr;
     float* apart = nullptr;
     int* acount = nullptr;
     float* hbest_v = nullptr;
@@ -402,7 +381,7 @@ int enqueue_step(kmr_model* m, const StepArgs& a, cudaStream_t st) {
         g.epi = EPI_STORE;
         g.y = m->qkv;
         g.ldy = nqkv;
-        if (enqueue_gemv(g, B, m->gpart, m->gcount, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        if (enqueue_gemv(g, B, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
         pdl = true;
         // attention (+ q/k norm, M-RoPE, KV write)
         AttnParams ap = {};
@@ -444,7 +423,7 @@ int enqueue_step(kmr_model* m, const StepArgs& a, cudaStream_t st) {
         g.epi = EPI_RESID;
         g.y = m->x_resid;
         g.ldy = c.hidden;
-        if (enqueue_gemv(g, B, m->gpart, m->gcount, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        if (enqueue_gemv(g, B, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
         // gate_up (+ post-attention RMSNorm) -> SiLU(gate) * up
         g = GemvLaunch{};
         g.w = L.w[KMR_W_GATE_UP];
@@ -456,7 +435,7 @@ int enqueue_step(kmr_model* m, const StepArgs& a, cudaStream_t st) {
         g.epi = EPI_SILU;
         g.y = m->act;
         g.ldy = c.intermediate;
-        if (enqueue_gemv(g, B, m->gpart, m->gcount, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        if (enqueue_gemv(g, B, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
         // down + residual
         g = GemvLaunch{};
         g.w = L.w[KMR_W_DOWN];
@@ -466,7 +445,7 @@ int enqueue_step(kmr_model* m, const StepArgs& a, cudaStream_t st) {
         g.epi = EPI_RESID;
         g.y = m->x_resid;
         g.ldy = c.hidden;
-        if (enqueue_gemv(g, B, m->gpart, m->gcount, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        if (enqueue_gemv(g, B, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
         (void)qd;
     }
     // final norm + LM head + argmax + finalize, in passes of at most 8 rows
@@ -592,19 +571,12 @@ extern "C" int kmr_model_create(const kmr_model_config* cfg, kmr_model** out) {
     }
     const int B = c.max_batch;
     const int nqkv = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
-    size_t max_tiles = 0, max_grid = 1;
-    for (int w = 0; w < 4; ++w) {
-        const PackGeom& pg = m->layers[0].g[w];
-        max_tiles = std::max(max_tiles, size_t(pg.tiles));
-        max_grid = std::max(max_grid, size_t(gemv_grid(pg.tiles * pg.ksl, m->sms)));
-    }
     m->kv_layer_elems = size_t(c.slots) * c.n_kv_heads * c.max_len * c.head_dim;
     if (dalloc(m, &m->embed, size_t(c.vocab) * c.hidden * 2) || dalloc(m, &m->final_norm, size_t(c.hidden) * 2) ||
         dalloc(m, &m->kc, m->kv_layer_elems * c.n_layers * 2) || dalloc(m, &m->vc, m->kv_layer_elems * c.n_layers * 2) ||
         dalloc(m, &m->inv_freq, size_t(c.head_dim / 2) * 4) || dalloc(m, &m->x_resid, size_t(B) * c.hidden * 4) ||
         dalloc(m, &m->qkv, size_t(B) * nqkv * 4) || dalloc(m, &m->attn_out, size_t(B) * c.n_q_heads * c.head_dim * 4) ||
         dalloc(m, &m->act, size_t(B) * c.intermediate * 4) ||
-        dalloc(m, &m->gpart, max_grid * 2 * 8 * kMaxMB * 4) || dalloc(m, &m->gcount, max_tiles * 4) ||
         dalloc(m, &m->apart, size_t(B) * c.n_q_heads * m->tsplit * (c.head_dim + 2) * 4) ||
         dalloc(m, &m->acount, size_t(B) * c.n_kv_heads * 4) || dalloc(m, &m->hbest_v, size_t(m->sms) * kMaxMB * 4) ||
         dalloc(m, &m->hbest_i, size_t(m->sms) * kMaxMB * 4) || dalloc(m, &m->hcount, 16) || dalloc(m, &m->err, 16) ||

@@ -393,8 +393,11 @@ cudaError_t attn_set_attributes() {
     const void* ks[6] = {(const void*)attn_kernel<64, 1>, (const void*)attn_kernel<64, 2>,
                          (const void*)attn_kernel<64, 4>, (const void*)attn_kernel<128, 1>,
                          (const void*)attn_kernel<128, 2>, (const void*)attn_kernel<128, 4>};
-    for (const void* k : ks)
+    for (const void* k : ks) {
         if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, mx))) return e;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+    }
     return cudaSuccess;
 }
 

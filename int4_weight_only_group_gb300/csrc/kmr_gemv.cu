@@ -1,4 +1,4 @@
-// Dequant-fused int4 weight-only GEMV / skinny GEMM (M <= 8 rows per pass).
+// Dequant-fused int4 weight-only GEMV / skinny GEMM (up to 8 rows of x per pass).
 //
 // What it computes ("kaminari — a single-GPU Qwen3-VL inference engine,
 // explained", §07 int4 sidecar quantization; group 128 along K):
@@ -7,25 +7,29 @@
 // residual add or SiLU(gate) * up (epilogue).
 //
 // GB300 design
-//   * HBM-bound: every packed byte is read exactly once.  The matrix is a
-//     sequence of equal units (8 rows x one K-slice, KMR4 layout); a
-//     persistent grid of one CTA per SM takes an equal, contiguous unit range
-//     (stream-K), so small-N matrices still spread over all 152 SMs.
-//   * Weights move with cp.async.bulk into a shared-memory ring.  The first
-//     ring fill is issued BEFORE griddepcontrol.wait, so with programmatic
-//     dependent launch a kernel streams its weights while the previous kernel
-//     of the decode step is still finishing.
-//   * Dequantisation is magic-number based: a nibble OR'd into the mantissa of
-//     fp16 1024.0 gives 1024 + q exactly (or 1024 + 16q for the nibble one
-//     position higher, compensated by pre-scaling that x by 1/16).  The f16
-//     products accumulate in f32 (fma.rn.f32.f16); the 1024 offset, the -8
-//     and the zero point are folded in once per 32-input chunk using the
-//     chunk sums of x:  y = s * (D - 1024 * X') + (z - 8 s) * X.
-//   * x is staged once per CTA in shared memory as fp16 scaled by a per-row
-//     power of two (exact) so its largest magnitude sits below 2^14.
-//   * Deterministic: fixed-order warp reduce-scatter, fixed-order sums over
-//     units, and a last-arriver (atomic counter, no float atomics) combine for
-//     tiles split between CTAs.  No result depends on M or on other rows.
+//   * HBM-bound: every packed byte is read once.  A CTA owns whole 16-row
+//     tiles (no cross-CTA reduction, no global scratch) and pulls them with
+//     cp.async.bulk into a shared-memory ring whose first fill is issued
+//     BEFORE griddepcontrol.wait: under programmatic dependent launch a kernel
+//     streams its weights while the previous kernel of the step finishes.
+//   * Issue-rate bound on CUDA cores: at GB300's ~47 int4 weights per SM-clock
+//     a float FMA per weight plus the unpacking would exceed the SM's issue
+//     rate (2+ instructions per weight at batch 1, 4+ at batch 4).  The
+//     multiply-adds therefore go to the tensor cores (mma.m16n8k16, f16 in,
+//     f32 accumulate, the 16 rows of a tile as M and the batch rows as N) and
+//     the threads only unpack: the KMR4 layout stores each lane's A fragment
+//     of one 16x16 block in one 32-bit word, so 8 weights cost one shift and
+//     four LOP3s.  OR-ing a nibble into the mantissa of fp16 1024.0 gives
+//     1024 + q exactly (1024 + 16q for rows 8..15, whose nibble sits one
+//     position higher); the offset, the -8 and the zero point are folded in
+//     once per group with the group sums X of x:
+//         y = s * (D - 1024 X) / c + (z - 8 s) X,   c = 1 or 16 per row.
+//   * x is staged once per CTA in shared memory as fp16, scaled per row by a
+//     power of two (exact) so its largest magnitude sits below 2^13, in the
+//     order of the B fragments.
+//   * Deterministic and batch invariant: fixed k order inside the mma, fixed
+//     group order per warp, fixed warp order in the tile sum; a row's result
+//     never depends on the other rows or on M.
 #include <cuda_fp16.h>
 
 #include "kmr_internal.cuh"
@@ -37,91 +41,56 @@ namespace {
 __host__ __device__ inline size_t al16(size_t v) { return (v + 15) & ~size_t(15); }
 
 struct GemvSmem {
-    size_t bar, xh, xs1, xs2, isig, red, upart, tval, flags, stage, total;
+    size_t bar, xh, xs, isig, red, part, stage, total;
 };
-__host__ __device__ inline GemvSmem gemv_layout(int MB, int K, int ub, int nst, int upc) {
+// xh: MB rows of (K + 8) halves; xs: [groups][8] group sums; part: [nst][8 warps][16 rows][8 cols]
+__host__ __device__ inline GemvSmem gemv_layout(int MB, int K, int tile_bytes, int nst) {
     GemvSmem L;
     size_t o = 0;
     L.bar = o;   o += al16(size_t(nst) * 8);
-    L.xh = o;    o += al16(size_t(MB) * K * 2);
-    L.xs1 = o;   o += al16(size_t(MB) * (K / 32) * 4);
-    L.xs2 = o;   o += al16(size_t(MB) * (K / 32) * 4);
-    L.isig = o;  o += al16(size_t(MB) * 4);
+    L.xh = o;    o += al16(size_t(MB) * (K + 8) * 2);
+    L.xs = o;    o += al16(size_t(K / 128) * 8 * 4);
+    L.isig = o;  o += al16(size_t(8) * 4);
     L.red = o;   o += al16(size_t(2) * 8 * 4);
-    L.upart = o; o += al16(size_t(upc) * 8 * MB * 4);
-    L.tval = o;  o += al16(size_t(upc + 2) * 8 * MB * 4);
-    L.flags = o; o += 16;
+    L.part = o;  o += al16(size_t(nst) * 8 * 128 * 4);
     o = (o + 127) & ~size_t(127);
-    L.stage = o; o += size_t(nst) * ub;
+    L.stage = o; o += size_t(nst) * tile_bytes;
     L.total = o;
     return L;
 }
 
-__device__ __forceinline__ long long unit_start(int c, int U, int P) { return (long long)c * U / P; }
-__device__ __forceinline__ int unit_owner(long long u, int U, int P) {
-    return int(((u + 1) * (long long)P - 1) / U);
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Block-wide sum / max over 256 threads through `red` (8 floats); all threads get the result.
-__device__ __forceinline__ float block_sum(float v, float* red) {
-    v = warp_sum(v);
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
-    if (l == 0) red[w] = v;
-    __syncthreads();
-    float r = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) r += red[i];
-    return r;
-}
-__device__ __forceinline__ float block_max(float v, float* red) {
-    v = warp_max(v);
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
-    if (l == 0) red[8 + w] = v;
-    __syncthreads();
-    float r = red[8];
-#pragma unroll
-    for (int i = 1; i < 8; ++i) r = fmaxf(r, red[8 + i]);
-    return r;
-}
-
-// One 32-bit word of 8 nibbles (KMR4 bit order) against 4 fp16 pairs of x.
-template <int MB>
-__device__ __forceinline__ void dot_word(float (&D)[MB], uint32_t w, const uint32_t (*xr)[16], int j) {
-    const uint32_t w2 = w >> 8;
-    const uint32_t h0 = and_or(w, 0x000F000Fu, 0x64006400u);    // 1024 + q  (k+0, k+1)
-    const uint32_t h1 = and_or(w, 0x00F000F0u, 0x64006400u);    // 1024 + 16q (k+2, k+3)
-    const uint32_t h2 = and_or(w2, 0x000F000Fu, 0x64006400u);   // 1024 + q  (k+4, k+5)
-    const uint32_t h3 = and_or(w2, 0x00F000F0u, 0x64006400u);   // 1024 + 16q (k+6, k+7)
-#pragma unroll
-    for (int m = 0; m < MB; ++m) {
-        fma_f16x2_f32(D[m], h0, xr[m][4 * j + 0]);
-        fma_f16x2_f32(D[m], h1, xr[m][4 * j + 1]);
-        fma_f16x2_f32(D[m], h2, xr[m][4 * j + 2]);
-        fma_f16x2_f32(D[m], h3, xr[m][4 * j + 3]);
-    }
+// Position (in halves, within a row of x') of input k in B-fragment order: blocks of
+// 64 inputs; inside a block, lane slot t (16 halves) holds, for each of the 4 k-steps
+// k0 = 64*block + 16*step, the inputs (k0+2t, k0+2t+1, k0+2t+8, k0+2t+9).
+__device__ __forceinline__ int xpos(int k) {
+    const int kk = k & 15;
+    return (k >> 6) * 64 + ((kk & 7) >> 1) * 16 + ((k >> 4) & 3) * 4 + (kk >> 3) * 2 + (kk & 1);
 }
 
 template <int MB>
-__global__ void __launch_bounds__(kThreads, (MB <= 4 ? 2 : 1)) gemv_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int U = p.units, P = gridDim.x, c = blockIdx.x;
-    const int u0 = int(unit_start(c, U, P)), u1 = int(unit_start(c + 1, U, P));
-    const int nu = u1 - u0;
-    const int ub = p.unit_bytes, nst = p.nstage, K = p.K, ksl = p.ksl;
-    const int upc = (U + P - 1) / P;
-    const GemvSmem L = gemv_layout(MB, K, ub, nst, upc);
+    const int P = gridDim.x, c = blockIdx.x;
+    const int t0 = int((long long)c * p.tiles / P), t1 = int((long long)(c + 1) * p.tiles / P);
+    const int nt = t1 - t0;
+    const int K = p.K, G = K >> 7, tb = p.tile_bytes, nst = p.nstage;
+    const GemvSmem L = gemv_layout(MB, K, tb, nst);
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
     __half* xh = reinterpret_cast<__half*>(smem + L.xh);
-    float* xs1 = reinterpret_cast<float*>(smem + L.xs1);
-    float* xs2 = reinterpret_cast<float*>(smem + L.xs2);
+    float* xs = reinterpret_cast<float*>(smem + L.xs);
     float* isig = reinterpret_cast<float*>(smem + L.isig);
     float* red = reinterpret_cast<float*>(smem + L.red);
-    float* upart = reinterpret_cast<float*>(smem + L.upart);
-    float* tval = reinterpret_cast<float*>(smem + L.tval);
-    int* flags = reinterpret_cast<int*>(smem + L.flags);
+    float* part = reinterpret_cast<float*>(smem + L.part);
     uint8_t* stages = smem + L.stage;
 
     // ---- weight ring: first fill before waiting on the previous kernel
@@ -132,29 +101,33 @@ __global__ void __launch_bounds__(kThreads, (MB <= 4 ? 2 : 1)) gemv_kernel(const
     __syncthreads();
     if (tid == 0) {
         const uint64_t pol = policy_evict_first();
-        const int n0 = nu < nst ? nu : nst;
+        const int n0 = nt < nst ? nt : nst;
         for (int i = 0; i < n0; ++i) {
-            mbar_arrive_expect_tx(&bar[i], ub);
-            bulk_g2s_stream(stages + size_t(i) * ub, p.w + size_t(u0 + i) * ub, ub, &bar[i], pol);
+            mbar_arrive_expect_tx(&bar[i], tb);
+            bulk_g2s_stream(stages + size_t(i) * tb, p.w + size_t(t0 + i) * tb, tb, &bar[i], pol);
         }
     }
     pdl_launch_dependents();
     pdl_wait();
 
-    // ---- prologue: x rows -> (RMSNorm) -> fp16, scaled, with chunk sums
+    // ---- prologue: x rows -> (RMSNorm) -> fp16 (scaled) in B-fragment order, group sums
     const int segs = K >> 3;
     const int nit = (segs + kThreads - 1) / kThreads;   // <= 4 (K <= 8192)
     const bool norm = p.in_kind != IN_F32;
+    for (int i = tid; i < G * (8 - MB); i += kThreads) xs[(i / (8 - MB)) * 8 + MB + i % (8 - MB)] = 0.f;
     for (int m = 0; m < MB; ++m) {
-        const bool real = m < p.M;
+        if (m >= p.M) {
+            for (int i = tid; i < G; i += kThreads) xs[i * 8 + m] = 0.f;
+            continue;
+        }
         float v[4][8];
-        float ss = 0.f;
+        float ss = 0.f, amax = 0.f;
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
             const int sg = it * kThreads + tid;
 #pragma unroll
             for (int e = 0; e < 8; ++e) v[it][e] = 0.f;
-            if (it < nit && sg < segs && real) {
+            if (it < nit && sg < segs) {
                 if (p.in_kind == IN_EMBED_NORM) {
                     int tok = p.tokens[m];
                     if (tok < 0 || tok >= p.vocab) {
@@ -180,220 +153,152 @@ __global__ void __launch_bounds__(kThreads, (MB <= 4 ? 2 : 1)) gemv_kernel(const
                     v[it][4] = b.x; v[it][5] = b.y; v[it][6] = b.z; v[it][7] = b.w;
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ss = __fmaf_rn(v[it][e], v[it][e], ss);
-            }
-        }
-        float r = 1.f;
-        if (norm) r = rsqrtf(block_sum(ss, red) / float(K) + p.eps);
-        float amax = 0.f;
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int sg = it * kThreads + tid;
-            if (it < nit && sg < segs) {
-#pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    float h = v[it][e];
-                    if (norm) h = __fmul_rn(__fmul_rn(h, r), bf16_to_f32(p.norm_w[sg * 8 + e]));
-                    v[it][e] = h;
-                    amax = fmaxf(amax, fabsf(h));
+                    ss = __fmaf_rn(v[it][e], v[it][e], ss);
+                    if (norm) v[it][e] = __fmul_rn(v[it][e], bf16_to_f32(p.norm_w[sg * 8 + e]));
+                    amax = fmaxf(amax, fabsf(v[it][e]));
                 }
             }
         }
-        amax = block_max(amax, red);
-        float sigma = 1.f;
-        if (amax > 0.f && amax < 3.0e38f) {
-            int ex;
-            frexpf(amax, &ex);            // amax < 2^ex
-            sigma = ldexpf(1.f, max(-100, min(100, 14 - ex)));
+        // one block reduction for both the sum of squares and the largest |x * w|
+        ss = warp_sum(ss);
+        amax = warp_max(amax);
+        if (lane == 0) {
+            red[warp] = ss;
+            red[8 + warp] = amax;
         }
+        __syncthreads();
+        float tot = 0.f, mx = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            tot += red[i];
+            mx = fmaxf(mx, red[8 + i]);
+        }
+        __syncthreads();
+        const float r = norm ? rsqrtf(tot / float(K) + p.eps) : 1.f;
+        if (norm) mx = __fmul_rn(mx, r);
+        float sigma = 1.f;
+        if (mx > 0.f && mx < 3.0e38f) {
+            int ex;
+            frexpf(mx, &ex);                       // mx < 2^ex
+            sigma = ldexpf(1.f, max(-100, min(100, 13 - ex)));
+        }
+        __half* xrow = xh + size_t(m) * (K + 8);
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
             if (it >= nit) break;
             const int sg = it * kThreads + tid;
-            float s1 = 0.f, s2 = 0.f;
+            float gs = 0.f;
             if (sg < segs) {
-                uint32_t hp[4];
 #pragma unroll
                 for (int e = 0; e < 8; e += 2) {
-                    const float f0 = __fmul_rn(__fmul_rn(v[it][e], sigma), (e & 2) ? 0.0625f : 1.f);
-                    const float f1 = __fmul_rn(__fmul_rn(v[it][e + 1], sigma), (e & 2) ? 0.0625f : 1.f);
-                    const __half a = __float2half_rn(f0), b = __float2half_rn(f1);
-                    const float ra = __half2float(a), rb = __half2float(b);
-                    const float pr = __fadd_rn(ra, rb);
-                    s1 = __fadd_rn(s1, pr);
-                    s2 = __fadd_rn(s2, (e & 2) ? __fmul_rn(16.f, pr) : pr);
-                    hp[e >> 1] = uint32_t(__half_as_ushort(a)) | (uint32_t(__half_as_ushort(b)) << 16);
+                    // (x * r) * w, then the exact power-of-two scale
+                    const float f0 = norm ? __fmul_rn(v[it][e], r) : v[it][e];
+                    const float f1 = norm ? __fmul_rn(v[it][e + 1], r) : v[it][e + 1];
+                    const __half a = __float2half_rn(__fmul_rn(f0, sigma));
+                    const __half b = __float2half_rn(__fmul_rn(f1, sigma));
+                    gs = __fadd_rn(gs, __fadd_rn(__half2float(a), __half2float(b)));
+                    *reinterpret_cast<__half2*>(xrow + xpos(sg * 8 + e)) = __halves2half2(a, b);
                 }
-                *reinterpret_cast<uint4*>(xh + size_t(m) * K + size_t(sg) * 8) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
             }
-            s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-            s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
-            s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
-            s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
-            if ((tid & 3) == 0 && sg < segs) {
-                xs1[m * (K / 32) + (sg >> 2)] = s1;
-                xs2[m * (K / 32) + (sg >> 2)] = s2;
-            }
+            // 16 consecutive threads cover one group of 128 inputs
+            gs += __shfl_xor_sync(0xffffffffu, gs, 1);
+            gs += __shfl_xor_sync(0xffffffffu, gs, 2);
+            gs += __shfl_xor_sync(0xffffffffu, gs, 4);
+            gs += __shfl_xor_sync(0xffffffffu, gs, 8);
+            if ((tid & 15) == 0 && sg < segs) xs[(sg >> 4) * 8 + m] = gs;
         }
         if (tid == 0) isig[m] = 1.f / sigma;
     }
     __syncthreads();
 
-    // ---- main loop: warp w takes local units w, w+8, ...
-    const int wks = p.wks;
-    const int lanes_act = wks >> 5;
-    const int rstride = wks >> 1, szstride = (wks >> 7) * 4;
-    for (int i = warp; i < nu; i += 8) {
+    // ---- main loop: all warps on one tile at a time; warp w takes groups w, w+8, ...
+    const int g = lane >> 2, t = lane & 3;
+    const bool bload = g < p.M;
+    const __half* xrow = xh + size_t(bload ? g : 0) * (K + 8);
+    for (int i = 0; i < nt; ++i) {
         const int s = i % nst;
         mbar_wait(&bar[s], uint32_t((i / nst) & 1), p.err);
-        const uint8_t* st = stages + size_t(s) * ub;
-        const int u = u0 + i;
-        const int j = u % ksl;
-        float acc[8][MB];
+        const uint8_t* st = stages + size_t(s) * tb;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int grp = warp; grp < G; grp += 8) {
+            const uint8_t* gb = st + size_t(grp) * 1088;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
-            for (int m = 0; m < MB; ++m) acc[r][m] = 0.f;
-        if (lane < lanes_act) {
-            const int ch = j * lanes_act + lane;             // 32-input chunk index along K
-            uint32_t xr[MB][16];
-            float c1[MB], c2[MB], is[MB];
-#pragma unroll
-            for (int m = 0; m < MB; ++m) {
-                const uint4* xp = reinterpret_cast<const uint4*>(xh + size_t(m) * K + size_t(ch) * 32);
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const uint4 t = xp[q4];
-                    xr[m][4 * q4 + 0] = t.x; xr[m][4 * q4 + 1] = t.y;
-                    xr[m][4 * q4 + 2] = t.z; xr[m][4 * q4 + 3] = t.w;
+            for (int blk = 0; blk < 2; ++blk) {
+                const uint4 wq = *reinterpret_cast<const uint4*>(gb + blk * 512 + lane * 16);
+                uint4 xa = make_uint4(0, 0, 0, 0), xb = make_uint4(0, 0, 0, 0);
+                if (bload) {
+                    const uint4* xp = reinterpret_cast<const uint4*>(xrow + (grp * 2 + blk) * 64 + t * 16);
+                    xa = xp[0];
+                    xb = xp[1];
                 }
-                c1[m] = 1024.f * xs1[m * (K / 32) + ch];
-                c2[m] = xs2[m * (K / 32) + ch];
-                is[m] = isig[m];
+                const uint32_t w4[4] = {wq.x, wq.y, wq.z, wq.w};
+                const uint32_t bx[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint32_t w = w4[ks], w2 = w >> 8;
+                    mma16816(d, and_or(w, 0x000F000Fu, 0x64006400u), and_or(w, 0x00F000F0u, 0x64006400u),
+                             and_or(w2, 0x000F000Fu, 0x64006400u), and_or(w2, 0x00F000F0u, 0x64006400u),
+                             bx[2 * ks], bx[2 * ks + 1]);
+                }
             }
-            const uint8_t* wrow = st + lane * 16;
-            const uint8_t* szp = st + 4 * wks + (lane >> 2) * 4;
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const uint4 wq = *reinterpret_cast<const uint4*>(wrow + r * rstride);
-                const uint32_t sz = *reinterpret_cast<const uint32_t*>(szp + r * szstride);
-                float D[MB];
-#pragma unroll
-                for (int m = 0; m < MB; ++m) D[m] = 0.f;
-                dot_word<MB>(D, wq.x, xr, 0);
-                dot_word<MB>(D, wq.y, xr, 1);
-                dot_word<MB>(D, wq.z, xr, 2);
-                dot_word<MB>(D, wq.w, xr, 3);
-                const float sc = bf16_lo(sz), zc = bf16_hi(sz);
-                const float z8 = __fmaf_rn(-8.f, sc, zc);
-#pragma unroll
-                for (int m = 0; m < MB; ++m)
-                    acc[r][m] = __fmul_rn(__fmaf_rn(sc, __fsub_rn(D[m], c1[m]), __fmul_rn(z8, c2[m])), is[m]);
-            }
+            // fold offset, -8 and zero point: rows g (x1) and g+8 (x16), batch cols 2t, 2t+1
+            const uint32_t sz0 = *reinterpret_cast<const uint32_t*>(gb + 1024 + g * 4);
+            const uint32_t sz1 = *reinterpret_cast<const uint32_t*>(gb + 1024 + (g + 8) * 4);
+            const float2 X = *reinterpret_cast<const float2*>(xs + grp * 8 + 2 * t);
+            const float s0 = bf16_lo(sz0), z0 = bf16_hi(sz0), s1 = bf16_lo(sz1), z1 = bf16_hi(sz1);
+            const float s1c = __fmul_rn(s1, 0.0625f);
+            const float zz0 = __fmaf_rn(-8.f, s0, z0), zz1 = __fmaf_rn(-8.f, s1, z1);
+            const float x0 = 1024.f * X.x, x1 = 1024.f * X.y;
+            acc[0] = __fadd_rn(acc[0], __fmaf_rn(s0, __fsub_rn(d[0], x0), __fmul_rn(zz0, X.x)));
+            acc[1] = __fadd_rn(acc[1], __fmaf_rn(s0, __fsub_rn(d[1], x1), __fmul_rn(zz0, X.y)));
+            acc[2] = __fadd_rn(acc[2], __fmaf_rn(s1c, __fsub_rn(d[2], x0), __fmul_rn(zz1, X.x)));
+            acc[3] = __fadd_rn(acc[3], __fmaf_rn(s1c, __fsub_rn(d[3], x1), __fmul_rn(zz1, X.y)));
         }
-        // reduce-scatter the 8 row sums over the 32 lanes: lane l ends with row (l>>2)&7
-        const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-        const int row = (lane >> 2) & 7;
-#pragma unroll
-        for (int m = 0; m < MB; ++m) {
-            float a[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float keep = b4 ? acc[q + 4][m] : acc[q][m];
-                const float send = b4 ? acc[q][m] : acc[q + 4][m];
-                a[q] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-            }
-            float cc[2];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const float keep = b3 ? a[q + 2] : a[q];
-                const float send = b3 ? a[q] : a[q + 2];
-                cc[q] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-            }
-            float e = (b2 ? cc[1] : cc[0]) + __shfl_xor_sync(0xffffffffu, b2 ? cc[0] : cc[1], 4);
-            e += __shfl_xor_sync(0xffffffffu, e, 2);
-            e += __shfl_xor_sync(0xffffffffu, e, 1);
-            if ((lane & 3) == 0) upart[(size_t(i) * 8 + row) * MB + m] = e;
-        }
-        __syncwarp();
-        if (lane == 0 && i + nst < nu) {
+        float* wp = part + (size_t(s) * 8 + warp) * 128;
+        wp[g * 8 + 2 * t] = acc[0];
+        wp[g * 8 + 2 * t + 1] = acc[1];
+        wp[(g + 8) * 8 + 2 * t] = acc[2];
+        wp[(g + 8) * 8 + 2 * t + 1] = acc[3];
+        __syncthreads();
+        // stage s is free again: refill it with tile i + nst while the epilogue runs
+        if (tid == 0 && i + nst < nt) {
             fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&bar[s], ub);
-            bulk_g2s_stream(stages + size_t(s) * ub, p.w + size_t(u0 + i + nst) * ub, ub, &bar[s],
+            mbar_arrive_expect_tx(&bar[s], tb);
+            bulk_g2s_stream(stages + size_t(s) * tb, p.w + size_t(t0 + i + nst) * tb, tb, &bar[s],
                             policy_evict_first());
         }
-    }
-    __syncthreads();
-    if (nu <= 0) return;
-
-    // ---- per-tile sums (fixed order over the CTA's units of each tile)
-    const int t_first = u0 / ksl, t_last = (u1 - 1) / ksl, ntl = t_last - t_first + 1;
-    const int RM = 8 * MB;
-    auto tile_full = [&](int tl) {
-        const int t = t_first + tl;
-        return u0 <= t * ksl && u1 >= t * ksl + ksl;
-    };
-    for (int idx = tid; idx < ntl * RM; idx += kThreads) {
-        const int tl = idx / RM, rm = idx % RM, t = t_first + tl;
-        const int ua = max(u0, t * ksl), ue = min(u1, t * ksl + ksl);
-        float v = 0.f;
-        for (int uu = ua; uu < ue; ++uu) v += upart[size_t(uu - u0) * RM + rm];
-        if (tile_full(tl)) tval[size_t(tl) * RM + rm] = v;
-        else p.gpart[(size_t(c) * 2 + (tl == 0 ? 0 : 1)) * RM + rm] = v;
-    }
-    __threadfence();
-    __syncthreads();
-    // ---- tiles shared with neighbouring CTAs: the last to arrive combines them
-    if (tid < 2) {
-        int last = 0;
-        const int tl = tid == 0 ? 0 : ntl - 1;
-        if ((tid == 0 || ntl > 1) && !tile_full(tl)) {
-            const int t = t_first + tl;
-            const int c_lo = unit_owner((long long)t * ksl, U, P), c_hi = unit_owner((long long)t * ksl + ksl - 1, U, P);
-            __threadfence();
-            const int old = atomicAdd(&p.counters[t], 1);
-            if (old == c_hi - c_lo) {
-                last = 1;
-                p.counters[t] = 0;
-                __threadfence();
-            }
-        }
-        flags[tid] = last;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-        if (!flags[b]) continue;
-        const int tl = b == 0 ? 0 : ntl - 1, t = t_first + tl;
-        const int c_lo = unit_owner((long long)t * ksl, U, P), c_hi = unit_owner((long long)t * ksl + ksl - 1, U, P);
-        for (int rm = tid; rm < RM; rm += kThreads) {
-            float v = 0.f;
-            for (int cc = c_lo; cc <= c_hi; ++cc) {
-                const int slot = (int(unit_start(cc, U, P)) / ksl == t) ? 0 : 1;
-                v += __ldcg(&p.gpart[(size_t(cc) * 2 + slot) * RM + rm]);
-            }
-            tval[size_t(tl) * RM + rm] = v;
-        }
-    }
-    __syncthreads();
-    // ---- epilogue on every tile this CTA completed
-    for (int idx = tid; idx < ntl * RM; idx += kThreads) {
-        const int tl = idx / RM, rm = idx % RM, r = rm / MB, m = rm % MB, t = t_first + tl;
-        const bool ready = tile_full(tl) || (tl == 0 && flags[0]) || (tl == ntl - 1 && ntl > 1 && flags[1]);
-        if (!ready || m >= p.M) continue;
-        const float v = tval[size_t(tl) * RM + rm];
+        // ---- epilogue: fixed-order sum over the 8 warps
+        const int tile = t0 + i;
+        const float* ps = part + size_t(s) * 8 * 128;
         if (p.epi == EPI_SILU) {
-            if (r >= 4) continue;
-            const int jj = t * 4 + r;
-            if (jj >= p.N / 2) continue;
-            const float up = tval[size_t(tl) * RM + (r + 4) * MB + m];
-            p.y[size_t(m) * p.ldy + jj] = __fmul_rn(__fdiv_rn(v, __fadd_rn(1.f, expf(-v))), up);
-        } else {
-            const int n = t * 8 + r;
-            if (n >= p.N) continue;
-            float* yp = p.y + size_t(m) * p.ldy + n;
-            if (p.epi == EPI_RESID) *yp = __fadd_rn(*yp, v);
-            else *yp = v;
+            if (tid < 8 * MB) {
+                const int j = tid / MB, m = tid % MB;
+                const int jj = tile * 8 + j;
+                if (m < p.M && jj < p.N / 2) {
+                    float gv = 0.f, uv = 0.f;
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        gv = __fadd_rn(gv, ps[w * 128 + j * 8 + m]);
+                        uv = __fadd_rn(uv, ps[w * 128 + (j + 8) * 8 + m]);
+                    }
+                    gv = __fmul_rn(gv, isig[m]);
+                    uv = __fmul_rn(uv, isig[m]);
+                    p.y[size_t(m) * p.ldy + jj] = __fmul_rn(__fdiv_rn(gv, __fadd_rn(1.f, expf(-gv))), uv);
+                }
+            }
+        } else if (tid < 16 * MB) {
+            const int r = tid / MB, m = tid % MB;
+            const int n = tile * 16 + r;
+            if (m < p.M && n < p.N) {
+                float v = 0.f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) v = __fadd_rn(v, ps[w * 128 + r * 8 + m]);
+                v = __fmul_rn(v, isig[m]);
+                float* yp = p.y + size_t(m) * p.ldy + n;
+                *yp = (p.epi == EPI_RESID) ? __fadd_rn(*yp, v) : v;
+            }
         }
     }
 }
@@ -401,36 +306,32 @@ __global__ void __launch_bounds__(kThreads, (MB <= 4 ? 2 : 1)) gemv_kernel(const
 }  // namespace
 
 int gemv_pick_mb(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
-int gemv_grid(int units, int sms) {
-    constexpr int kMaxUnitsPerCta = 64;
-    int g = sms < 1 ? 1 : sms;
-    if ((units + g - 1) / g > kMaxUnitsPerCta) g = (units + kMaxUnitsPerCta - 1) / kMaxUnitsPerCta;
-    if (g > units) g = units;
+
+// At most one CTA per SM, each owning ceil(tiles / SMs) whole tiles (the last
+// CTA may own fewer), never more CTAs than tiles.
+int gemv_grid(int tiles, int sms) {
+    if (sms < 1) sms = 1;
+    const int tpc = (tiles + sms - 1) / sms;
+    const int g = (tiles + tpc - 1) / tpc;
     return g < 1 ? 1 : g;
 }
-int gemv_units_per_cta(int units, int grid) { return (units + grid - 1) / grid; }
-int gemv_nstage(int units, int grid, int unit_bytes) {
-    const int upc = gemv_units_per_cta(units, grid);
-    int cap = (96 * 1024) / unit_bytes;
+int gemv_nstage(int tiles, int grid, int tile_bytes) {
+    const int tpc = (tiles + grid - 1) / grid;
+    int cap = (104 * 1024) / tile_bytes;
     if (cap < 2) cap = 2;
-    const int n = upc < cap ? upc : cap;
+    const int n = tpc < cap ? tpc : cap;
     return n < 1 ? 1 : n;
 }
-size_t gemv_smem_bytes(int MB, int K, int unit_bytes, int nstage, int upc) {
-    return gemv_layout(MB, K, unit_bytes, nstage, upc).total;
-}
-size_t gemv_workspace_bytes(int grid, int tiles) {
-    return al16(size_t(grid) * 2 * 8 * kMaxMB * sizeof(float)) + al16(size_t(tiles) * sizeof(int));
+size_t gemv_smem_bytes(int MB, int K, int tile_bytes, int nstage) {
+    return gemv_layout(MB, K, tile_bytes, nstage).total;
 }
 
 template <int MB>
 static cudaError_t launch_mb(const GemvParams& p, int grid, cudaStream_t st, bool pdl) {
-    const int upc = gemv_units_per_cta(p.units, grid);
-    const size_t smem = gemv_smem_bytes(MB, p.K, p.unit_bytes, p.nstage, upc);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = gemv_smem_bytes(MB, p.K, p.tile_bytes, p.nstage);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -451,11 +352,15 @@ cudaError_t launch_gemv(const GemvParams& p, int MB, int grid, cudaStream_t st, 
 
 cudaError_t gemv_set_attributes() {
     const int mx = 227 * 1024;
-    cudaError_t e;
-    if ((e = cudaFuncSetAttribute(gemv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx))) return e;
-    if ((e = cudaFuncSetAttribute(gemv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx))) return e;
-    if ((e = cudaFuncSetAttribute(gemv_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx))) return e;
-    return cudaFuncSetAttribute(gemv_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    const void* ks[4] = {(const void*)gemv_kernel<1>, (const void*)gemv_kernel<2>, (const void*)gemv_kernel<4>,
+                         (const void*)gemv_kernel<8>};
+    for (const void* k : ks) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace kmr

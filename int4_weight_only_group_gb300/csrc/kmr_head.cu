@@ -300,11 +300,15 @@ cudaError_t launch_head(const HeadParams& p, int MB, int grid, cudaStream_t st, 
 
 cudaError_t head_set_attributes() {
     const int mx = 227 * 1024;
-    cudaError_t e;
-    if ((e = cudaFuncSetAttribute(head_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx))) return e;
-    if ((e = cudaFuncSetAttribute(head_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx))) return e;
-    if ((e = cudaFuncSetAttribute(head_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx))) return e;
-    return cudaFuncSetAttribute(head_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    const void* ks[4] = {(const void*)head_kernel<1>, (const void*)head_kernel<2>, (const void*)head_kernel<4>,
+                         (const void*)head_kernel<8>};
+    for (const void* k : ks) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace kmr

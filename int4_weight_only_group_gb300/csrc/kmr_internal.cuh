@@ -140,9 +140,10 @@ __device__ __forceinline__ float warp_max(float v) {
 
 // ------------------------------------------------------------------ packed layout
 struct PackGeom {
-    int N, K, wks, ksl, tiles, unit_bytes;
+    int N, K, groups, tiles, tile_bytes;   // 16-row tiles, groups of 128 inputs
     long long bytes;
 };
+constexpr int kGroupBytes = 1088;          // one (tile, group): 1024 B of nibbles + 16 x (s, z)
 // Returns false for unsupported shapes (group != 128, K not a multiple of 128).
 bool pack_geom(int N, int K, int group, PackGeom* g);
 
@@ -151,9 +152,9 @@ enum InKind { IN_F32 = 0, IN_F32_NORM = 1, IN_EMBED_NORM = 2 };
 enum EpiKind { EPI_STORE = 0, EPI_RESID = 1, EPI_SILU = 2 };
 
 struct GemvParams {
-    const uint8_t* w;            // packed KMR4 units
-    int N, K, wks, ksl, tiles, units, unit_bytes;
-    int M;                       // rows in this pass (<= MB)
+    const uint8_t* w;            // packed KMR4 tiles
+    int N, K, tiles, tile_bytes;
+    int M;                       // rows of x in this pass (<= MB <= 8)
     int in_kind;
     const float* x;              // [M][K] fp32, row stride K (IN_F32*)
     const uint16_t* embed;       // IN_EMBED_NORM: bf16 [V][K]
@@ -165,21 +166,15 @@ struct GemvParams {
     int epi;
     float* y;                    // output, row stride ldy
     int ldy;
-    float* gpart;                // [grid][2][8][MB] boundary-tile partial sums
-    int* counters;               // [tiles] arrivals per boundary tile (zero between launches)
     int* err;
-    int nstage;                  // weight ring depth (units)
+    int nstage;                  // weight ring depth (tiles)
 };
-size_t gemv_smem_bytes(int MB, int K, int unit_bytes, int nstage, int units_per_cta);
+size_t gemv_smem_bytes(int MB, int K, int tile_bytes, int nstage);
 cudaError_t launch_gemv(const GemvParams& p, int MB, int grid, cudaStream_t st, bool pdl);
 int gemv_pick_mb(int M);
-// Persistent grid for a matrix of `units` units: one CTA per SM, more when a CTA
-// would otherwise hold more than 64 units (bounded shared memory per CTA).
-int gemv_grid(int units, int sms);
-int gemv_units_per_cta(int units, int grid);
-int gemv_nstage(int units, int grid, int unit_bytes);
-// workspace: gpart floats + counters ints, for grid CTAs and `tiles` tiles
-size_t gemv_workspace_bytes(int grid, int tiles);
+// At most one CTA per SM, each owning an equal count of whole 16-row tiles.
+int gemv_grid(int tiles, int sms);
+int gemv_nstage(int tiles, int grid, int tile_bytes);
 
 // ------------------------------------------------------------------ LM head
 struct HeadParams {

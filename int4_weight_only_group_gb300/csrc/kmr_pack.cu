@@ -1,5 +1,5 @@
 // KMR4 packing of canonical int4 weights (q codes, bf16 scale / zero per
-// group of 128 along K) into the unit layout the GEMV streams, and back.
+// group of 128 along K) into the tile layout the GEMV streams, and back.
 // The layout is specified in kmr.h; this file is its only implementation in
 // the library (host loop and a device kernel that produce identical bytes).
 #include <string.h>
@@ -8,114 +8,122 @@
 
 namespace kmr {
 
-static const int kBitOff[8] = {0, 16, 4, 20, 8, 24, 12, 28};
-__constant__ int c_bitoff[8] = {0, 16, 4, 20, 8, 24, 12, 28};
-
 bool pack_geom(int N, int K, int group, PackGeom* g) {
     if (group != 128 || N <= 0 || K <= 0 || K % 128 != 0) return false;
-    int wks = 0;
-    for (int w = 1024; w >= 128; w -= 128)
-        if (K % w == 0) { wks = w; break; }
     g->N = N;
     g->K = K;
-    g->wks = wks;
-    g->ksl = K / wks;
-    g->tiles = (N + 7) / 8;
-    g->unit_bytes = 4 * wks + wks / 4;
-    g->bytes = (long long)g->tiles * g->ksl * g->unit_bytes;
+    g->groups = K / 128;
+    g->tiles = (N + 15) / 16;
+    g->tile_bytes = g->groups * kGroupBytes;
+    g->bytes = (long long)g->tiles * g->tile_bytes;
     return true;
 }
 
 // Canonical row held by packed row p (-1: padding row).
 __host__ __device__ static inline int canon_row(int p, int N, int gate_up) {
     if (!gate_up) return p < N ? p : -1;
-    const int t = p >> 3, r = p & 7, half = N >> 1;
-    return r < 4 ? 4 * t + r : half + 4 * t + (r - 4);
+    const int t = p >> 4, r = p & 15, half = N >> 1;
+    return r < 8 ? 8 * t + r : half + 8 * t + (r - 8);
+}
+
+// The 32-bit word of lane l, k-step ks of group gr in tile T: the lane's mma A
+// fragment of that 16x16 block.  g = l / 4, t = l % 4, k0 = 128 gr + 16 ks:
+//   bits  0-3 (g, k0+2t)      16-19 (g, k0+2t+1)
+//   bits  4-7 (g+8, k0+2t)    20-23 (g+8, k0+2t+1)
+//   bits  8-11 (g, k0+2t+8)   24-27 (g, k0+2t+9)
+//   bits 12-15 (g+8, k0+2t+8) 28-31 (g+8, k0+2t+9)
+// stored at T * tile_bytes + gr * 1088 + (ks / 4) * 512 + l * 16 + (ks % 4) * 4.
+__host__ __device__ static inline uint32_t code_at(const uint8_t* q, int N, int K, int gate_up, int prow, int k) {
+    const int n = canon_row(prow, N, gate_up);
+    return n < 0 ? 8u : (uint32_t(q[(size_t)n * K + k]) & 15u);
+}
+__host__ __device__ static inline uint32_t pack_word(const uint8_t* q, int N, int K, int gate_up, int T, int gr,
+                                                     int ks, int l) {
+    const int g = l >> 2, t = l & 3, k0 = gr * 128 + ks * 16;
+    const int r0 = T * 16 + g, r1 = r0 + 8;
+    return code_at(q, N, K, gate_up, r0, k0 + 2 * t) | code_at(q, N, K, gate_up, r0, k0 + 2 * t + 1) << 16 |
+           code_at(q, N, K, gate_up, r1, k0 + 2 * t) << 4 | code_at(q, N, K, gate_up, r1, k0 + 2 * t + 1) << 20 |
+           code_at(q, N, K, gate_up, r0, k0 + 2 * t + 8) << 8 | code_at(q, N, K, gate_up, r0, k0 + 2 * t + 9) << 24 |
+           code_at(q, N, K, gate_up, r1, k0 + 2 * t + 8) << 12 | code_at(q, N, K, gate_up, r1, k0 + 2 * t + 9) << 28;
+}
+__host__ __device__ static inline size_t word_offset(const PackGeom& g, int T, int gr, int ks, int l) {
+    return (size_t)T * g.tile_bytes + (size_t)gr * kGroupBytes + (ks >> 2) * 512 + l * 16 + (ks & 3) * 4;
+}
+__host__ __device__ static inline void unpack_word(uint32_t w, uint8_t* q, int N, int K, int gate_up, int T, int gr,
+                                                   int ks, int l) {
+    const int g = l >> 2, t = l & 3, k0 = gr * 128 + ks * 16;
+    const int rows[2] = {T * 16 + g, T * 16 + g + 8};
+    const int sh[2][4] = {{0, 16, 8, 24}, {4, 20, 12, 28}};
+    const int kk[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+    for (int h = 0; h < 2; ++h) {
+        const int n = canon_row(rows[h], N, gate_up);
+        if (n < 0) continue;
+        for (int e = 0; e < 4; ++e) q[(size_t)n * K + k0 + kk[e]] = uint8_t((w >> sh[h][e]) & 15u);
+    }
 }
 
 // ------------------------------------------------------------------ host
 static void pack_host(const uint8_t* q, const uint16_t* s, const uint16_t* z, const PackGeom& g, int gate_up,
                       uint8_t* out) {
-    const int W = g.wks, G = W / 128, KG = g.K / 128;
-    for (int p = 0; p < g.tiles * 8; ++p) {
-        const int n = canon_row(p, g.N, gate_up);
-        const int t = p >> 3, r = p & 7;
-        for (int j = 0; j < g.ksl; ++j) {
-            uint8_t* unit = out + ((size_t)t * g.ksl + j) * g.unit_bytes;
-            uint8_t* rowp = unit + (size_t)r * (W / 2);
-            for (int i = 0; i < W / 8; ++i) {
-                uint32_t word = 0;
-                for (int e = 0; e < 8; ++e) {
-                    const uint32_t code = n < 0 ? 8u : q[(size_t)n * g.K + (size_t)j * W + 8 * i + e];
-                    word |= code << kBitOff[e];
+    for (int T = 0; T < g.tiles; ++T)
+        for (int gr = 0; gr < g.groups; ++gr) {
+            for (int ks = 0; ks < 8; ++ks)
+                for (int l = 0; l < 32; ++l) {
+                    const uint32_t w = pack_word(q, g.N, g.K, gate_up, T, gr, ks, l);
+                    memcpy(out + word_offset(g, T, gr, ks, l), &w, 4);   // little-endian host
                 }
-                memcpy(rowp + 4 * i, &word, 4);   // little-endian host
-            }
-            uint8_t* szp = unit + 4 * W + (size_t)r * G * 4;
-            for (int gl = 0; gl < G; ++gl) {
-                const uint16_t sv = n < 0 ? 0 : s[(size_t)n * KG + j * G + gl];
-                const uint16_t zv = n < 0 ? 0 : z[(size_t)n * KG + j * G + gl];
-                memcpy(szp + 4 * gl, &sv, 2);
-                memcpy(szp + 4 * gl + 2, &zv, 2);
+            uint8_t* szp = out + (size_t)T * g.tile_bytes + (size_t)gr * kGroupBytes + 1024;
+            for (int r = 0; r < 16; ++r) {
+                const int n = canon_row(T * 16 + r, g.N, gate_up);
+                const uint16_t sv = n < 0 ? 0 : s[(size_t)n * g.groups + gr];
+                const uint16_t zv = n < 0 ? 0 : z[(size_t)n * g.groups + gr];
+                memcpy(szp + 4 * r, &sv, 2);
+                memcpy(szp + 4 * r + 2, &zv, 2);
             }
         }
-    }
 }
 
 static void unpack_host(const uint8_t* in, const PackGeom& g, int gate_up, uint8_t* q, uint16_t* s, uint16_t* z) {
-    const int W = g.wks, G = W / 128, KG = g.K / 128;
-    for (int p = 0; p < g.tiles * 8; ++p) {
-        const int n = canon_row(p, g.N, gate_up);
-        if (n < 0) continue;
-        const int t = p >> 3, r = p & 7;
-        for (int j = 0; j < g.ksl; ++j) {
-            const uint8_t* unit = in + ((size_t)t * g.ksl + j) * g.unit_bytes;
-            const uint8_t* rowp = unit + (size_t)r * (W / 2);
-            for (int i = 0; i < W / 8; ++i) {
-                uint32_t word;
-                memcpy(&word, rowp + 4 * i, 4);
-                for (int e = 0; e < 8; ++e) q[(size_t)n * g.K + (size_t)j * W + 8 * i + e] = (word >> kBitOff[e]) & 15u;
-            }
-            const uint8_t* szp = unit + 4 * W + (size_t)r * G * 4;
-            for (int gl = 0; gl < G; ++gl) {
-                memcpy(&s[(size_t)n * KG + j * G + gl], szp + 4 * gl, 2);
-                memcpy(&z[(size_t)n * KG + j * G + gl], szp + 4 * gl + 2, 2);
+    for (int T = 0; T < g.tiles; ++T)
+        for (int gr = 0; gr < g.groups; ++gr) {
+            for (int ks = 0; ks < 8; ++ks)
+                for (int l = 0; l < 32; ++l) {
+                    uint32_t w;
+                    memcpy(&w, in + word_offset(g, T, gr, ks, l), 4);
+                    unpack_word(w, q, g.N, g.K, gate_up, T, gr, ks, l);
+                }
+            const uint8_t* szp = in + (size_t)T * g.tile_bytes + (size_t)gr * kGroupBytes + 1024;
+            for (int r = 0; r < 16; ++r) {
+                const int n = canon_row(T * 16 + r, g.N, gate_up);
+                if (n < 0) continue;
+                memcpy(&s[(size_t)n * g.groups + gr], szp + 4 * r, 2);
+                memcpy(&z[(size_t)n * g.groups + gr], szp + 4 * r + 2, 2);
             }
         }
-    }
 }
 
 // ------------------------------------------------------------------ device
-// One thread per packed 32-bit nibble word, plus one per (row, group) scale/zero pair.
+// One thread per packed word, plus one per (row, group) scale/zero pair.
 __global__ void pack_kernel(const uint8_t* __restrict__ q, const uint16_t* __restrict__ s,
                             const uint16_t* __restrict__ z, PackGeom g, int gate_up, uint8_t* __restrict__ out) {
-    const int W = g.wks, G = W / 128, KG = g.K / 128, wpr = g.K / 8;   // words per packed row
-    const long long nwords = (long long)g.tiles * 8 * wpr;
-    const long long nsz = (long long)g.tiles * 8 * KG;
+    const long long nwords = (long long)g.tiles * g.groups * 256;
+    const long long nsz = (long long)g.tiles * g.groups * 16;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < nwords + nsz;
          idx += (long long)gridDim.x * blockDim.x) {
         if (idx < nwords) {
-            const int p = int(idx / wpr), wi = int(idx % wpr);
-            const int n = canon_row(p, g.N, gate_up);
-            const int j = (wi * 8) / W, i = wi - j * (W / 8);
-            uint32_t word = 0;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uint32_t code = n < 0 ? 8u : (q[(size_t)n * g.K + (size_t)wi * 8 + e] & 15u);
-                word |= code << c_bitoff[e];
-            }
-            const int t = p >> 3, r = p & 7;
-            *reinterpret_cast<uint32_t*>(out + ((size_t)t * g.ksl + j) * g.unit_bytes + (size_t)r * (W / 2) + 4 * i) =
-                word;
+            const int l = int(idx & 31), ks = int((idx >> 5) & 7);
+            const long long tg = idx >> 8;
+            const int gr = int(tg % g.groups), T = int(tg / g.groups);
+            *reinterpret_cast<uint32_t*>(out + word_offset(g, T, gr, ks, l)) = pack_word(q, g.N, g.K, gate_up, T, gr, ks, l);
         } else {
             const long long k2 = idx - nwords;
-            const int p = int(k2 / KG), kg = int(k2 % KG);
-            const int n = canon_row(p, g.N, gate_up);
-            const int j = kg / G, gl = kg % G;
-            const int t = p >> 3, r = p & 7;
-            const uint32_t sv = n < 0 ? 0u : s[(size_t)n * KG + kg];
-            const uint32_t zv = n < 0 ? 0u : z[(size_t)n * KG + kg];
-            *reinterpret_cast<uint32_t*>(out + ((size_t)t * g.ksl + j) * g.unit_bytes + 4 * W + ((size_t)r * G + gl) * 4) =
+            const int r = int(k2 & 15);
+            const long long tg = k2 >> 4;
+            const int gr = int(tg % g.groups), T = int(tg / g.groups);
+            const int n = canon_row(T * 16 + r, g.N, gate_up);
+            const uint32_t sv = n < 0 ? 0u : s[(size_t)n * g.groups + gr];
+            const uint32_t zv = n < 0 ? 0u : z[(size_t)n * g.groups + gr];
+            *reinterpret_cast<uint32_t*>(out + (size_t)T * g.tile_bytes + (size_t)gr * kGroupBytes + 1024 + r * 4) =
                 sv | (zv << 16);
         }
     }
@@ -123,32 +131,27 @@ __global__ void pack_kernel(const uint8_t* __restrict__ q, const uint16_t* __res
 
 __global__ void unpack_kernel(const uint8_t* __restrict__ in, PackGeom g, int gate_up, uint8_t* __restrict__ q,
                               uint16_t* __restrict__ s, uint16_t* __restrict__ z) {
-    const int W = g.wks, G = W / 128, KG = g.K / 128, wpr = g.K / 8;
-    const long long nwords = (long long)g.tiles * 8 * wpr;
-    const long long nsz = (long long)g.tiles * 8 * KG;
+    const long long nwords = (long long)g.tiles * g.groups * 256;
+    const long long nsz = (long long)g.tiles * g.groups * 16;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < nwords + nsz;
          idx += (long long)gridDim.x * blockDim.x) {
         if (idx < nwords) {
-            const int p = int(idx / wpr), wi = int(idx % wpr);
-            const int n = canon_row(p, g.N, gate_up);
-            if (n < 0) continue;
-            const int j = (wi * 8) / W, i = wi - j * (W / 8);
-            const int t = p >> 3, r = p & 7;
-            const uint32_t word = *reinterpret_cast<const uint32_t*>(
-                in + ((size_t)t * g.ksl + j) * g.unit_bytes + (size_t)r * (W / 2) + 4 * i);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) q[(size_t)n * g.K + (size_t)wi * 8 + e] = (word >> c_bitoff[e]) & 15u;
+            const int l = int(idx & 31), ks = int((idx >> 5) & 7);
+            const long long tg = idx >> 8;
+            const int gr = int(tg % g.groups), T = int(tg / g.groups);
+            unpack_word(*reinterpret_cast<const uint32_t*>(in + word_offset(g, T, gr, ks, l)), q, g.N, g.K, gate_up, T,
+                        gr, ks, l);
         } else {
             const long long k2 = idx - nwords;
-            const int p = int(k2 / KG), kg = int(k2 % KG);
-            const int n = canon_row(p, g.N, gate_up);
+            const int r = int(k2 & 15);
+            const long long tg = k2 >> 4;
+            const int gr = int(tg % g.groups), T = int(tg / g.groups);
+            const int n = canon_row(T * 16 + r, g.N, gate_up);
             if (n < 0) continue;
-            const int j = kg / G, gl = kg % G;
-            const int t = p >> 3, r = p & 7;
-            const uint32_t v = *reinterpret_cast<const uint32_t*>(
-                in + ((size_t)t * g.ksl + j) * g.unit_bytes + 4 * W + ((size_t)r * G + gl) * 4);
-            s[(size_t)n * KG + kg] = uint16_t(v & 0xFFFFu);
-            z[(size_t)n * KG + kg] = uint16_t(v >> 16);
+            const uint32_t v = *reinterpret_cast<const uint32_t*>(in + (size_t)T * g.tile_bytes +
+                                                                  (size_t)gr * kGroupBytes + 1024 + r * 4);
+            s[(size_t)n * g.groups + gr] = uint16_t(v & 0xFFFFu);
+            z[(size_t)n * g.groups + gr] = uint16_t(v >> 16);
         }
     }
 }
@@ -160,7 +163,7 @@ int pack_run(const uint8_t* q, const uint16_t* s, const uint16_t* z, int N, int 
     if (flags & ~KMR_PACK_GATE_UP) return KMR_ERR_INVALID_ARG;
     if (!pack_geom(N, K, group, &g)) return KMR_ERR_SHAPE;
     const int gate_up = flags & KMR_PACK_GATE_UP;
-    if (gate_up && N % 8 != 0) return KMR_ERR_SHAPE;
+    if (gate_up && N % 16 != 0) return KMR_ERR_SHAPE;
     if (packed_bytes < (size_t)g.bytes) return KMR_ERR_BUFFER_SIZE;
     if (!on_device) {
         const size_t n = (size_t)N * K;
@@ -180,7 +183,7 @@ int unpack_run(const void* packed, size_t packed_bytes, int N, int K, int group,
     if (flags & ~KMR_PACK_GATE_UP) return KMR_ERR_INVALID_ARG;
     if (!pack_geom(N, K, group, &g)) return KMR_ERR_SHAPE;
     const int gate_up = flags & KMR_PACK_GATE_UP;
-    if (gate_up && N % 8 != 0) return KMR_ERR_SHAPE;
+    if (gate_up && N % 16 != 0) return KMR_ERR_SHAPE;
     if (packed_bytes < (size_t)g.bytes) return KMR_ERR_BUFFER_SIZE;
     if (!on_device) {
         unpack_host(static_cast<const uint8_t*>(packed), g, gate_up, q, s, z);

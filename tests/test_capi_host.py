@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported_and_bound(L):
 
 
 def test_status_strings_and_version(L):
-    assert kmr.kmr_layout_version() == 1
+    assert kmr.kmr_layout_version() == 2
     assert kmr.kmr_status_string(0) == "ok"
     for code in range(-9, 0):
         assert kmr.kmr_status_string(code) != "unknown status"
@@ -53,7 +53,7 @@ def _canon(r, N, K):
 
 
 @pytest.mark.parametrize("N,K,flags", [(8, 128, 0), (13, 256, 0), (40, 768, 0), (64, 2048, 0), (24, 6144, 0),
-                                       (16, 640, 1), (48, 2048, 1)])
+                                       (16, 640, 1), (48, 2048, 1), (32, 384, 1)])
 def test_host_pack_matches_spec_and_roundtrips(L, N, K, flags):
     r = np.random.default_rng(N * 7 + K)
     q, s, z = _canon(r, N, K)
@@ -78,7 +78,7 @@ def test_every_code_value_roundtrips(L):
     size = kmr.kmr_packed_size(N, K, 128)
     out = np.zeros(size, np.uint8)
     kmr.kmr_pack_int4(q, s, z, N, K, 128, 0, out, size, 0)
-    nib = out.reshape(-1, 4 * 1024 + 256)[:, :4096].reshape(-1)
+    nib = out.reshape(-1, 1088)[:, :1024].reshape(-1)
     assert set(np.unique(nib)) == set(range(256))
     q2, s2, z2 = np.zeros_like(q), np.zeros_like(s), np.zeros_like(z)
     kmr.kmr_unpack_int4(out, size, N, K, 128, 0, q2, s2, z2, 0)
@@ -111,13 +111,16 @@ def test_host_pack_rejects_bad_input(L):
 
 def test_entry_points_reject_bad_arguments_without_a_gpu(L):
     # every check below runs on the host before any CUDA call
-    assert L.kmr_int4_gemv(None, 8, 128, 128, 0, None, 1, None, 0, None, 0, None) == kmr.KMR_ERR_INVALID_ARG
-    assert L.kmr_int4_gemv(1, 8, 100, 128, 0, 1, 1, 1, 0, 1, 1 << 20, None) == kmr.KMR_ERR_SHAPE
-    assert L.kmr_int4_gemv(1, 8, 128, 128, 0, 1, 0, 1, 0, 1, 1 << 20, None) == kmr.KMR_ERR_BATCH
-    assert L.kmr_int4_gemv(1, 8, 128, 128, 0, 1, 17, 1, 0, 1, 1 << 20, None) == kmr.KMR_ERR_BATCH
-    assert L.kmr_int4_gemv(1, 8, 128, 128, 0, 1, 1, 1, 2, 1, 1 << 20, None) == kmr.KMR_ERR_INVALID_ARG
-    assert L.kmr_int4_gemv(1, 8, 128, 128, 0, 1, 1, 1, 7, 1, 1 << 20, None) == kmr.KMR_ERR_INVALID_ARG
-    assert L.kmr_int4_gemv(1, 8, 128, 128, 0, 1, 1, 1, 0, 1, 0, None) == kmr.KMR_ERR_BUFFER_SIZE
+    assert L.kmr_int4_gemv(None, 8, 128, 128, 0, None, 1, None, 0, None) == kmr.KMR_ERR_INVALID_ARG
+    assert L.kmr_int4_gemv(1, 8, 100, 128, 0, 1, 1, 1, 0, None) == kmr.KMR_ERR_SHAPE
+    assert L.kmr_int4_gemv(1, 8, 128, 64, 0, 1, 1, 1, 0, None) == kmr.KMR_ERR_SHAPE
+    assert L.kmr_int4_gemv(1, 8, 8320, 128, 0, 1, 1, 1, 0, None) == kmr.KMR_ERR_SHAPE
+    assert L.kmr_int4_gemv(1, 8, 128, 128, 0, 1, 0, 1, 0, None) == kmr.KMR_ERR_BATCH
+    assert L.kmr_int4_gemv(1, 8, 128, 128, 0, 1, 17, 1, 0, None) == kmr.KMR_ERR_BATCH
+    assert L.kmr_int4_gemv(1, 16, 128, 128, 0, 1, 1, 1, 2, None) == kmr.KMR_ERR_INVALID_ARG   # SiLU needs gate/up packing
+    assert L.kmr_int4_gemv(1, 8, 128, 128, 1, 1, 1, 1, 2, None) == kmr.KMR_ERR_INVALID_ARG    # N not a multiple of 16
+    assert L.kmr_int4_gemv(1, 8, 128, 128, 0, 1, 1, 1, 7, None) == kmr.KMR_ERR_INVALID_ARG
+    assert L.kmr_int4_gemv(1, 8, 128, 128, 2, 1, 1, 1, 0, None) == kmr.KMR_ERR_INVALID_ARG
     assert L.kmr_decode_attn(None, 1, 1, 1, 1, 1, 16, 8, 128, 64, 1, 0.1, 1, 1, 1 << 30, None) == kmr.KMR_ERR_INVALID_ARG
     assert L.kmr_decode_attn(1, 1, 1, 1, 1, 1, 16, 8, 96, 64, 1, 0.1, 1, 1, 1 << 30, None) == kmr.KMR_ERR_SHAPE
     assert L.kmr_decode_attn(1, 1, 1, 1, 1, 1, 16, 5, 128, 64, 1, 0.1, 1, 1, 1 << 30, None) == kmr.KMR_ERR_SHAPE

@@ -39,7 +39,7 @@ def _device_pack(torch, q, s, z, flags=0):
 
 # ------------------------------------------------------------------ packing (bit-exact)
 @pytest.mark.parametrize("N,K,flags", [(13, 256, 0), (64, 768, 0), (4096, 2048, 0), (2048, 6144, 0),
-                                       (12288, 2048, 1), (24, 640, 1)])
+                                       (12288, 2048, 1), (32, 640, 1)])
 def test_device_pack_bit_exact(torch, N, K, flags):
     q, s, z = _canon(N + K, N, K)
     dev = _device_pack(torch, q, s, z, flags).cpu().numpy()
@@ -61,16 +61,12 @@ def test_device_pack_bit_exact(torch, N, K, flags):
 # ------------------------------------------------------------------ int4 GEMV
 def _gemv(torch, packed, N, K, x, epi=kmr.KMR_EPI_NONE, flags=0, y0=None):
     M = x.shape[0]
-    ws_bytes = kmr.kmr_int4_gemv_workspace_size(N, K, 128, M)
-    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
     ncol = N // 2 if epi == kmr.KMR_EPI_SILU_MUL else N
     y = torch.from_numpy(y0).cuda() if y0 is not None else torch.zeros((M, ncol), dtype=torch.float32, device="cuda")
     xd = torch.from_numpy(np.ascontiguousarray(x, np.float32)).cuda()
-    kmr.kmr_int4_gemv(packed, N, K, 128, flags, xd, M, y, epi, ws, ws_bytes, torch.cuda.current_stream())
+    kmr.kmr_int4_gemv(packed, N, K, 128, flags, xd, M, y, epi, torch.cuda.current_stream())
     torch.cuda.synchronize()
     assert kmr.kmr_last_device_error() == 0
-    cnt_bytes = ((N + 7) // 8 * 4 + 15) // 16 * 16
-    assert int(ws[-cnt_bytes:].sum().item()) == 0, "arrival counters must be left zeroed"
     return y.cpu().numpy()
 
 
@@ -130,16 +126,16 @@ def test_int4_gemv_epilogues(torch):
 
 
 def test_int4_gemv_special_cases(torch):
-    # The kernel folds the 1024 magic offset, the -8 and the zero point in once per 32
-    # inputs (y = s (D - 1024 X') + (z - 8 s) X), so an all-zero weight row leaves a
-    # float32 cancellation residue of order 2^-24 * 1024 * |x'| per chunk: far below the
-    # 1e-2 bar, bounded here by 1e-4 * s * ||x||.
+    # The tensor cores accumulate (1024 + c q) x' in float32 and the 1024 offset is removed
+    # once per group (y = s (D - 1024 X) / c + (z - 8 s) X), so an all-zero weight row leaves
+    # a cancellation residue of order (k-steps per group) * 2^-24 * 1032 * |x| per group:
+    # bounded here by 2^-14 * s * ||x||_1, four orders of magnitude below a wrong term.
     N, K = 64, 1024
     q = np.full((N, K), 8, np.uint8)
     s = f32_to_bf16_bits(np.full((N, K // 128), 0.5, np.float32))
     z = np.zeros((N, K // 128), np.uint16)
     x = np.random.default_rng(0).standard_normal((3, K)).astype(np.float32)
-    bound = 1e-4 * 0.5 * np.linalg.norm(x, axis=1, keepdims=True)
+    bound = 2.0 ** -14 * 0.5 * np.abs(x).sum(axis=1, keepdims=True)
     y = _gemv(torch, _device_pack(torch, q, s, z), N, K, x)
     assert np.all(np.abs(y) <= bound)                                                     # W = 0
     q[5, 777] = 9                                                                         # one code 9
