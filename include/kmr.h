@@ -144,6 +144,35 @@ int kmr_decode_attn(const float* q, const uint16_t* k_cache, const uint16_t* v_c
                     int B, int n_q_heads, int n_kv_heads, int head_dim, int max_len, int slots,
                     float scale, float* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Fixed device scratch of kmr_decode_attn_noalloc, in bytes (4 MiB). */
+#define KMR_NOALLOC_ATTN_SCRATCH_BYTES (4u << 20)
+
+/* kmr_decode_attn without a workspace argument, for callers that cannot
+ * allocate device memory: code running while a CUDA graph is captured in
+ * global mode, engines whose memory planner owns the whole device heap, and
+ * latency-critical loops that cannot afford cudaMalloc's implicit device
+ * synchronisation.  The pages this library follows have no counterpart of
+ * this entry point; it exists only for such callers.
+ *   Same arguments, layouts and results as kmr_decode_attn, minus the
+ *   workspace.  The split partials live in one fixed array inside the
+ *   library's device image (KMR_NOALLOC_ATTN_SCRATCH_BYTES, held by every GPU
+ *   that loads the library until the process exits); the call allocates
+ *   nothing, and clears the array's arrival counters with cudaMemsetAsync on
+ *   `stream` before launching.
+ *   Limit: B * n_q_heads * splits * (head_dim + 2) * 4 bytes (rounded up to
+ *   16) + B * n_kv_heads * 4 bytes must fit the array, where splits =
+ *   ceil(SM count / n_kv_heads) capped at 32 (19 for 8 KV heads on a 152-SM
+ *   GB300); larger problems return KMR_ERR_SHAPE and launch nothing.
+ *   Every call on a device shares the array and it keeps the last call's
+ *   contents, so calls that overlap on the GPU race: order them on one stream.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *   first call before any stream capture. */
+int kmr_decode_attn_noalloc(const float* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                            const int32_t* slot_ids, const int32_t* cache_position,
+                            int B, int n_q_heads, int n_kv_heads, int head_dim, int max_len, int slots,
+                            float scale, float* out, void* stream);
+
 /* Error word of the standalone kernels (kmr_int4_gemv, kmr_decode_attn) on the
  * current device: synchronises the device, returns the first recorded
  * KMR_ERR_* (or KMR_OK) and clears it. */

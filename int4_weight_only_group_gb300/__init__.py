@@ -24,7 +24,7 @@ __all__ = [
     "KMR_W_QKV", "KMR_W_O", "KMR_W_GATE_UP", "KMR_W_DOWN", "KMR_N_INPUT", "KMR_N_POST", "KMR_N_Q", "KMR_N_K",
     "ModelConfig", "kmr_status_string", "kmr_layout_version", "kmr_packed_size", "kmr_pack_int4",
     "kmr_unpack_int4", "kmr_int4_gemv", "kmr_decode_attn_workspace_size",
-    "kmr_decode_attn", "kmr_last_device_error", "Model",
+    "kmr_decode_attn", "kmr_decode_attn_noalloc", "kmr_last_device_error", "Model",
 ]
 
 KMR_OK = 0
@@ -84,6 +84,7 @@ _SIGNATURES = {
     "kmr_int4_gemv": (_I, [_P, _I, _I, _I, _I, _P, _I, _P, _I, _P]),
     "kmr_decode_attn_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "kmr_decode_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _SZ, _P]),
+    "kmr_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P]),
     "kmr_last_device_error": (_I, []),
     "kmr_model_create": (_I, [ctypes.POINTER(ModelConfig), ctypes.POINTER(_P)]),
     "kmr_model_destroy": (_I, [_P]),
@@ -188,6 +189,15 @@ def kmr_decode_attn(q, k_cache, v_cache, slot_ids, cache_position, B, nq, nkv, d
     _check(lib().kmr_decode_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(slot_ids), _ptr(cache_position), B,
                                  nq, nkv, d, max_len, slots, float(scale), _ptr(out), _ptr(workspace),
                                  workspace_bytes, _stream(stream)), "kmr_decode_attn")
+
+
+def kmr_decode_attn_noalloc(q, k_cache, v_cache, slot_ids, cache_position, B, nq, nkv, d, max_len, slots, scale,
+                            out, stream=None) -> None:
+    """kmr_decode_attn for callers that cannot allocate device memory: no workspace argument,
+    the library's fixed device scratch is used instead (see include/kmr.h for its limit)."""
+    _check(lib().kmr_decode_attn_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(slot_ids),
+                                         _ptr(cache_position), B, nq, nkv, d, max_len, slots, float(scale),
+                                         _ptr(out), _stream(stream)), "kmr_decode_attn_noalloc")
 
 
 def kmr_last_device_error() -> int:
