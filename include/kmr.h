@@ -270,7 +270,21 @@ int kmr_decode_step_host(kmr_model* m, int32_t* token_ids, int32_t* positions, i
 /* Synchronise `stream`, then return and clear the model's device error word. */
 int kmr_model_sync_status(kmr_model* m, void* stream);
 
-/* Launches one step makes (kernels per step) for the given B, for accounting. */
+/* ---- Diagnostics (no counterpart in the method's description) ----------------
+ * Shared-memory poisoning.  kmr_smem_poison fills the shared memory of every SM
+ * of the current device with the 32-bit `pattern`, asynchronously on `stream`
+ * (one CTA per SM holding 227 KB).  With kmr_model_set_smem_poison(m, 1, pattern)
+ * every kernel of the model's decode step is preceded by such a fill, so a
+ * kernel that reads shared memory it did not write sees `pattern` (choose NaN
+ * or Inf bits) rather than leftovers; a poisoned step must equal a clean one
+ * bit for bit.  Enabling or disabling synchronises the device and drops the
+ * model's captured step graphs.  Off by default; costs one extra launch per
+ * kernel.  Returns KMR_OK, KMR_ERR_INVALID_ARG (null model) or KMR_ERR_CUDA. */
+int kmr_smem_poison(uint32_t pattern, void* stream);
+int kmr_model_set_smem_poison(kmr_model* m, int enable, uint32_t pattern);
+
+/* Launches one step makes (kernels per step) for the given B, for accounting
+ * (twice as many while shared-memory poisoning is on). */
 int kmr_model_kernels_per_step(const kmr_model* m, int B);
 
 #ifdef __cplusplus

@@ -24,7 +24,7 @@ __all__ = [
     "KMR_W_QKV", "KMR_W_O", "KMR_W_GATE_UP", "KMR_W_DOWN", "KMR_N_INPUT", "KMR_N_POST", "KMR_N_Q", "KMR_N_K",
     "ModelConfig", "kmr_status_string", "kmr_layout_version", "kmr_packed_size", "kmr_pack_int4",
     "kmr_unpack_int4", "kmr_int4_gemv", "kmr_decode_attn_workspace_size",
-    "kmr_decode_attn", "kmr_decode_attn_noalloc", "kmr_last_device_error", "Model",
+    "kmr_decode_attn", "kmr_decode_attn_noalloc", "kmr_last_device_error", "kmr_smem_poison", "Model",
 ]
 
 KMR_OK = 0
@@ -97,6 +97,8 @@ _SIGNATURES = {
     "kmr_decode_step_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P]),
     "kmr_model_sync_status": (_I, [_P, _P]),
     "kmr_model_kernels_per_step": (_I, [_P, _I]),
+    "kmr_smem_poison": (_I, [ctypes.c_uint32, _P]),
+    "kmr_model_set_smem_poison": (_I, [_P, _I, ctypes.c_uint32]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
 
@@ -204,6 +206,11 @@ def kmr_last_device_error() -> int:
     return lib().kmr_last_device_error()
 
 
+def kmr_smem_poison(pattern: int, stream=None) -> None:
+    """Fill every SM's shared memory with the 32-bit `pattern` (diagnostic; see include/kmr.h)."""
+    _check(lib().kmr_smem_poison(pattern & 0xFFFFFFFF, _stream(stream)), "kmr_smem_poison")
+
+
 # ------------------------------------------------------------------ model handle
 class Model:
     """Owner of one kmr_model (packed weights, static KV cache, step scratch)."""
@@ -281,3 +288,8 @@ class Model:
 
     def kernels_per_step(self, B: int) -> int:
         return lib().kmr_model_kernels_per_step(self._h, B)
+
+    def set_smem_poison(self, enable: bool, pattern: int = 0xFFFFFFFF) -> None:
+        """Precede every kernel of the step with a shared-memory fill of `pattern` (diagnostic)."""
+        _check(lib().kmr_model_set_smem_poison(self._h, int(bool(enable)), pattern & 0xFFFFFFFF),
+               "kmr_model_set_smem_poison")

@@ -4,6 +4,8 @@
 // standalone GEMV / attention entry points.
 #include <math.h>
 #include <stdio.h>
+
+#include <cmath>
 #include <string.h>
 
 #include <algorithm>
@@ -54,6 +56,7 @@ cudaError_t ensure_kernel_attributes() {
     if ((e = gemv_set_attributes()) != cudaSuccess) return e;
     if ((e = head_set_attributes()) != cudaSuccess) return e;
     if ((e = attn_set_attributes()) != cudaSuccess) return e;
+    if ((e = poison_set_attributes()) != cudaSuccess) return e;
     done[dev] = true;
     return cudaSuccess;
 }
@@ -76,7 +79,9 @@ struct GemvLaunch {
 };
 
 // Rows in passes of at most 8; returns the number of launches or a negative KMR code.
-static int enqueue_gemv(const GemvLaunch& a, int M, int* err, cudaStream_t st, bool pdl, int sms) {
+// With `poison`, every pass is preceded by the shared-memory poisoning diagnostic.
+static int enqueue_gemv(const GemvLaunch& a, int M, int* err, cudaStream_t st, bool pdl, int sms,
+                        bool poison = false, uint32_t pattern = 0) {
     int launches = 0;
     const int grid = gemv_grid(a.g.tiles, sms);
     for (int r0 = 0; r0 < M; r0 += kMaxMB) {
@@ -102,6 +107,7 @@ static int enqueue_gemv(const GemvLaunch& a, int M, int* err, cudaStream_t st, b
         p.ldy = a.ldy;
         p.err = err;
         p.nstage = gemv_nstage(a.g.tiles, grid, a.g.tile_bytes);
+        if (poison && launch_smem_poison(pattern, sms, st) != cudaSuccess) return KMR_ERR_CUDA;
         if (launch_gemv(p, MB, grid, st, pdl || launches > 0) != cudaSuccess) return KMR_ERR_CUDA;
         ++launches;
     }
@@ -289,6 +295,8 @@ struct kmr_model {
     cudaStream_t cap = nullptr;
     std::vector<GraphEntry> graphs;
     unsigned long long tick = 0;
+    bool poison = false;           // diagnostic: fill shared memory before every kernel of the step
+    uint32_t poison_pattern = 0;
     std::vector<void*> allocs;
     std::mutex mu;
 };
@@ -381,7 +389,7 @@ int enqueue_step(kmr_model* m, const StepArgs& a, cudaStream_t st) {
         g.epi = EPI_STORE;
         g.y = m->qkv;
         g.ldy = nqkv;
-        if (enqueue_gemv(g, B, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        if (enqueue_gemv(g, B, m->err, st, pdl, grid, m->poison, m->poison_pattern) < 0) return KMR_ERR_CUDA;
         pdl = true;
         // attention (+ q/k norm, M-RoPE, KV write)
         AttnParams ap = {};
@@ -408,11 +416,13 @@ int enqueue_step(kmr_model* m, const StepArgs& a, cudaStream_t st) {
         ap.S = c.max_len;
         ap.slots = c.slots;
         ap.scale = 1.0f / sqrtf(float(c.head_dim));
-        ap.tsplit = m->tsplit;
+        ap.tsplit = kAttnClusterSplits;
+        ap.cluster = 1;
         ap.out = m->attn_out;
         ap.part = m->apart;
         ap.counters = m->acount;
         ap.err = m->err;
+        if (m->poison && launch_smem_poison(m->poison_pattern, grid, st) != cudaSuccess) return KMR_ERR_CUDA;
         if (launch_attn(ap, st, pdl) != cudaSuccess) return KMR_ERR_CUDA;
         // O projection + residual
         g = GemvLaunch{};
@@ -423,7 +433,7 @@ int enqueue_step(kmr_model* m, const StepArgs& a, cudaStream_t st) {
         g.epi = EPI_RESID;
         g.y = m->x_resid;
         g.ldy = c.hidden;
-        if (enqueue_gemv(g, B, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        if (enqueue_gemv(g, B, m->err, st, pdl, grid, m->poison, m->poison_pattern) < 0) return KMR_ERR_CUDA;
         // gate_up (+ post-attention RMSNorm) -> SiLU(gate) * up
         g = GemvLaunch{};
         g.w = L.w[KMR_W_GATE_UP];
@@ -435,7 +445,7 @@ int enqueue_step(kmr_model* m, const StepArgs& a, cudaStream_t st) {
         g.epi = EPI_SILU;
         g.y = m->act;
         g.ldy = c.intermediate;
-        if (enqueue_gemv(g, B, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        if (enqueue_gemv(g, B, m->err, st, pdl, grid, m->poison, m->poison_pattern) < 0) return KMR_ERR_CUDA;
         // down + residual
         g = GemvLaunch{};
         g.w = L.w[KMR_W_DOWN];
@@ -445,7 +455,7 @@ int enqueue_step(kmr_model* m, const StepArgs& a, cudaStream_t st) {
         g.epi = EPI_RESID;
         g.y = m->x_resid;
         g.ldy = c.hidden;
-        if (enqueue_gemv(g, B, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        if (enqueue_gemv(g, B, m->err, st, pdl, grid, m->poison, m->poison_pattern) < 0) return KMR_ERR_CUDA;
         (void)qd;
     }
     // final norm + LM head + argmax + finalize, in passes of at most 8 rows
@@ -481,6 +491,7 @@ int enqueue_step(kmr_model* m, const StepArgs& a, cudaStream_t st) {
         if (nst < 2) nst = 2;
         if (nst > tpc) nst = tpc;
         hp.nstage = nst;
+        if (m->poison && launch_smem_poison(m->poison_pattern, grid, st) != cudaSuccess) return KMR_ERR_CUDA;
         if (launch_head(hp, MB, hgrid, st, true) != cudaSuccess) return KMR_ERR_CUDA;
     }
     return KMR_OK;
@@ -692,6 +703,24 @@ extern "C" int kmr_model_kv_pointers(kmr_model* m, int layer, void** k, void** v
     return KMR_OK;
 }
 
+extern "C" int kmr_smem_poison(uint32_t pattern, void* stream) {
+    if (ensure_kernel_attributes() != cudaSuccess) return KMR_ERR_CUDA;
+    return launch_smem_poison(pattern, num_sms(), static_cast<cudaStream_t>(stream)) == cudaSuccess ? KMR_OK
+                                                                                                 : KMR_ERR_CUDA;
+}
+
+extern "C" int kmr_model_set_smem_poison(kmr_model* m, int enable, uint32_t pattern) {
+    if (!m) return KMR_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(m->mu);
+    DeviceGuard dg(m->device);
+    if (cudaDeviceSynchronize() != cudaSuccess) return KMR_ERR_CUDA;
+    m->poison = enable != 0;
+    m->poison_pattern = pattern;
+    for (GraphEntry& e : m->graphs) cudaGraphExecDestroy(e.exec);   // captured graphs follow the old setting
+    m->graphs.clear();
+    return KMR_OK;
+}
+
 extern "C" int kmr_decode_step(kmr_model* m, int32_t* tok, int32_t* pos, int32_t* cpos, const int32_t* slot,
                                uint8_t* fin, int B, float* logits, void* stream) {
     if (!m || !tok || !pos || !cpos || !slot || !fin) return KMR_ERR_INVALID_ARG;
@@ -780,5 +809,6 @@ extern "C" int kmr_model_sync_status(kmr_model* m, void* stream) {
 extern "C" int kmr_model_kernels_per_step(const kmr_model* m, int B) {
     if (!m || B < 1) return 0;
     const int passes = (B + kMaxMB - 1) / kMaxMB;
-    return m->cfg.n_layers * (4 * passes + 1) + passes;
+    const int k = m->cfg.n_layers * (4 * passes + 1) + passes;
+    return m->poison ? 2 * k : k;                 // the diagnostic adds one fill per kernel
 }

@@ -3,33 +3,37 @@
 // What it computes ("kaminari — a single-GPU Qwen3-VL inference engine,
 // explained", §07 int4 sidecar quantization; group 128 along K):
 //     y[m, n] = sum_k x[m, k] * ((q[n, k] - 8) * s[n, k/128] + z[n, k/128])
-// optionally after an RMSNorm of x (prologue) and followed by a store, a
-// residual add or SiLU(gate) * up (epilogue).
+// optionally on RMSNorm(x) (prologue) and followed by a store, a residual
+// add or SiLU(gate) * up (epilogue).
 //
 // GB300 design
 //   * HBM-bound: every packed byte is read once.  A CTA owns whole 16-row
 //     tiles (no cross-CTA reduction, no global scratch) and pulls them with
-//     cp.async.bulk into a shared-memory ring whose first fill is issued
-//     BEFORE griddepcontrol.wait: under programmatic dependent launch a kernel
+//     cp.async.bulk into shared memory; the whole fill is issued BEFORE
+//     griddepcontrol.wait, so under programmatic dependent launch a kernel
 //     streams its weights while the previous kernel of the step finishes.
 //   * Issue-rate bound on CUDA cores: at GB300's ~47 int4 weights per SM-clock
 //     a float FMA per weight plus the unpacking would exceed the SM's issue
-//     rate (2+ instructions per weight at batch 1, 4+ at batch 4).  The
-//     multiply-adds therefore go to the tensor cores (mma.m16n8k16, f16 in,
-//     f32 accumulate, the 16 rows of a tile as M and the batch rows as N) and
-//     the threads only unpack: the KMR4 layout stores each lane's A fragment
-//     of one 16x16 block in one 32-bit word, so 8 weights cost one shift and
-//     four LOP3s.  OR-ing a nibble into the mantissa of fp16 1024.0 gives
-//     1024 + q exactly (1024 + 16q for rows 8..15, whose nibble sits one
-//     position higher); the offset, the -8 and the zero point are folded in
-//     once per group with the group sums X of x:
-//         y = s * (D - 1024 X) / c + (z - 8 s) X,   c = 1 or 16 per row.
-//   * x is staged once per CTA in shared memory as fp16, scaled per row by a
-//     power of two (exact) so its largest magnitude sits below 2^13, in the
-//     order of the B fragments.
+//     rate.  The multiply-adds therefore go to the tensor cores (mma.m16n8k16,
+//     f16 in, f32 accumulate; 16 tile rows as M, batch rows as N) and the
+//     threads only unpack: the KMR4 layout stores each lane's A fragment of a
+//     16x16 block in one 32-bit word, so 8 weights cost one shift and four
+//     LOP3s.  OR-ing a nibble into the mantissa of fp16 1024.0 gives 1024 + q
+//     exactly (1024 + 16q for tile rows 8..15, whose nibble sits one position
+//     higher); the offset, the -8 and the zero point are folded in once per
+//     group with the group sum X' of the staged x:
+//         y += (s (D - 1024 X') / c + (z - 8 s) X') / sigma,   c = 1 or 16.
+//   * Latency: after griddepcontrol.wait nothing waits on a block barrier
+//     until the products are done.  Each warp stages only the x of its own
+//     groups (w, w + 16, ...): one coalesced load per lane, fp16 scaled by a
+//     per-(row, group) power of two sigma taken from that group's largest
+//     value (exact; undone in the fold), in B-fragment order in a warp-private
+//     shared buffer.  RMSNorm is applied to the result instead of the input,
+//     y = r * W (x * w) with r = rsqrt(mean(x^2) + eps), so its reduction
+//     joins the one barrier before the epilogue.
 //   * Deterministic and batch invariant: fixed k order inside the mma, fixed
-//     group order per warp, fixed warp order in the tile sum; a row's result
-//     never depends on the other rows or on M.
+//     group and warp orders in every sum; a row's result never depends on the
+//     other rows or on M.
 #include <cuda_fp16.h>
 
 #include "kmr_internal.cuh"
@@ -40,19 +44,23 @@ namespace {
 
 __host__ __device__ inline size_t al16(size_t v) { return (v + 15) & ~size_t(15); }
 
+constexpr int kGemvThreads = 512;              // 16 warps: latency hiding for the unpack + mma chains
+constexpr int kGemvWarps = kGemvThreads / 32;
+
+// xw: per warp, GPW groups x MB rows of 128 staged halves (B-fragment order);
+// xst: per warp, GPW groups x 8 rows x (X', 1/sigma); ssw: per warp, sum of x^2 per row;
+// part: per tile in the ring, per warp, 16 rows x MB columns.
 struct GemvSmem {
-    size_t bar, xh, xs, isig, red, part, stage, total;
+    size_t bar, xw, xst, ssw, part, stage, total;
 };
-// xh: MB rows of (K + 8) halves; xs: [groups][8] group sums; part: [nst][8 warps][16 rows][8 cols]
-__host__ __device__ inline GemvSmem gemv_layout(int MB, int K, int tile_bytes, int nst) {
+__host__ __device__ inline GemvSmem gemv_layout(int MB, int GPW, int tile_bytes, int nst) {
     GemvSmem L;
     size_t o = 0;
     L.bar = o;   o += al16(size_t(nst) * 8);
-    L.xh = o;    o += al16(size_t(MB) * (K + 8) * 2);
-    L.xs = o;    o += al16(size_t(K / 128) * 8 * 4);
-    L.isig = o;  o += al16(size_t(8) * 4);
-    L.red = o;   o += al16(size_t(2) * 8 * 4);
-    L.part = o;  o += al16(size_t(nst) * 8 * 128 * 4);
+    L.xw = o;    o += al16(size_t(kGemvWarps) * GPW * MB * 128 * 2);
+    L.xst = o;   o += al16(size_t(kGemvWarps) * GPW * 8 * 2 * 4);
+    L.ssw = o;   o += al16(size_t(kGemvWarps) * 8 * 4);
+    L.part = o;  o += al16(size_t(nst) * kGemvWarps * 16 * MB * 4);
     o = (o + 127) & ~size_t(127);
     L.stage = o; o += size_t(nst) * tile_bytes;
     L.total = o;
@@ -68,32 +76,139 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Position (in halves, within a row of x') of input k in B-fragment order: blocks of
-// 64 inputs; inside a block, lane slot t (16 halves) holds, for each of the 4 k-steps
-// k0 = 64*block + 16*step, the inputs (k0+2t, k0+2t+1, k0+2t+8, k0+2t+9).
-__device__ __forceinline__ int xpos(int k) {
-    const int kk = k & 15;
-    return (k >> 6) * 64 + ((kk & 7) >> 1) * 16 + ((k >> 4) & 3) * 4 + (kk >> 3) * 2 + (kk & 1);
+// Position (in halves) of group-local input kk (0..127) in B-fragment order: two blocks
+// of 64; inside a block, lane slot t (16 halves) holds for each of its 4 k-steps
+// (k0 = 16 step) the inputs (k0+2t, k0+2t+1, k0+2t+8, k0+2t+9).
+__device__ __forceinline__ int bpos(int kk) {
+    const int j = kk & 15;
+    return (kk >> 6) * 64 + ((j & 7) >> 1) * 16 + ((kk >> 4) & 3) * 4 + (j >> 3) * 2 + (j & 1);
 }
 
+// 2^(13 - floor(log2 a)) for a > 0 finite (a * sigma < 2^14), else 1.
+__device__ __forceinline__ float pow2_scale(float a) {
+    if (!(a > 0.f && a <= 3.4e38f)) return 1.f;
+    const int ex = int((__float_as_uint(a) >> 23) & 0xFFu) - 127;
+    return __uint_as_float(uint32_t(max(1, min(254, 127 + 13 - ex))) << 23);
+}
+
+// One (16-row tile, 128-input group) block: 8 tensor-core k-steps on four independent
+// accumulator chains, then the fold for rows g (x1) and g+8 (x16) and batch columns
+// 2t, 2t+1.  xb: the group's staged halves of batch row g; st: (X', 1/sigma) per row.
+__device__ __forceinline__ void group_product(const uint8_t* gb, const __half* xb, bool bload, int lane,
+                                              const float* st, float (&acc)[4]) {
+    const int g = lane >> 2, t = lane & 3;
+    float d[4][4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) d[c][0] = d[c][1] = d[c][2] = d[c][3] = 0.f;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+        const uint4 wq = *reinterpret_cast<const uint4*>(gb + blk * 512 + lane * 16);
+        uint4 xa = make_uint4(0, 0, 0, 0), xc = make_uint4(0, 0, 0, 0);
+        if (bload) {
+            const uint4* xp = reinterpret_cast<const uint4*>(xb + blk * 64 + t * 16);
+            xa = xp[0];
+            xc = xp[1];
+        }
+        const uint32_t w4[4] = {wq.x, wq.y, wq.z, wq.w};
+        const uint32_t bx[8] = {xa.x, xa.y, xa.z, xa.w, xc.x, xc.y, xc.z, xc.w};
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t w = w4[ks], w2 = w >> 8;
+            mma16816(d[ks], and_or(w, 0x000F000Fu, 0x64006400u), and_or(w, 0x00F000F0u, 0x64006400u),
+                     and_or(w2, 0x000F000Fu, 0x64006400u), and_or(w2, 0x00F000F0u, 0x64006400u), bx[2 * ks],
+                     bx[2 * ks + 1]);
+        }
+    }
+    float D[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) D[i] = __fadd_rn(__fadd_rn(d[0][i], d[1][i]), __fadd_rn(d[2][i], d[3][i]));
+    const uint32_t sz0 = *reinterpret_cast<const uint32_t*>(gb + 1024 + g * 4);
+    const uint32_t sz1 = *reinterpret_cast<const uint32_t*>(gb + 1024 + (g + 8) * 4);
+    const float4 X = *reinterpret_cast<const float4*>(st + 4 * t);       // (X'_{2t}, is_{2t}, X'_{2t+1}, is_{2t+1})
+    const float s0 = bf16_lo(sz0), z0 = bf16_hi(sz0), s1 = bf16_lo(sz1), z1 = bf16_hi(sz1);
+    const float s1c = __fmul_rn(s1, 0.0625f);
+    const float zz0 = __fmaf_rn(-8.f, s0, z0), zz1 = __fmaf_rn(-8.f, s1, z1);
+    const float x0 = 1024.f * X.x, x1 = 1024.f * X.z;
+    acc[0] = __fmaf_rn(__fmaf_rn(s0, __fsub_rn(D[0], x0), __fmul_rn(zz0, X.x)), X.y, acc[0]);
+    acc[1] = __fmaf_rn(__fmaf_rn(s0, __fsub_rn(D[1], x1), __fmul_rn(zz0, X.z)), X.w, acc[1]);
+    acc[2] = __fmaf_rn(__fmaf_rn(s1c, __fsub_rn(D[2], x0), __fmul_rn(zz1, X.x)), X.y, acc[2]);
+    acc[3] = __fmaf_rn(__fmaf_rn(s1c, __fsub_rn(D[3], x1), __fmul_rn(zz1, X.z)), X.w, acc[3]);
+}
+
+// The warp's partial of one tile: rows g, g+8 and batch columns 2t, 2t+1 (< MB kept).
 template <int MB>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
+__device__ __forceinline__ void store_part(float* wp, int lane, const float (&acc)[4]) {
+    const int g = lane >> 2, t = lane & 3, c0 = 2 * t, c1 = 2 * t + 1;
+    if (c0 < MB) {
+        wp[g * MB + c0] = acc[0];
+        wp[(g + 8) * MB + c0] = acc[2];
+    }
+    if (c1 < MB) {
+        wp[g * MB + c1] = acc[1];
+        wp[(g + 8) * MB + c1] = acc[3];
+    }
+}
+
+// RMSNorm factor of row m from the per-warp sums of squares (fixed warp order).
+__device__ __forceinline__ float norm_factor(const GemvParams& p, const float* ssw, int m) {
+    if (p.in_kind == IN_F32) return 1.f;
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kGemvWarps; ++w) tot = __fadd_rn(tot, ssw[w * 8 + m]);
+    return rsqrtf(tot / float(p.K) + p.eps);
+}
+
+// Epilogue of one tile: fixed-order sum of the warp partials, RMSNorm factor, store / add / SiLU-mul.
+template <int MB>
+__device__ __forceinline__ void tile_epilogue(const GemvParams& p, const float* ps, int tile, int idx,
+                                              const float* ssw) {
+    constexpr int WS = 16 * MB;                     // floats per warp partial
+    if (p.epi == EPI_SILU) {
+        if (idx >= 8 * MB) return;
+        const int j = idx / MB, m = idx % MB;
+        const int jj = tile * 8 + j;
+        if (m >= p.M || jj >= p.N / 2) return;
+        float gv = 0.f, uv = 0.f;
+#pragma unroll
+        for (int w = 0; w < kGemvWarps; ++w) {
+            gv = __fadd_rn(gv, ps[w * WS + j * MB + m]);
+            uv = __fadd_rn(uv, ps[w * WS + (j + 8) * MB + m]);
+        }
+        const float r = norm_factor(p, ssw, m);
+        gv = __fmul_rn(gv, r);
+        uv = __fmul_rn(uv, r);
+        p.y[size_t(m) * p.ldy + jj] = __fmul_rn(__fdiv_rn(gv, __fadd_rn(1.f, expf(-gv))), uv);
+    } else {
+        if (idx >= 16 * MB) return;
+        const int rr = idx / MB, m = idx % MB;
+        const int n = tile * 16 + rr;
+        if (m >= p.M || n >= p.N) return;
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kGemvWarps; ++w) v = __fadd_rn(v, ps[w * WS + rr * MB + m]);
+        v = __fmul_rn(v, norm_factor(p, ssw, m));
+        float* yp = p.y + size_t(m) * p.ldy + n;
+        *yp = (p.epi == EPI_RESID) ? __fadd_rn(*yp, v) : v;
+    }
+}
+
+template <int MB, int GPW>
+__global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int P = gridDim.x, c = blockIdx.x;
     const int t0 = int((long long)c * p.tiles / P), t1 = int((long long)(c + 1) * p.tiles / P);
     const int nt = t1 - t0;
     const int K = p.K, G = K >> 7, tb = p.tile_bytes, nst = p.nstage;
-    const GemvSmem L = gemv_layout(MB, K, tb, nst);
+    const GemvSmem L = gemv_layout(MB, GPW, tb, nst);
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
-    __half* xh = reinterpret_cast<__half*>(smem + L.xh);
-    float* xs = reinterpret_cast<float*>(smem + L.xs);
-    float* isig = reinterpret_cast<float*>(smem + L.isig);
-    float* red = reinterpret_cast<float*>(smem + L.red);
+    __half* xw = reinterpret_cast<__half*>(smem + L.xw) + size_t(warp) * GPW * MB * 128;
+    float* xst = reinterpret_cast<float*>(smem + L.xst) + size_t(warp) * GPW * 16;
+    float* ssw = reinterpret_cast<float*>(smem + L.ssw);
     float* part = reinterpret_cast<float*>(smem + L.part);
     uint8_t* stages = smem + L.stage;
 
-    // ---- weight ring: first fill before waiting on the previous kernel
+    // ---- weight ring: whole fill issued before waiting on the previous kernel
     if (tid == 0) {
         for (int s = 0; s < nst; ++s) mbar_init(&bar[s], 1);
         fence_mbar_init();
@@ -107,205 +222,141 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
             bulk_g2s_stream(stages + size_t(i) * tb, p.w + size_t(t0 + i) * tb, tb, &bar[i], pol);
         }
     }
+    const bool norm = p.in_kind != IN_F32;
+    // norm weights of this warp's groups (constants): fetched before the wait
+    uint2 nwv[GPW];
+#pragma unroll
+    for (int j = 0; j < GPW; ++j) {
+        const int grp = warp + j * kGemvWarps;
+        nwv[j] = (norm && grp < G) ? *reinterpret_cast<const uint2*>(p.norm_w + size_t(grp) * 128 + lane * 4)
+                                   : make_uint2(0, 0);
+    }
     pdl_launch_dependents();
     pdl_wait();
 
-    // ---- prologue: x rows -> (RMSNorm) -> fp16 (scaled) in B-fragment order, group sums
-    const int segs = K >> 3;
-    const int nit = (segs + kThreads - 1) / kThreads;   // <= 4 (K <= 8192)
-    const bool norm = p.in_kind != IN_F32;
-    for (int i = tid; i < G * (8 - MB); i += kThreads) xs[(i / (8 - MB)) * 8 + MB + i % (8 - MB)] = 0.f;
-    for (int m = 0; m < MB; ++m) {
-        if (m >= p.M) {
-            for (int i = tid; i < G; i += kThreads) xs[i * 8 + m] = 0.f;
-            continue;
-        }
-        float v[4][8];
-        float ss = 0.f, amax = 0.f;
+    // ---- stage x for this warp's groups: lane l holds inputs 4l..4l+3 of each group
+    float ss[MB];
 #pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int sg = it * kThreads + tid;
+    for (int m = 0; m < MB; ++m) ss[m] = 0.f;
+    float4 xv[GPW][MB];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[it][e] = 0.f;
-            if (it < nit && sg < segs) {
-                if (p.in_kind == IN_EMBED_NORM) {
-                    int tok = p.tokens[m];
-                    if (tok < 0 || tok >= p.vocab) {
-                        if (sg == 0) set_error(p.err, KMR_ERR_INVALID_ARG);
-                        tok = 0;
-                    }
-                    const uint4 raw = *reinterpret_cast<const uint4*>(p.embed + size_t(tok) * K + size_t(sg) * 8);
-                    const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+    for (int j = 0; j < GPW; ++j) {
+        const int grp = warp + j * kGemvWarps;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        v[it][2 * e] = bf16_lo(rw[e]);
-                        v[it][2 * e + 1] = bf16_hi(rw[e]);
-                    }
-                    if (c == 0 && p.x_out) {
-                        float4* xo = reinterpret_cast<float4*>(p.x_out + size_t(m) * K + size_t(sg) * 8);
-                        xo[0] = make_float4(v[it][0], v[it][1], v[it][2], v[it][3]);
-                        xo[1] = make_float4(v[it][4], v[it][5], v[it][6], v[it][7]);
-                    }
-                } else {
-                    const float4* xp = reinterpret_cast<const float4*>(p.x + size_t(m) * K + size_t(sg) * 8);
-                    const float4 a = xp[0], b = xp[1];
-                    v[it][0] = a.x; v[it][1] = a.y; v[it][2] = a.z; v[it][3] = a.w;
-                    v[it][4] = b.x; v[it][5] = b.y; v[it][6] = b.z; v[it][7] = b.w;
+        for (int m = 0; m < MB; ++m) {
+            xv[j][m] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (grp >= G || m >= p.M) continue;
+            const size_t k = size_t(grp) * 128 + lane * 4;
+            if (p.in_kind == IN_EMBED_NORM) {
+                int tok = p.tokens[m];
+                if (tok < 0 || tok >= p.vocab) {
+                    if (lane == 0 && grp == 0) set_error(p.err, KMR_ERR_INVALID_ARG);
+                    tok = 0;
                 }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    ss = __fmaf_rn(v[it][e], v[it][e], ss);
-                    if (norm) v[it][e] = __fmul_rn(v[it][e], bf16_to_f32(p.norm_w[sg * 8 + e]));
-                    amax = fmaxf(amax, fabsf(v[it][e]));
-                }
+                const uint2 raw = *reinterpret_cast<const uint2*>(p.embed + size_t(tok) * K + k);
+                xv[j][m] = make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
+                if (c == 0 && p.x_out) *reinterpret_cast<float4*>(p.x_out + size_t(m) * K + k) = xv[j][m];
+            } else {
+                xv[j][m] = *reinterpret_cast<const float4*>(p.x + size_t(m) * K + k);
             }
         }
-        // one block reduction for both the sum of squares and the largest |x * w|
-        ss = warp_sum(ss);
-        amax = warp_max(amax);
-        if (lane == 0) {
-            red[warp] = ss;
-            red[8 + warp] = amax;
-        }
-        __syncthreads();
-        float tot = 0.f, mx = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            tot += red[i];
-            mx = fmaxf(mx, red[8 + i]);
-        }
-        __syncthreads();
-        const float r = norm ? rsqrtf(tot / float(K) + p.eps) : 1.f;
-        if (norm) mx = __fmul_rn(mx, r);
-        float sigma = 1.f;
-        if (mx > 0.f && mx < 3.0e38f) {
-            int ex;
-            frexpf(mx, &ex);                       // mx < 2^ex
-            sigma = ldexpf(1.f, max(-100, min(100, 13 - ex)));
-        }
-        __half* xrow = xh + size_t(m) * (K + 8);
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            if (it >= nit) break;
-            const int sg = it * kThreads + tid;
-            float gs = 0.f;
-            if (sg < segs) {
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    // (x * r) * w, then the exact power-of-two scale
-                    const float f0 = norm ? __fmul_rn(v[it][e], r) : v[it][e];
-                    const float f1 = norm ? __fmul_rn(v[it][e + 1], r) : v[it][e + 1];
-                    const __half a = __float2half_rn(__fmul_rn(f0, sigma));
-                    const __half b = __float2half_rn(__fmul_rn(f1, sigma));
-                    gs = __fadd_rn(gs, __fadd_rn(__half2float(a), __half2float(b)));
-                    *reinterpret_cast<__half2*>(xrow + xpos(sg * 8 + e)) = __halves2half2(a, b);
-                }
-            }
-            // 16 consecutive threads cover one group of 128 inputs
-            gs += __shfl_xor_sync(0xffffffffu, gs, 1);
-            gs += __shfl_xor_sync(0xffffffffu, gs, 2);
-            gs += __shfl_xor_sync(0xffffffffu, gs, 4);
-            gs += __shfl_xor_sync(0xffffffffu, gs, 8);
-            if ((tid & 15) == 0 && sg < segs) xs[(sg >> 4) * 8 + m] = gs;
-        }
-        if (tid == 0) isig[m] = 1.f / sigma;
     }
-    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < GPW; ++j) {
+        const int grp = warp + j * kGemvWarps;
+        const float w0 = bf16_lo(nwv[j].x), w1 = bf16_hi(nwv[j].x), w2 = bf16_lo(nwv[j].y), w3 = bf16_hi(nwv[j].y);
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            float u[4] = {xv[j][m].x, xv[j][m].y, xv[j][m].z, xv[j][m].w};
+            if (norm) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) ss[m] = __fmaf_rn(u[e], u[e], ss[m]);
+                u[0] = __fmul_rn(u[0], w0);
+                u[1] = __fmul_rn(u[1], w1);
+                u[2] = __fmul_rn(u[2], w2);
+                u[3] = __fmul_rn(u[3], w3);
+            }
+            // per-(row, group) power-of-two scale from the group's largest |u|
+            const float sig = pow2_scale(warp_max(fmaxf(fmaxf(fabsf(u[0]), fabsf(u[1])),
+                                                        fmaxf(fabsf(u[2]), fabsf(u[3])))));
+            const __half2 h01 = __floats2half2_rn(__fmul_rn(u[0], sig), __fmul_rn(u[1], sig));
+            const __half2 h23 = __floats2half2_rn(__fmul_rn(u[2], sig), __fmul_rn(u[3], sig));
+            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+            const float gsum = warp_sum(__fadd_rn(__fadd_rn(f01.x, f01.y), __fadd_rn(f23.x, f23.y)));
+            __half* blk = xw + size_t(j * MB + m) * 128;
+            *reinterpret_cast<__half2*>(blk + bpos(lane * 4)) = h01;
+            *reinterpret_cast<__half2*>(blk + bpos(lane * 4 + 2)) = h23;
+            if (lane == 0 && grp < G) {
+                xst[j * 16 + m * 2] = gsum;
+                xst[j * 16 + m * 2 + 1] = 1.f / sig;
+            }
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int m = MB; m < 8; ++m) xst[j * 16 + m * 2] = xst[j * 16 + m * 2 + 1] = 0.f;
+        }
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int m = 0; m < 8; ++m) ssw[warp * 8 + m] = 0.f;
+    }
+#pragma unroll
+    for (int m = 0; m < MB; ++m) {
+        const float tot = warp_sum(ss[m]);
+        if (lane == 0) ssw[warp * 8 + m] = tot;
+    }
+    __syncwarp();
 
-    // ---- main loop: all warps on one tile at a time; warp w takes groups w, w+8, ...
-    const int g = lane >> 2, t = lane & 3;
+    // ---- products: every warp runs its groups of every tile, no block barrier until the end
+    const int g = lane >> 2;
     const bool bload = g < p.M;
-    const __half* xrow = xh + size_t(bload ? g : 0) * (K + 8);
+    constexpr int WS = 16 * MB;                    // floats per warp partial
+    auto tile_products = [&](const uint8_t* st, float (&acc)[4]) {
+#pragma unroll
+        for (int j = 0; j < GPW; ++j) {
+            const int grp = warp + j * kGemvWarps;
+            if (grp < G)
+                group_product(st + size_t(grp) * kGroupBytes, xw + size_t(j * MB + (bload ? g : 0)) * 128, bload,
+                              lane, xst + j * 16, acc);
+        }
+    };
+    if (nt <= nst) {
+        for (int tl = 0; tl < nt; ++tl) {
+            mbar_wait(&bar[tl], 0u, p.err);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            tile_products(stages + size_t(tl) * tb, acc);
+            store_part<MB>(part + (size_t(tl) * kGemvWarps + warp) * WS, lane, acc);
+        }
+        __syncthreads();
+        const int per = (p.epi == EPI_SILU ? 8 : 16) * MB;
+        for (int idx = tid; idx < nt * per; idx += kGemvThreads) {
+            const int tl = idx / per;
+            tile_epilogue<MB>(p, part + size_t(tl) * kGemvWarps * WS, t0 + tl, idx - tl * per, ssw);
+        }
+        return;
+    }
+    // ---- ring: one tile at a time, a barrier per tile frees its stage
     for (int i = 0; i < nt; ++i) {
         const int s = i % nst;
         mbar_wait(&bar[s], uint32_t((i / nst) & 1), p.err);
-        const uint8_t* st = stages + size_t(s) * tb;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int grp = warp; grp < G; grp += 8) {
-            const uint8_t* gb = st + size_t(grp) * 1088;
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int blk = 0; blk < 2; ++blk) {
-                const uint4 wq = *reinterpret_cast<const uint4*>(gb + blk * 512 + lane * 16);
-                uint4 xa = make_uint4(0, 0, 0, 0), xb = make_uint4(0, 0, 0, 0);
-                if (bload) {
-                    const uint4* xp = reinterpret_cast<const uint4*>(xrow + (grp * 2 + blk) * 64 + t * 16);
-                    xa = xp[0];
-                    xb = xp[1];
-                }
-                const uint32_t w4[4] = {wq.x, wq.y, wq.z, wq.w};
-                const uint32_t bx[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t w = w4[ks], w2 = w >> 8;
-                    mma16816(d, and_or(w, 0x000F000Fu, 0x64006400u), and_or(w, 0x00F000F0u, 0x64006400u),
-                             and_or(w2, 0x000F000Fu, 0x64006400u), and_or(w2, 0x00F000F0u, 0x64006400u),
-                             bx[2 * ks], bx[2 * ks + 1]);
-                }
-            }
-            // fold offset, -8 and zero point: rows g (x1) and g+8 (x16), batch cols 2t, 2t+1
-            const uint32_t sz0 = *reinterpret_cast<const uint32_t*>(gb + 1024 + g * 4);
-            const uint32_t sz1 = *reinterpret_cast<const uint32_t*>(gb + 1024 + (g + 8) * 4);
-            const float2 X = *reinterpret_cast<const float2*>(xs + grp * 8 + 2 * t);
-            const float s0 = bf16_lo(sz0), z0 = bf16_hi(sz0), s1 = bf16_lo(sz1), z1 = bf16_hi(sz1);
-            const float s1c = __fmul_rn(s1, 0.0625f);
-            const float zz0 = __fmaf_rn(-8.f, s0, z0), zz1 = __fmaf_rn(-8.f, s1, z1);
-            const float x0 = 1024.f * X.x, x1 = 1024.f * X.y;
-            acc[0] = __fadd_rn(acc[0], __fmaf_rn(s0, __fsub_rn(d[0], x0), __fmul_rn(zz0, X.x)));
-            acc[1] = __fadd_rn(acc[1], __fmaf_rn(s0, __fsub_rn(d[1], x1), __fmul_rn(zz0, X.y)));
-            acc[2] = __fadd_rn(acc[2], __fmaf_rn(s1c, __fsub_rn(d[2], x0), __fmul_rn(zz1, X.x)));
-            acc[3] = __fadd_rn(acc[3], __fmaf_rn(s1c, __fsub_rn(d[3], x1), __fmul_rn(zz1, X.y)));
-        }
-        float* wp = part + (size_t(s) * 8 + warp) * 128;
-        wp[g * 8 + 2 * t] = acc[0];
-        wp[g * 8 + 2 * t + 1] = acc[1];
-        wp[(g + 8) * 8 + 2 * t] = acc[2];
-        wp[(g + 8) * 8 + 2 * t + 1] = acc[3];
+        tile_products(stages + size_t(s) * tb, acc);
+        store_part<MB>(part + (size_t(s) * kGemvWarps + warp) * WS, lane, acc);
         __syncthreads();
-        // stage s is free again: refill it with tile i + nst while the epilogue runs
         if (tid == 0 && i + nst < nt) {
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(&bar[s], tb);
             bulk_g2s_stream(stages + size_t(s) * tb, p.w + size_t(t0 + i + nst) * tb, tb, &bar[s],
                             policy_evict_first());
         }
-        // ---- epilogue: fixed-order sum over the 8 warps
-        const int tile = t0 + i;
-        const float* ps = part + size_t(s) * 8 * 128;
-        if (p.epi == EPI_SILU) {
-            if (tid < 8 * MB) {
-                const int j = tid / MB, m = tid % MB;
-                const int jj = tile * 8 + j;
-                if (m < p.M && jj < p.N / 2) {
-                    float gv = 0.f, uv = 0.f;
-#pragma unroll
-                    for (int w = 0; w < 8; ++w) {
-                        gv = __fadd_rn(gv, ps[w * 128 + j * 8 + m]);
-                        uv = __fadd_rn(uv, ps[w * 128 + (j + 8) * 8 + m]);
-                    }
-                    gv = __fmul_rn(gv, isig[m]);
-                    uv = __fmul_rn(uv, isig[m]);
-                    p.y[size_t(m) * p.ldy + jj] = __fmul_rn(__fdiv_rn(gv, __fadd_rn(1.f, expf(-gv))), uv);
-                }
-            }
-        } else if (tid < 16 * MB) {
-            const int r = tid / MB, m = tid % MB;
-            const int n = tile * 16 + r;
-            if (m < p.M && n < p.N) {
-                float v = 0.f;
-#pragma unroll
-                for (int w = 0; w < 8; ++w) v = __fadd_rn(v, ps[w * 128 + r * 8 + m]);
-                v = __fmul_rn(v, isig[m]);
-                float* yp = p.y + size_t(m) * p.ldy + n;
-                *yp = (p.epi == EPI_RESID) ? __fadd_rn(*yp, v) : v;
-            }
-        }
+        tile_epilogue<MB>(p, part + size_t(s) * kGemvWarps * WS, t0 + i, tid, ssw);
     }
 }
 
 }  // namespace
 
 int gemv_pick_mb(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
+static int gemv_gpw(int K) { return ((K >> 7) + kGemvWarps - 1) / kGemvWarps; }
 
 // At most one CTA per SM, each owning ceil(tiles / SMs) whole tiles (the last
 // CTA may own fewer), never more CTAs than tiles.
@@ -323,14 +374,37 @@ int gemv_nstage(int tiles, int grid, int tile_bytes) {
     return n < 1 ? 1 : n;
 }
 size_t gemv_smem_bytes(int MB, int K, int tile_bytes, int nstage) {
-    return gemv_layout(MB, K, tile_bytes, nstage).total;
+    return gemv_layout(MB, gemv_gpw(K), tile_bytes, nstage).total;
 }
 
-template <int MB>
-static cudaError_t launch_mb(const GemvParams& p, int grid, cudaStream_t st, bool pdl) {
+template <int MB, int GPW>
+static const void* gemv_fn() { return (const void*)gemv_kernel<MB, GPW>; }
+
+static const void* gemv_fn_for(int MB, int GPW) {
+    switch (MB * 8 + GPW) {
+        case 1 * 8 + 1: return gemv_fn<1, 1>();
+        case 1 * 8 + 2: return gemv_fn<1, 2>();
+        case 1 * 8 + 3: return gemv_fn<1, 3>();
+        case 1 * 8 + 4: return gemv_fn<1, 4>();
+        case 2 * 8 + 1: return gemv_fn<2, 1>();
+        case 2 * 8 + 2: return gemv_fn<2, 2>();
+        case 2 * 8 + 3: return gemv_fn<2, 3>();
+        case 2 * 8 + 4: return gemv_fn<2, 4>();
+        case 4 * 8 + 1: return gemv_fn<4, 1>();
+        case 4 * 8 + 2: return gemv_fn<4, 2>();
+        case 4 * 8 + 3: return gemv_fn<4, 3>();
+        case 4 * 8 + 4: return gemv_fn<4, 4>();
+        case 8 * 8 + 1: return gemv_fn<8, 1>();
+        case 8 * 8 + 2: return gemv_fn<8, 2>();
+        case 8 * 8 + 3: return gemv_fn<8, 3>();
+        default: return gemv_fn<8, 4>();
+    }
+}
+
+cudaError_t launch_gemv(const GemvParams& p, int MB, int grid, cudaStream_t st, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kGemvThreads);
     cfg.dynamicSmemBytes = gemv_smem_bytes(MB, p.K, p.tile_bytes, p.nstage);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -338,28 +412,22 @@ static cudaError_t launch_mb(const GemvParams& p, int grid, cudaStream_t st, boo
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<MB>, p);
-}
-
-cudaError_t launch_gemv(const GemvParams& p, int MB, int grid, cudaStream_t st, bool pdl) {
-    switch (MB) {
-        case 1: return launch_mb<1>(p, grid, st, pdl);
-        case 2: return launch_mb<2>(p, grid, st, pdl);
-        case 4: return launch_mb<4>(p, grid, st, pdl);
-        default: return launch_mb<8>(p, grid, st, pdl);
-    }
+    GemvParams q = p;
+    void* args[] = {&q};
+    return cudaLaunchKernelExC(&cfg, gemv_fn_for(MB, gemv_gpw(p.K)), args);
 }
 
 cudaError_t gemv_set_attributes() {
     const int mx = 227 * 1024;
-    const void* ks[4] = {(const void*)gemv_kernel<1>, (const void*)gemv_kernel<2>, (const void*)gemv_kernel<4>,
-                         (const void*)gemv_kernel<8>};
-    for (const void* k : ks) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) return e;
-    }
+    const int mbs[4] = {1, 2, 4, 8};
+    for (int mb : mbs)
+        for (int gpw = 1; gpw <= 4; ++gpw) {
+            const void* k = gemv_fn_for(mb, gpw);
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+            if (e != cudaSuccess) return e;
+        }
     return cudaSuccess;
 }
 

@@ -221,12 +221,18 @@ struct AttnParams {
     int sec0, sec1;              // frequencies [0,sec0) follow T, [sec0, sec0+sec1) follow H, rest W
     int B, nq, nkv, d, S, slots;
     float scale;
-    int tsplit;                  // grid.x: largest number of splits per (row, kv head)
+    int tsplit;                  // grid.x (global merge): largest number of splits per (row, kv head)
+    int cluster;                 // 1: splits of a (row, kv head) form one cluster, merged through DSMEM
     float* out;                  // [B][nq*d]
     float* part;                 // [B][nkv][tsplit][rep][d+2]
     int* counters;               // [B][nkv]
     int* err;
 };
+// Shared-memory poisoning diagnostic (kmr_poison.cu).
+cudaError_t poison_set_attributes();
+cudaError_t launch_smem_poison(uint32_t pattern, int sms, cudaStream_t st);
+
+constexpr int kAttnClusterSplits = 8;     // cluster size of the DSMEM-merged attention (portable)
 size_t attn_smem_bytes(int d, int rep);
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t st, bool pdl);
 size_t attn_workspace_bytes(int B, int nq, int nkv, int d, int tsplit);

@@ -59,11 +59,13 @@ def test_device_pack_bit_exact(torch, N, K, flags):
 
 
 # ------------------------------------------------------------------ int4 GEMV
-def _gemv(torch, packed, N, K, x, epi=kmr.KMR_EPI_NONE, flags=0, y0=None):
+def _gemv(torch, packed, N, K, x, epi=kmr.KMR_EPI_NONE, flags=0, y0=None, poison=None):
     M = x.shape[0]
     ncol = N // 2 if epi == kmr.KMR_EPI_SILU_MUL else N
     y = torch.from_numpy(y0).cuda() if y0 is not None else torch.zeros((M, ncol), dtype=torch.float32, device="cuda")
     xd = torch.from_numpy(np.ascontiguousarray(x, np.float32)).cuda()
+    if poison is not None:
+        kmr.kmr_smem_poison(poison, torch.cuda.current_stream())
     kmr.kmr_int4_gemv(packed, N, K, 128, flags, xd, M, y, epi, torch.cuda.current_stream())
     torch.cuda.synchronize()
     assert kmr.kmr_last_device_error() == 0
@@ -157,8 +159,28 @@ def test_int4_gemv_deterministic_and_batch_invariant(torch):
     assert np.array_equal(_gemv(torch, packed, N, K, x[4:8]), y16[4:8])
 
 
+# Shared memory filled with NaN / Inf / large-value bits before the launch must not change a
+# single output bit: no kernel may read shared memory it did not write in the same launch.
+POISON_PATTERNS = (0xFFFFFFFF, 0x7F807F80, 0x7BFF7BFF)
+
+
+@pytest.mark.parametrize("N,K,M,epi", [(13, 256, 3, kmr.KMR_EPI_NONE), (768, 768, 1, kmr.KMR_EPI_NONE),
+                                       (4096, 2048, 4, kmr.KMR_EPI_RESIDUAL), (2048, 6144, 8, kmr.KMR_EPI_NONE),
+                                       (512, 256, 5, kmr.KMR_EPI_SILU_MUL), (12288, 2048, 2, kmr.KMR_EPI_SILU_MUL)])
+def test_int4_gemv_ignores_stale_shared_memory(torch, N, K, M, epi):
+    flags = kmr.KMR_PACK_GATE_UP if epi == kmr.KMR_EPI_SILU_MUL else 0
+    q, s, z = _canon(3 * N + K, N, K)
+    packed = _device_pack(torch, q, s, z, flags)
+    x = np.random.default_rng(N + M).standard_normal((M, K)).astype(np.float32)
+    y0 = np.random.default_rng(1).standard_normal((M, N)).astype(np.float32) if epi == kmr.KMR_EPI_RESIDUAL else None
+    clean = _gemv(torch, packed, N, K, x, epi, flags, y0)
+    assert np.all(np.isfinite(clean))
+    for pat in POISON_PATTERNS:
+        assert np.array_equal(_gemv(torch, packed, N, K, x, epi, flags, y0, poison=pat), clean), hex(pat)
+
+
 # ------------------------------------------------------------------ decode attention
-def _attn_case(torch, B, nq, nkv, d, S, slots, cpos, slot_ids, seed=0):
+def _attn_case(torch, B, nq, nkv, d, S, slots, cpos, slot_ids, seed=0, poison=None):
     r = np.random.default_rng(seed)
     q = r.standard_normal((B, nq, d)).astype(np.float32)
     kc = np.full((slots, nkv, S, d), BF16_NAN, np.uint16)
@@ -172,9 +194,11 @@ def _attn_case(torch, B, nq, nkv, d, S, slots, cpos, slot_ids, seed=0):
     out = torch.zeros((B, nq, d), dtype=torch.float32, device="cuda")
     dk = torch.from_numpy(kc.view(np.int16)).cuda()
     dv = torch.from_numpy(vc.view(np.int16)).cuda()
+    if poison is not None:
+        kmr.kmr_smem_poison(poison, torch.cuda.current_stream())
     kmr.kmr_decode_attn(torch.from_numpy(q).cuda(), dk, dv, torch.tensor(slot_ids, dtype=torch.int32, device="cuda"),
                         torch.tensor(cpos, dtype=torch.int32, device="cuda"), B, nq, nkv, d, S, slots,
-                        1.0 / math.sqrt(d), out, ws, ws_bytes)
+                        1.0 / math.sqrt(d), out, ws, ws_bytes, torch.cuda.current_stream())
     torch.cuda.synchronize()
     err = kmr.kmr_last_device_error()
     cnt_bytes = (B * nkv * 4 + 15) // 16 * 16
@@ -212,6 +236,16 @@ def test_decode_attn_single_token_and_determinism(torch):
     assert rel_l2(out, ref) <= 1e-5
     again, _, _ = _attn_case(torch, 3, 16, 8, 128, 64, 3, [0, 40, 63], [2, 0, 1], seed=5)
     assert np.array_equal(out, again)
+
+
+def test_decode_attn_ignores_stale_shared_memory(torch):
+    cpos = [0, 6, 15, 16, 70, 127, 1000]          # lone last positions, exact splits, ragged tails
+    args = (torch, len(cpos), 16, 4, 128, 1024, len(cpos), cpos, list(range(len(cpos))))
+    clean, ref, err = _attn_case(*args, seed=11)
+    assert err == 0 and np.all(np.isfinite(clean)) and rel_l2(clean, ref) <= 1e-4
+    for pat in POISON_PATTERNS:
+        out, _, err = _attn_case(*args, seed=11, poison=pat)
+        assert err == 0 and np.array_equal(out, clean), hex(pat)
 
 
 def test_decode_attn_bad_rows_flag_errors(torch):

@@ -237,6 +237,32 @@ def test_batch_invariance_and_determinism(torch):
     m2.close()
 
 
+def test_step_ignores_stale_shared_memory(torch):
+    """Every kernel of the step preceded by a shared-memory fill of NaN / Inf bits gives the
+    same step bit for bit (rows 1 and 2 end their last split on a lone position)."""
+    from workloads import Workload
+    cfg = tiny_config(slots=4)
+    wl = Workload("tiny b4", cfg, 0, batch=4, prefill=[10, 38, 70, 127], rope_delta=[0, -3, -7, 0],
+                  slot_ids=[2, 0, 3, 1], first_tokens=[5, 77, 300, 1000], steps=1)
+    m, _ = build_model(wl, max_batch=4)
+    st = od.initial_state(wl)
+    clean = Dev(torch, *st, cfg.vocab)
+    clean.step(m)
+    ref = clean.host()
+    assert np.all(np.isfinite(ref[4]))
+    base = m.kernels_per_step(4)
+    for pat in (0xFFFFFFFF, 0x7F807F80):
+        m.set_smem_poison(True, pat)
+        assert m.kernels_per_step(4) == 2 * base
+        dev = Dev(torch, *st, cfg.vocab)
+        dev.step(m)
+        for a, b in zip(dev.host(), ref):
+            assert np.array_equal(a, b), hex(pat)
+    m.set_smem_poison(False)
+    assert m.kernels_per_step(4) == base
+    m.close()
+
+
 # ------------------------------------------------------------------ 2B-shaped workloads
 def test_single_2b_layer_step(torch):
     wl = layer2b_workload()
