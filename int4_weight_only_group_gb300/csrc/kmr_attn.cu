@@ -18,15 +18,25 @@
 // fixed per call site — it depends only on the row's own length, never on the
 // batch, so a row's result is the same at any batch size.  Each CTA streams its
 // K and V positions with cp.async.bulk (contiguous in the [slot][head][pos][d]
-// layout) into a 2-stage ring whose first fill is issued before
-// griddepcontrol.wait.  Every warp runs its own online softmax over its
-// positions (two at a time, no block barrier inside the loop); the 8 warp
-// states merge in shared memory, then the splits merge in split order:
-//   * cluster mode: the splits of one (row, KV head) are one thread-block
-//     cluster; the merge reads the peers' shared memory (DSMEM) after a
-//     cluster barrier — no global memory, no atomics;
-//   * global mode: each split writes its state to a caller workspace and the
-//     last CTA to arrive (atomic counter) merges — for any number of splits.
+// layout) into a ring of shared-memory stages whose first fill is issued,
+// together with the RoPE angles, before griddepcontrol.wait.
+//   * Scoring: a warp takes 8 positions at a time.  Every lane holds d/32
+//     dimensions of each query head and forms partial dot products for all 8
+//     positions and all heads of the group; one reduce-scatter over the warp
+//     (halving the values held at each shuffle level) leaves each lane one
+//     complete score, so 8 x heads scores cost about as many shuffles as full
+//     butterflies would for one or two.  Online softmax in base 2 (log2(e)
+//     folded into the query scale), no block barrier inside the loop.
+//   * Merge: the 8 warp states merge in shared memory; then the splits merge
+//     in split order:
+//       - cluster mode: the splits of one (row, KV head) are one thread-block
+//         cluster; every split pushes its state for output slice r into CTA
+//         r's shared memory (distributed shared memory stores), one cluster
+//         barrier, and each CTA merges its slice from local memory — no
+//         global memory, no atomics, no remote loads on the critical path;
+//       - global mode: each split writes its state to a caller workspace and
+//         the last CTA to arrive (atomic counter) merges — for any number of
+//         splits.
 #include <cooperative_groups.h>
 #include <math.h>
 
@@ -38,41 +48,75 @@ namespace kmr {
 
 namespace {
 
-constexpr int kSub = 64;       // positions per ring stage
-constexpr int kStages = 2;
-constexpr int kMaxRep = 4;     // query heads per KV head supported
+constexpr int kSub = 64;            // positions per ring stage: 8 warps x 8
+constexpr int kChunk = 8;           // positions a warp scores at once
+constexpr int kMaxStages = 4;
+constexpr int kMaxRep = 4;          // query heads per KV head supported
+constexpr float kLog2e = 1.4426950408889634f;
 
 __host__ __device__ inline size_t al16a(size_t v) { return (v + 15) & ~size_t(15); }
 
 struct AttnSmem {
-    size_t bar, kst, vst, knew, vnew, qs, wml, wo, cml, co, flag, total;
+    size_t bar, kst, vst, knew, vnew, qs, wml, wo, co, cml, recv, flag, total;
 };
-__host__ __device__ inline AttnSmem attn_layout(int D, int rep) {
+__host__ __device__ inline AttnSmem attn_layout(int D, int rep, int nstage) {
     AttnSmem L;
+    const int per = rep * D / 8;                                // output slice merged by each cluster rank
     size_t o = 0;
-    L.bar = o;   o += al16a(kStages * 8);
+    L.bar = o;   o += al16a(kMaxStages * 8);
     o = (o + 127) & ~size_t(127);
-    L.kst = o;   o += size_t(kStages) * kSub * D * 2;
-    L.vst = o;   o += size_t(kStages) * kSub * D * 2;
+    L.kst = o;   o += size_t(nstage) * kSub * D * 2;
+    L.vst = o;   o += size_t(nstage) * kSub * D * 2;
     L.knew = o;  o += al16a(size_t(D) * 2);
     L.vnew = o;  o += al16a(size_t(D) * 2);
     L.qs = o;    o += al16a(size_t(rep) * D * 4);
-    L.wml = o;   o += al16a(size_t(8) * kMaxRep * 2 * 4);     // per warp: (m, l) per head
-    L.wo = o;    o += al16a(size_t(8) * rep * D * 4);         // per warp: o per head
-    L.cml = o;   o += al16a(size_t(kMaxRep) * 2 * 4);         // CTA state: (m, l) per head
-    L.co = o;    o += al16a(size_t(rep) * D * 4);             // CTA state: o per head
+    L.wml = o;   o += al16a(size_t(8) * kMaxRep * 2 * 4);      // per warp: (m, l) per head
+    L.wo = o;    o += al16a(size_t(8) * rep * D * 4);          // per warp: o per head
+    L.co = o;    o += al16a(size_t(rep) * D * 4);              // CTA state (global mode)
+    L.cml = o;   o += al16a(size_t(kMaxRep) * 2 * 4);
+    L.recv = o;  o += al16a(size_t(8) * (per + 2) * 4);        // per source rank: (m, l, slice)
     L.flag = o;  o += 16;
     L.total = o;
     return L;
 }
 
+// Sum of NV per-lane values over the warp, scattered: value i's total ends on the
+// lanes l with l / (32 / NV) == i.  Fixed shuffle order, so deterministic.
+template <int NV>
+__device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
+    int n = NV;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        if (n > 1) {
+            const int half = n / 2;
+            const bool up = (lane & off) != 0;
+#pragma unroll
+            for (int i = 0; i < NV / 2; ++i) {
+                if (i < half) {
+                    const float keep = up ? v[i + half] : v[i];
+                    const float send = up ? v[i] : v[i + half];
+                    v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, off));
+                }
+            }
+            n = half;
+        } else {
+            v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xffffffffu, v[0], off));
+        }
+    }
+    return v[0];
+}
+
 template <int D, int REP, bool CLUSTER>
 __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int EPL = D / 32;               // contiguous dims per lane
+    constexpr int NV = REP * kChunk;          // partial scores per lane before the reduce-scatter
+    constexpr int JS = 32 / NV;               // lanes sharing one score after it
+    constexpr int PER = REP * D / 8;          // output slice per cluster rank
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int EPL = D / 32;          // contiguous dims per lane
-    const AttnSmem L = attn_layout(D, REP);
+    const int nst = p.nstage;
+    const AttnSmem L = attn_layout(D, REP, nst);
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
     uint16_t* kst = reinterpret_cast<uint16_t*>(smem + L.kst);
     uint16_t* vst = reinterpret_cast<uint16_t*>(smem + L.vst);
@@ -81,12 +125,14 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     float* qs = reinterpret_cast<float*>(smem + L.qs);
     float* wml = reinterpret_cast<float*>(smem + L.wml);
     float* wo = reinterpret_cast<float*>(smem + L.wo);
-    float* cml = reinterpret_cast<float*>(smem + L.cml);
     float* co = reinterpret_cast<float*>(smem + L.co);
+    float* cml = reinterpret_cast<float*>(smem + L.cml);
+    float* recv = reinterpret_cast<float*>(smem + L.recv);
     int* flag = reinterpret_cast<int*>(smem + L.flag);
 
-    // Row state comes from the previous step (complete before this graph ran), not
-    // from the kernels of this step, so it may be read before griddepcontrol.wait.
+    // Row state (and the positions) come from the previous step, complete before
+    // this graph ran, not from the kernels of this step, so they may be read
+    // before griddepcontrol.wait.
     const bool fin = p.finished != nullptr && p.finished[b] != 0;
     const int slot = p.slot_ids[b], cp = p.cpos[b];
     const bool bad_slot = slot < 0 || slot >= p.slots;
@@ -104,7 +150,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     const int Lq = cp + 1;
     const int chunk = (((Lq + nsplit - 1) / nsplit) + 15) & ~15;
     const int ns = (Lq + chunk - 1) / chunk;
-    if (!CLUSTER && s >= ns) return;             // (cluster mode: empty splits still join the barriers)
+    if (!CLUSTER && s >= ns) return;             // (cluster mode: empty splits still merge a slice)
     const int t0 = s * chunk, t1 = min(Lq, t0 + chunk);      // t1 <= t0 for an empty split
     const int cached_end = p.fused ? min(t1, cp) : t1;
     const int nsub = t1 > t0 ? (t1 - t0 + kSub - 1) / kSub : 0;
@@ -113,12 +159,12 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     const uint16_t* vbase = p.vc + headoff;
 
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) mbar_init(&bar[i], 1);
+        for (int i = 0; i < nst; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
     }
     __syncthreads();
     auto issue = [&](int st) {
-        const int sb = st % kStages;
+        const int sb = st % nst;
         const int pa = t0 + st * kSub;
         const int pb = min(pa + kSub, cached_end);
         const int np = pb > pa ? pb - pa : 0;
@@ -132,27 +178,28 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
         }
     };
     if (tid == 0) {
-        const int n0 = nsub < kStages ? nsub : kStages;
+        const int n0 = nsub < nst ? nsub : nst;
         for (int i = 0; i < n0; ++i) issue(i);
     }
-    // constants of the prologue, fetched before the wait as well
+    // constants of the prologue, and the RoPE angles of this row's positions, before the wait
     const bool qk_warp = p.fused && warp <= REP;
-    float nw[EPL], invf[EPL];
-    int axis[EPL];
+    float nw[EPL], cs[EPL], sn[EPL];
     if (qk_warp) {
         const uint16_t* nrm = warp < REP ? p.qn_w : p.kn_w;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) {
             const int dim = lane * EPL + e, f = dim % (D / 2);
             nw[e] = nrm ? bf16_to_f32(nrm[dim]) : 1.f;
-            invf[e] = p.inv_freq[f];
-            axis[e] = f < p.sec0 ? 0 : (f < p.sec0 + p.sec1 ? 1 : 2);
+            const int axis = f < p.sec0 ? 0 : (f < p.sec0 + p.sec1 ? 1 : 2);
+            const float pos = float(p.positions[size_t(axis) * p.pos_ld + b]);
+            sincosf(pos * p.inv_freq[f], &sn[e], &cs[e]);
         }
     }
     pdl_launch_dependents();
     pdl_wait();
 
     // ---- prologue: q (and, fused, the new k / v) of this KV head
+    const float qscale = __fmul_rn(p.scale, kLog2e);       // scores in base 2
     const float* in = p.in + size_t(b) * p.in_ld;
     if (p.fused) {
         if (warp <= REP + 1) {
@@ -178,16 +225,13 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
 #pragma unroll
                 for (int e = 0; e < EPL; ++e) {
                     const float other = __shfl_xor_sync(0xffffffffu, x[e], 16);
-                    const float pos = float(p.positions[size_t(axis[e]) * p.pos_ld + b]);
-                    float sn, cs;
-                    sincosf(pos * invf[e], &sn, &cs);
-                    x[e] = lo ? __fsub_rn(__fmul_rn(x[e], cs), __fmul_rn(other, sn))
-                              : __fadd_rn(__fmul_rn(x[e], cs), __fmul_rn(other, sn));
+                    x[e] = lo ? __fsub_rn(__fmul_rn(x[e], cs[e]), __fmul_rn(other, sn[e]))
+                              : __fadd_rn(__fmul_rn(x[e], cs[e]), __fmul_rn(other, sn[e]));
                 }
             }
             if (isq) {
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) qs[warp * D + lane * EPL + e] = __fmul_rn(x[e], p.scale);
+                for (int e = 0; e < EPL; ++e) qs[warp * D + lane * EPL + e] = __fmul_rn(x[e], qscale);
             } else {
                 uint16_t* dst = isk ? knew : vnew;
                 uint16_t* cache = isk ? p.kc : p.vc;
@@ -200,11 +244,11 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
             }
         }
     } else {
-        for (int i = tid; i < REP * D; i += kThreads) qs[i] = __fmul_rn(in[size_t(h) * REP * D + i], p.scale);
+        for (int i = tid; i < REP * D; i += kThreads) qs[i] = __fmul_rn(in[size_t(h) * REP * D + i], qscale);
     }
     __syncthreads();
 
-    // ---- per-warp online softmax over positions t0 + warp + 8 i, two at a time
+    // ---- per-warp online softmax, 8 positions at a time
     float qreg[REP][EPL];
 #pragma unroll
     for (int hh = 0; hh < REP; ++hh)
@@ -227,67 +271,85 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
             v[0] = bf16_lo(u); v[1] = bf16_hi(u);
         }
     };
+    const int myidx = lane / JS;                 // (head, position) of the score this lane completes
+    const int myhh = myidx / kChunk, myj = myidx % kChunk;
     for (int st = 0; st < nsub; ++st) {
-        const int sb = st % kStages;
-        mbar_wait(&bar[sb], uint32_t((st / kStages) & 1), p.err);
+        const int sb = st % nst;
+        mbar_wait(&bar[sb], uint32_t((st / nst) & 1), p.err);
         const int pa = t0 + st * kSub;
-        const int np = min(kSub, t1 - pa);
-        const uint16_t* ks = kst + size_t(sb) * kSub * D;
-        const uint16_t* vs = vst + size_t(sb) * kSub * D;
-        for (int i = warp; i < np; i += 16) {
-            const bool two = i + 8 < np;
-            const int i1 = two ? i + 8 : i;       // a lone last position pairs with itself (weight 0)
-            const uint16_t* k0 = (p.fused && pa + i == cp) ? knew : ks + size_t(i) * D;
-            const uint16_t* k1 = (p.fused && pa + i1 == cp) ? knew : ks + size_t(i1) * D;
-            float ka[EPL], kb[EPL];
-            load_row(k0, ka);
-            load_row(k1, kb);
-            float s0[REP], s1[REP];
+        const int np = min(kSub, t1 - pa);       // positions of this stage, the new one included
+        const int c0 = warp * kChunk;
+        if (c0 < np) {
+            const int nv = min(kChunk, np - c0);
+            const uint16_t* ks = kst + size_t(sb) * kSub * D;
+            const uint16_t* vs = vst + size_t(sb) * kSub * D;
+            // rows past the end of the chunk re-read its first row (weight 0 below)
+            auto krow = [&](int j) {
+                const int i = c0 + (j < nv ? j : 0);
+                return (p.fused && pa + i == cp) ? knew : ks + size_t(i) * D;
+            };
+            auto vrow = [&](int j) {
+                const int i = c0 + (j < nv ? j : 0);
+                return (p.fused && pa + i == cp) ? vnew : vs + size_t(i) * D;
+            };
+            float sc[NV];
 #pragma unroll
-            for (int hh = 0; hh < REP; ++hh) {
-                float a = 0.f, c = 0.f;
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) {
-                    a = __fmaf_rn(qreg[hh][e], ka[e], a);
-                    c = __fmaf_rn(qreg[hh][e], kb[e], c);
-                }
-                s0[hh] = a;
-                s1[hh] = c;
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
+            for (int j = 0; j < kChunk; ++j) {
+                float kv[EPL];
+                load_row(krow(j), kv);
 #pragma unroll
                 for (int hh = 0; hh < REP; ++hh) {
-                    s0[hh] += __shfl_xor_sync(0xffffffffu, s0[hh], off);
-                    s1[hh] += __shfl_xor_sync(0xffffffffu, s1[hh], off);
+                    float a = 0.f;
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) a = __fmaf_rn(qreg[hh][e], kv[e], a);
+                    sc[hh * kChunk + j] = a;
                 }
-            const uint16_t* v0 = (p.fused && pa + i == cp) ? vnew : vs + size_t(i) * D;
-            const uint16_t* v1 = (p.fused && pa + i1 == cp) ? vnew : vs + size_t(i1) * D;
-            float va[EPL], vb[EPL];
-            load_row(v0, va);
-            load_row(v1, vb);
+            }
+            const float mine = reduce_scatter<NV>(sc, lane);
+            const bool valid = myj < nv;
+            const float sv = valid ? mine : -INFINITY;
+            // chunk maximum per head: butterfly over the lanes of the same head
+            float cm = sv;
+#pragma unroll
+            for (int off = JS; off < JS * kChunk; off <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+            float mn[REP], cf[REP], mymn = 0.f;
 #pragma unroll
             for (int hh = 0; hh < REP; ++hh) {
-                const float mn = fmaxf(m[hh], two ? fmaxf(s0[hh], s1[hh]) : s0[hh]);
-                const float cf = (m[hh] == -INFINITY) ? 0.f : expf(m[hh] - mn);
-                const float p0 = expf(s0[hh] - mn);
-                const float p1 = two ? expf(s1[hh] - mn) : 0.f;
-                l[hh] = __fadd_rn(__fmaf_rn(l[hh], cf, p0), p1);
+                const float cmh = __shfl_sync(0xffffffffu, cm, hh * kChunk * JS);
+                mn[hh] = fmaxf(m[hh], cmh);
+                cf[hh] = (m[hh] == -INFINITY) ? 0.f : exp2f(__fsub_rn(m[hh], mn[hh]));
+                if (hh == myhh) mymn = mn[hh];
+            }
+            const float pme = valid ? exp2f(__fsub_rn(sv, mymn)) : 0.f;
 #pragma unroll
-                for (int e = 0; e < EPL; ++e)
-                    o[hh][e] = __fmaf_rn(p1, vb[e], __fmaf_rn(p0, va[e], __fmul_rn(o[hh][e], cf)));
-                m[hh] = mn;
+            for (int hh = 0; hh < REP; ++hh) {
+                l[hh] = __fmul_rn(l[hh], cf[hh]);
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) o[hh][e] = __fmul_rn(o[hh][e], cf[hh]);
+                m[hh] = mn[hh];
+            }
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) {
+                float vv[EPL];
+                load_row(vrow(j), vv);
+#pragma unroll
+                for (int hh = 0; hh < REP; ++hh) {
+                    const float pj = __shfl_sync(0xffffffffu, pme, (hh * kChunk + j) * JS);
+                    l[hh] = __fadd_rn(l[hh], pj);
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) o[hh][e] = __fmaf_rn(pj, vv[e], o[hh][e]);
+                }
             }
         }
-        if (st + kStages < nsub) {
+        if (st + nst < nsub) {
             __syncthreads();                      // every warp is done with this stage
             if (tid == 0) {
                 fence_proxy_async_smem();
-                issue(st + kStages);
+                issue(st + nst);
             }
         }
     }
-    // ---- merge the 8 warps (fixed order) into the CTA state
+    // ---- merge the 8 warps (fixed order)
 #pragma unroll
     for (int hh = 0; hh < REP; ++hh) {
         if (lane == 0) {
@@ -308,39 +370,46 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
 #pragma unroll
             for (int w = 0; w < 8; ++w) {
                 const float mw = wml[(w * kMaxRep + hh) * 2];
-                const float wt = (mw == -INFINITY) ? 0.f : expf(mw - mx);
+                const float wt = (mw == -INFINITY) ? 0.f : exp2f(__fsub_rn(mw, mx));
                 den = __fmaf_rn(wt, wml[(w * kMaxRep + hh) * 2 + 1], den);
                 num = __fmaf_rn(wt, wo[(size_t(w) * REP + hh) * D + dim], num);
             }
         }
-        co[hh * D + dim] = num;
-        if (dim == 0) {
-            cml[hh * 2] = mx;
-            cml[hh * 2 + 1] = den;
+        if constexpr (CLUSTER) {
+            // push this split's state for output i to the rank that merges i's slice
+            if (s < ns) {
+                const int dest = i / PER, k = i % PER;
+                float* r = cg::this_cluster().map_shared_rank(recv, dest) + s * (PER + 2);
+                r[2 + k] = num;
+                if (k == 0) {
+                    r[0] = mx;
+                    r[1] = den;
+                }
+            }
+        } else {
+            co[i] = num;
+            if (dim == 0) {
+                cml[hh * 2] = mx;
+                cml[hh * 2 + 1] = den;
+            }
         }
     }
     if constexpr (CLUSTER) {
-        // ---- merge the splits of this (row, KV head) through distributed shared memory
-        cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();
-        const int per = (REP * D + nsplit - 1) / nsplit;       // outputs merged by each rank
-        for (int i = tid; i < per; i += kThreads) {
-            const int oi = s * per + i;
-            if (oi >= REP * D) break;
-            const int hh = oi / D, dim = oi % D;
+        // ---- every split's state for this rank's slice is now in local shared memory
+        cg::this_cluster().sync();
+        for (int k = tid; k < PER; k += kThreads) {
             float mx = -INFINITY;
-            for (int r = 0; r < ns; ++r) mx = fmaxf(mx, cluster.map_shared_rank(cml, r)[hh * 2]);
+            for (int r = 0; r < ns; ++r) mx = fmaxf(mx, recv[r * (PER + 2)]);
             float num = 0.f, den = 0.f;
             for (int r = 0; r < ns; ++r) {
-                const float* rml = cluster.map_shared_rank(cml, r);
-                const float mr = rml[hh * 2];
-                const float wt = (mr == -INFINITY) ? 0.f : expf(mr - mx);
-                den = __fmaf_rn(wt, rml[hh * 2 + 1], den);
-                num = __fmaf_rn(wt, cluster.map_shared_rank(co, r)[hh * D + dim], num);
+                const float* rr = recv + r * (PER + 2);
+                const float mr = rr[0];
+                const float wt = (mr == -INFINITY) ? 0.f : exp2f(__fsub_rn(mr, mx));
+                den = __fmaf_rn(wt, rr[1], den);
+                num = __fmaf_rn(wt, rr[2 + k], num);
             }
-            outrow[oi] = __fdiv_rn(num, den);
+            outrow[s * PER + k] = __fdiv_rn(num, den);
         }
-        cluster.sync();                           // peers' shared memory stays alive until read
     } else {
         // ---- global mode: one split writes directly; otherwise the last CTA merges
         __syncthreads();
@@ -376,7 +445,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
             for (int q = 0; q < ns; ++q) {
                 const float* pq = parts + (size_t(q) * REP + hh) * (D + 2);
                 const float mq = __ldcg(&pq[0]);
-                const float wt = (mq == -INFINITY) ? 0.f : expf(mq - mx);
+                const float wt = (mq == -INFINITY) ? 0.f : exp2f(__fsub_rn(mq, mx));
                 den = __fmaf_rn(wt, __ldcg(&pq[1]), den);
                 num = __fmaf_rn(wt, __ldcg(&pq[2 + dim]), num);
             }
@@ -399,7 +468,14 @@ const void* attn_fn(int d, int rep) {
 
 }  // namespace
 
-size_t attn_smem_bytes(int d, int rep) { return attn_layout(d, rep).total; }
+// Ring depth: enough stages for the longest split the cache allows, at most kMaxStages.
+int attn_stages(int max_len, int splits) {
+    if (splits < 1) splits = 1;
+    const int chunk = (((max_len + splits - 1) / splits) + 15) & ~15;
+    const int sub = (chunk + kSub - 1) / kSub;
+    return sub < 1 ? 1 : (sub > kMaxStages ? kMaxStages : sub);
+}
+size_t attn_smem_bytes(int d, int rep, int nstage) { return attn_layout(d, rep, nstage).total; }
 int attn_default_tsplit(int nkv) {
     int t = (num_sms() + nkv - 1) / nkv;
     return t < 1 ? 1 : (t > 32 ? 32 : t);
@@ -410,10 +486,13 @@ size_t attn_workspace_bytes(int B, int nq, int nkv, int d, int tsplit) {
 
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t st, bool pdl) {
     const int rep = p.nq / p.nkv;
+    AttnParams q = p;
+    if (p.cluster) q.tsplit = kAttnClusterSplits;
+    q.nstage = attn_stages(p.S, q.tsplit);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.cluster ? kAttnClusterSplits : p.tsplit, p.nkv, p.B);
+    cfg.gridDim = dim3(q.tsplit, p.nkv, p.B);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = attn_smem_bytes(p.d, rep);
+    cfg.dynamicSmemBytes = attn_smem_bytes(p.d, rep, q.nstage);
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     int n = 0;
@@ -431,8 +510,6 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t st, bool pdl) {
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    AttnParams q = p;
-    if (p.cluster) q.tsplit = kAttnClusterSplits;
     const void* fn = p.cluster ? attn_fn<true>(p.d, rep) : attn_fn<false>(p.d, rep);
     void* args[] = {&q};
     return cudaLaunchKernelExC(&cfg, fn, args);

@@ -222,6 +222,7 @@ struct AttnParams {
     int B, nq, nkv, d, S, slots;
     float scale;
     int tsplit;                  // grid.x (global merge): largest number of splits per (row, kv head)
+    int nstage;                  // K/V ring stages (set by launch_attn from S and the split count)
     int cluster;                 // 1: splits of a (row, kv head) form one cluster, merged through DSMEM
     float* out;                  // [B][nq*d]
     float* part;                 // [B][nkv][tsplit][rep][d+2]
@@ -233,7 +234,8 @@ cudaError_t poison_set_attributes();
 cudaError_t launch_smem_poison(uint32_t pattern, int sms, cudaStream_t st);
 
 constexpr int kAttnClusterSplits = 8;     // cluster size of the DSMEM-merged attention (portable)
-size_t attn_smem_bytes(int d, int rep);
+size_t attn_smem_bytes(int d, int rep, int nstage);
+int attn_stages(int max_len, int splits);
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t st, bool pdl);
 size_t attn_workspace_bytes(int B, int nq, int nkv, int d, int tsplit);
 int attn_default_tsplit(int nkv);
