@@ -69,8 +69,7 @@ __host__ __device__ inline GemvSmem gemv_layout(int MB, int GPW, int tile_bytes,
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -84,39 +83,61 @@ __device__ __forceinline__ int bpos(int kk) {
     return (kk >> 6) * 64 + ((j & 7) >> 1) * 16 + ((kk >> 4) & 3) * 4 + (j >> 3) * 2 + (j & 1);
 }
 
-// 2^(13 - floor(log2 a)) for a > 0 finite (a * sigma < 2^14), else 1.
-__device__ __forceinline__ float pow2_scale(float a) {
-    if (!(a > 0.f && a <= 3.4e38f)) return 1.f;
-    const int ex = int((__float_as_uint(a) >> 23) & 0xFFu) - 127;
-    return __uint_as_float(uint32_t(max(1, min(254, 127 + 13 - ex))) << 23);
+// sigma = 2^(13 - floor(log2 a)) (so a * sigma lies in [2^13, 2^14)) and 1 / sigma, from the
+// bits of a = the group's largest |u|; 1 for a group of zeros, denormals or non-finite values.
+// Both are powers of two built from the exponent field: exact, and no division.
+__device__ __forceinline__ void pow2_scale(uint32_t abits, float& sig, float& isig) {
+    const int e = int(abits >> 23);                        // biased exponent (abits has no sign bit)
+    if (e == 0 || e >= 255) {
+        sig = isig = 1.f;
+        return;
+    }
+    const int se = max(1, min(253, 267 - e));              // 127 + 13 - (e - 127), clamped
+    sig = __uint_as_float(uint32_t(se) << 23);
+    isig = __uint_as_float(uint32_t(254 - se) << 23);
 }
 
-// One (16-row tile, 128-input group) block: 8 tensor-core k-steps on four independent
-// accumulator chains, then the fold for rows g (x1) and g+8 (x16) and batch columns
-// 2t, 2t+1.  xb: the group's staged halves of batch row g; st: (X', 1/sigma) per row.
-__device__ __forceinline__ void group_product(const uint8_t* gb, const __half* xb, bool bload, int lane,
-                                              const float* st, float (&acc)[4]) {
-    const int g = lane >> 2, t = lane & 3;
-    float d[4][4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) d[c][0] = d[c][1] = d[c][2] = d[c][3] = 0.f;
+// The B fragments of one staged group for this lane (batch row g, both 64-input blocks)
+// and the fold constants (X'_{2t}, 1/sigma_{2t}, X'_{2t+1}, 1/sigma_{2t+1}); loaded once
+// per group and reused for every tile.
+struct XFrag {
+    uint32_t b[16];
+    float4 X;
+};
+__device__ __forceinline__ void load_xfrag(XFrag& f, const __half* xb, bool bload, int lane, const float* st) {
+    const int t = lane & 3;
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
-        const uint4 wq = *reinterpret_cast<const uint4*>(gb + blk * 512 + lane * 16);
         uint4 xa = make_uint4(0, 0, 0, 0), xc = make_uint4(0, 0, 0, 0);
         if (bload) {
             const uint4* xp = reinterpret_cast<const uint4*>(xb + blk * 64 + t * 16);
             xa = xp[0];
             xc = xp[1];
         }
+        f.b[blk * 8 + 0] = xa.x; f.b[blk * 8 + 1] = xa.y; f.b[blk * 8 + 2] = xa.z; f.b[blk * 8 + 3] = xa.w;
+        f.b[blk * 8 + 4] = xc.x; f.b[blk * 8 + 5] = xc.y; f.b[blk * 8 + 6] = xc.z; f.b[blk * 8 + 7] = xc.w;
+    }
+    f.X = *reinterpret_cast<const float4*>(st + 4 * t);
+}
+
+// One (16-row tile, 128-input group) block: 8 tensor-core k-steps on four independent
+// accumulator chains, then the fold for rows g (x1) and g+8 (x16) and batch columns
+// 2t, 2t+1.
+__device__ __forceinline__ void group_product(const uint8_t* gb, const XFrag& xf, int lane, float (&acc)[4]) {
+    const int g = lane >> 2;
+    float d[4][4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) d[c][0] = d[c][1] = d[c][2] = d[c][3] = 0.f;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+        const uint4 wq = *reinterpret_cast<const uint4*>(gb + blk * 512 + lane * 16);
         const uint32_t w4[4] = {wq.x, wq.y, wq.z, wq.w};
-        const uint32_t bx[8] = {xa.x, xa.y, xa.z, xa.w, xc.x, xc.y, xc.z, xc.w};
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
             const uint32_t w = w4[ks], w2 = w >> 8;
             mma16816(d[ks], and_or(w, 0x000F000Fu, 0x64006400u), and_or(w, 0x00F000F0u, 0x64006400u),
-                     and_or(w2, 0x000F000Fu, 0x64006400u), and_or(w2, 0x00F000F0u, 0x64006400u), bx[2 * ks],
-                     bx[2 * ks + 1]);
+                     and_or(w2, 0x000F000Fu, 0x64006400u), and_or(w2, 0x00F000F0u, 0x64006400u),
+                     xf.b[blk * 8 + 2 * ks], xf.b[blk * 8 + 2 * ks + 1]);
         }
     }
     float D[4];
@@ -124,7 +145,7 @@ __device__ __forceinline__ void group_product(const uint8_t* gb, const __half* x
     for (int i = 0; i < 4; ++i) D[i] = __fadd_rn(__fadd_rn(d[0][i], d[1][i]), __fadd_rn(d[2][i], d[3][i]));
     const uint32_t sz0 = *reinterpret_cast<const uint32_t*>(gb + 1024 + g * 4);
     const uint32_t sz1 = *reinterpret_cast<const uint32_t*>(gb + 1024 + (g + 8) * 4);
-    const float4 X = *reinterpret_cast<const float4*>(st + 4 * t);       // (X'_{2t}, is_{2t}, X'_{2t+1}, is_{2t+1})
+    const float4 X = xf.X;                                                // (X'_{2t}, is_{2t}, X'_{2t+1}, is_{2t+1})
     const float s0 = bf16_lo(sz0), z0 = bf16_hi(sz0), s1 = bf16_lo(sz1), z1 = bf16_hi(sz1);
     const float s1c = __fmul_rn(s1, 0.0625f);
     const float zz0 = __fmaf_rn(-8.f, s0, z0), zz1 = __fmaf_rn(-8.f, s1, z1);
@@ -192,8 +213,10 @@ __device__ __forceinline__ void tile_epilogue(const GemvParams& p, const float* 
     }
 }
 
+// Two CTAs per SM (so the next GEMV of the step can be resident and prefetching) where the
+// staging registers allow it.
 template <int MB, int GPW>
-__global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(kGemvThreads, (MB * GPW <= 8) ? 2 : 1) gemv_kernel(const GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int P = gridDim.x, c = blockIdx.x;
@@ -276,9 +299,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
                 u[2] = __fmul_rn(u[2], w2);
                 u[3] = __fmul_rn(u[3], w3);
             }
-            // per-(row, group) power-of-two scale from the group's largest |u|
-            const float sig = pow2_scale(warp_max(fmaxf(fmaxf(fabsf(u[0]), fabsf(u[1])),
-                                                        fmaxf(fabsf(u[2]), fabsf(u[3])))));
+            // per-(row, group) power-of-two scale from the group's largest |u| (one redux:
+            // the bits of non-negative floats order like unsigned integers)
+            const float la = fmaxf(fmaxf(fabsf(u[0]), fabsf(u[1])), fmaxf(fabsf(u[2]), fabsf(u[3])));
+            float sig, isig;
+            pow2_scale(__reduce_max_sync(0xffffffffu, __float_as_uint(la)), sig, isig);
             const __half2 h01 = __floats2half2_rn(__fmul_rn(u[0], sig), __fmul_rn(u[1], sig));
             const __half2 h23 = __floats2half2_rn(__fmul_rn(u[2], sig), __fmul_rn(u[3], sig));
             const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
@@ -288,7 +313,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
             *reinterpret_cast<__half2*>(blk + bpos(lane * 4 + 2)) = h23;
             if (lane == 0 && grp < G) {
                 xst[j * 16 + m * 2] = gsum;
-                xst[j * 16 + m * 2 + 1] = 1.f / sig;
+                xst[j * 16 + m * 2 + 1] = isig;
             }
         }
         if (lane == 0) {
@@ -311,18 +336,32 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
     const int g = lane >> 2;
     const bool bload = g < p.M;
     constexpr int WS = 16 * MB;                    // floats per warp partial
+    // One group per warp (K <= 2048): its x fragments stay in registers across tiles.
+    // More groups per warp: reloaded from shared memory per tile (registers would
+    // otherwise keep two CTAs from sharing an SM).
+    XFrag xf1;
+    if (GPW == 1 && warp < G) load_xfrag(xf1, xw + size_t(bload ? g : 0) * 128, bload, lane, xst);
     auto tile_products = [&](const uint8_t* st, float (&acc)[4]) {
+        if constexpr (GPW == 1) {
+            if (warp < G) group_product(st + size_t(warp) * kGroupBytes, xf1, lane, acc);
+        } else {
 #pragma unroll
-        for (int j = 0; j < GPW; ++j) {
-            const int grp = warp + j * kGemvWarps;
-            if (grp < G)
-                group_product(st + size_t(grp) * kGroupBytes, xw + size_t(j * MB + (bload ? g : 0)) * 128, bload,
-                              lane, xst + j * 16, acc);
+            for (int j = 0; j < GPW; ++j) {
+                const int grp = warp + j * kGemvWarps;
+                if (grp < G) {
+                    XFrag xf;
+                    load_xfrag(xf, xw + size_t(j * MB + (bload ? g : 0)) * 128, bload, lane, xst + j * 16);
+                    group_product(st + size_t(grp) * kGroupBytes, xf, lane, acc);
+                }
+            }
         }
     };
     if (nt <= nst) {
+        // every tile was requested before griddepcontrol.wait; with all of them in, the
+        // product loop has no wait between tiles and the compiler may overlap them
+        for (int tl = 0; tl < nt; ++tl) mbar_wait(&bar[tl], 0u, p.err);
+#pragma unroll 1
         for (int tl = 0; tl < nt; ++tl) {
-            mbar_wait(&bar[tl], 0u, p.err);
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             tile_products(stages + size_t(tl) * tb, acc);
             store_part<MB>(part + (size_t(tl) * kGemvWarps + warp) * WS, lane, acc);
