@@ -398,15 +398,26 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
         // ---- every split's state for this rank's slice is now in local shared memory
         cg::this_cluster().sync();
         for (int k = tid; k < PER; k += kThreads) {
+            // all sources' states first (independent loads), then the fixed-order sums
+            float mr[kAttnClusterSplits], lr[kAttnClusterSplits], nr[kAttnClusterSplits];
             float mx = -INFINITY;
-            for (int r = 0; r < ns; ++r) mx = fmaxf(mx, recv[r * (PER + 2)]);
+#pragma unroll
+            for (int r = 0; r < kAttnClusterSplits; ++r) {
+                mr[r] = -INFINITY;
+                lr[r] = nr[r] = 0.f;
+                if (r < ns) {
+                    mr[r] = recv[r * (PER + 2)];
+                    lr[r] = recv[r * (PER + 2) + 1];
+                    nr[r] = recv[r * (PER + 2) + 2 + k];
+                }
+                mx = fmaxf(mx, mr[r]);
+            }
             float num = 0.f, den = 0.f;
-            for (int r = 0; r < ns; ++r) {
-                const float* rr = recv + r * (PER + 2);
-                const float mr = rr[0];
-                const float wt = (mr == -INFINITY) ? 0.f : exp2f(__fsub_rn(mr, mx));
-                den = __fmaf_rn(wt, rr[1], den);
-                num = __fmaf_rn(wt, rr[2 + k], num);
+#pragma unroll
+            for (int r = 0; r < kAttnClusterSplits; ++r) {
+                const float wt = (mr[r] == -INFINITY) ? 0.f : exp2f(__fsub_rn(mr[r], mx));
+                den = __fmaf_rn(wt, lr[r], den);
+                num = __fmaf_rn(wt, nr[r], num);
             }
             outrow[s * PER + k] = __fdiv_rn(num, den);
         }

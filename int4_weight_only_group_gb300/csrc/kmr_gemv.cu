@@ -36,6 +36,7 @@
 //     other rows or on M.
 #include <cuda_fp16.h>
 
+#include "kmr_int4_mma.cuh"
 #include "kmr_internal.cuh"
 
 namespace kmr {
@@ -67,94 +68,6 @@ __host__ __device__ inline GemvSmem gemv_layout(int MB, int GPW, int tile_bytes,
     return L;
 }
 
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// Position (in halves) of group-local input kk (0..127) in B-fragment order: two blocks
-// of 64; inside a block, lane slot t (16 halves) holds for each of its 4 k-steps
-// (k0 = 16 step) the inputs (k0+2t, k0+2t+1, k0+2t+8, k0+2t+9).
-__device__ __forceinline__ int bpos(int kk) {
-    const int j = kk & 15;
-    return (kk >> 6) * 64 + ((j & 7) >> 1) * 16 + ((kk >> 4) & 3) * 4 + (j >> 3) * 2 + (j & 1);
-}
-
-// sigma = 2^(13 - floor(log2 a)) (so a * sigma lies in [2^13, 2^14)) and 1 / sigma, from the
-// bits of a = the group's largest |u|; 1 for a group of zeros, denormals or non-finite values.
-// Both are powers of two built from the exponent field: exact, and no division.
-__device__ __forceinline__ void pow2_scale(uint32_t abits, float& sig, float& isig) {
-    const int e = int(abits >> 23);                        // biased exponent (abits has no sign bit)
-    if (e == 0 || e >= 255) {
-        sig = isig = 1.f;
-        return;
-    }
-    const int se = max(1, min(253, 267 - e));              // 127 + 13 - (e - 127), clamped
-    sig = __uint_as_float(uint32_t(se) << 23);
-    isig = __uint_as_float(uint32_t(254 - se) << 23);
-}
-
-// The B fragments of one staged group for this lane (batch row g, both 64-input blocks)
-// and the fold constants (X'_{2t}, 1/sigma_{2t}, X'_{2t+1}, 1/sigma_{2t+1}); loaded once
-// per group and reused for every tile.
-struct XFrag {
-    uint32_t b[16];
-    float4 X;
-};
-__device__ __forceinline__ void load_xfrag(XFrag& f, const __half* xb, bool bload, int lane, const float* st) {
-    const int t = lane & 3;
-#pragma unroll
-    for (int blk = 0; blk < 2; ++blk) {
-        uint4 xa = make_uint4(0, 0, 0, 0), xc = make_uint4(0, 0, 0, 0);
-        if (bload) {
-            const uint4* xp = reinterpret_cast<const uint4*>(xb + blk * 64 + t * 16);
-            xa = xp[0];
-            xc = xp[1];
-        }
-        f.b[blk * 8 + 0] = xa.x; f.b[blk * 8 + 1] = xa.y; f.b[blk * 8 + 2] = xa.z; f.b[blk * 8 + 3] = xa.w;
-        f.b[blk * 8 + 4] = xc.x; f.b[blk * 8 + 5] = xc.y; f.b[blk * 8 + 6] = xc.z; f.b[blk * 8 + 7] = xc.w;
-    }
-    f.X = *reinterpret_cast<const float4*>(st + 4 * t);
-}
-
-// One (16-row tile, 128-input group) block: 8 tensor-core k-steps on four independent
-// accumulator chains, then the fold for rows g (x1) and g+8 (x16) and batch columns
-// 2t, 2t+1.
-__device__ __forceinline__ void group_product(const uint8_t* gb, const XFrag& xf, int lane, float (&acc)[4]) {
-    const int g = lane >> 2;
-    float d[4][4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) d[c][0] = d[c][1] = d[c][2] = d[c][3] = 0.f;
-#pragma unroll
-    for (int blk = 0; blk < 2; ++blk) {
-        const uint4 wq = *reinterpret_cast<const uint4*>(gb + blk * 512 + lane * 16);
-        const uint32_t w4[4] = {wq.x, wq.y, wq.z, wq.w};
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t w = w4[ks], w2 = w >> 8;
-            mma16816(d[ks], and_or(w, 0x000F000Fu, 0x64006400u), and_or(w, 0x00F000F0u, 0x64006400u),
-                     and_or(w2, 0x000F000Fu, 0x64006400u), and_or(w2, 0x00F000F0u, 0x64006400u),
-                     xf.b[blk * 8 + 2 * ks], xf.b[blk * 8 + 2 * ks + 1]);
-        }
-    }
-    float D[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) D[i] = __fadd_rn(__fadd_rn(d[0][i], d[1][i]), __fadd_rn(d[2][i], d[3][i]));
-    const uint32_t sz0 = *reinterpret_cast<const uint32_t*>(gb + 1024 + g * 4);
-    const uint32_t sz1 = *reinterpret_cast<const uint32_t*>(gb + 1024 + (g + 8) * 4);
-    const float4 X = xf.X;                                                // (X'_{2t}, is_{2t}, X'_{2t+1}, is_{2t+1})
-    const float s0 = bf16_lo(sz0), z0 = bf16_hi(sz0), s1 = bf16_lo(sz1), z1 = bf16_hi(sz1);
-    const float s1c = __fmul_rn(s1, 0.0625f);
-    const float zz0 = __fmaf_rn(-8.f, s0, z0), zz1 = __fmaf_rn(-8.f, s1, z1);
-    const float x0 = 1024.f * X.x, x1 = 1024.f * X.z;
-    acc[0] = __fmaf_rn(__fmaf_rn(s0, __fsub_rn(D[0], x0), __fmul_rn(zz0, X.x)), X.y, acc[0]);
-    acc[1] = __fmaf_rn(__fmaf_rn(s0, __fsub_rn(D[1], x1), __fmul_rn(zz0, X.z)), X.w, acc[1]);
-    acc[2] = __fmaf_rn(__fmaf_rn(s1c, __fsub_rn(D[2], x0), __fmul_rn(zz1, X.x)), X.y, acc[2]);
-    acc[3] = __fmaf_rn(__fmaf_rn(s1c, __fsub_rn(D[3], x1), __fmul_rn(zz1, X.z)), X.w, acc[3]);
-}
 
 // The warp's partial of one tile: rows g, g+8 and batch columns 2t, 2t+1 (< MB kept).
 template <int MB>
@@ -170,13 +83,22 @@ __device__ __forceinline__ void store_part(float* wp, int lane, const float (&ac
     }
 }
 
-// RMSNorm factor of row m from the per-warp sums of squares (fixed warp order).
+// Sum of the 16 per-warp values v[w * stride] as a fixed pairwise tree (depth 4).
+__device__ __forceinline__ float warp16_sum(const float* v, int stride) {
+    float a[kGemvWarps];
+#pragma unroll
+    for (int w = 0; w < kGemvWarps; ++w) a[w] = v[w * stride];
+#pragma unroll
+    for (int n = kGemvWarps / 2; n > 0; n >>= 1)
+#pragma unroll
+        for (int i = 0; i < n; ++i) a[i] = __fadd_rn(a[2 * i], a[2 * i + 1]);
+    return a[0];
+}
+
+// RMSNorm factor of row m from the per-warp sums of squares.
 __device__ __forceinline__ float norm_factor(const GemvParams& p, const float* ssw, int m) {
     if (p.in_kind == IN_F32) return 1.f;
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < kGemvWarps; ++w) tot = __fadd_rn(tot, ssw[w * 8 + m]);
-    return rsqrtf(tot / float(p.K) + p.eps);
+    return rsqrtf(warp16_sum(ssw + m, 8) / float(p.K) + p.eps);
 }
 
 // Epilogue of one tile: fixed-order sum of the warp partials, RMSNorm factor, store / add / SiLU-mul.
@@ -189,12 +111,7 @@ __device__ __forceinline__ void tile_epilogue(const GemvParams& p, const float* 
         const int j = idx / MB, m = idx % MB;
         const int jj = tile * 8 + j;
         if (m >= p.M || jj >= p.N / 2) return;
-        float gv = 0.f, uv = 0.f;
-#pragma unroll
-        for (int w = 0; w < kGemvWarps; ++w) {
-            gv = __fadd_rn(gv, ps[w * WS + j * MB + m]);
-            uv = __fadd_rn(uv, ps[w * WS + (j + 8) * MB + m]);
-        }
+        float gv = warp16_sum(ps + j * MB + m, WS), uv = warp16_sum(ps + (j + 8) * MB + m, WS);
         const float r = norm_factor(p, ssw, m);
         gv = __fmul_rn(gv, r);
         uv = __fmul_rn(uv, r);
@@ -204,10 +121,7 @@ __device__ __forceinline__ void tile_epilogue(const GemvParams& p, const float* 
         const int rr = idx / MB, m = idx % MB;
         const int n = tile * 16 + rr;
         if (m >= p.M || n >= p.N) return;
-        float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < kGemvWarps; ++w) v = __fadd_rn(v, ps[w * WS + rr * MB + m]);
-        v = __fmul_rn(v, norm_factor(p, ssw, m));
+        float v = __fmul_rn(warp16_sum(ps + rr * MB + m, WS), norm_factor(p, ssw, m));
         float* yp = p.y + size_t(m) * p.ldy + n;
         *yp = (p.epi == EPI_RESID) ? __fadd_rn(*yp, v) : v;
     }
@@ -239,10 +153,16 @@ __global__ void __launch_bounds__(kGemvThreads, (MB * GPW <= 8) ? 2 : 1) gemv_ke
     __syncthreads();
     if (tid == 0) {
         const uint64_t pol = policy_evict_first();
-        const int n0 = nt < nst ? nt : nst;
-        for (int i = 0; i < n0; ++i) {
-            mbar_arrive_expect_tx(&bar[i], tb);
-            bulk_g2s_stream(stages + size_t(i) * tb, p.w + size_t(t0 + i) * tb, tb, &bar[i], pol);
+        if (nt <= nst) {
+            // every tile fits: one barrier counts all of them (nt * tb < 2^20 bytes)
+            mbar_arrive_expect_tx(&bar[0], uint32_t(nt) * tb);
+            for (int i = 0; i < nt; ++i)
+                bulk_g2s_stream(stages + size_t(i) * tb, p.w + size_t(t0 + i) * tb, tb, &bar[0], pol);
+        } else {
+            for (int i = 0; i < nst; ++i) {
+                mbar_arrive_expect_tx(&bar[i], tb);
+                bulk_g2s_stream(stages + size_t(i) * tb, p.w + size_t(t0 + i) * tb, tb, &bar[i], pol);
+            }
         }
     }
     const bool norm = p.in_kind != IN_F32;
@@ -257,10 +177,9 @@ __global__ void __launch_bounds__(kGemvThreads, (MB * GPW <= 8) ? 2 : 1) gemv_ke
     pdl_launch_dependents();
     pdl_wait();
 
-    // ---- stage x for this warp's groups: lane l holds inputs 4l..4l+3 of each group
-    float ss[MB];
-#pragma unroll
-    for (int m = 0; m < MB; ++m) ss[m] = 0.f;
+    // ---- stage x for this warp's groups: lane l holds inputs 4l..4l+3 of each group.
+    // Loads first, then every (group, row)'s arithmetic, then all warp reductions
+    // together (independent, so their latencies overlap), then the stores.
     float4 xv[GPW][MB];
 #pragma unroll
     for (int j = 0; j < GPW; ++j) {
@@ -284,9 +203,13 @@ __global__ void __launch_bounds__(kGemvThreads, (MB * GPW <= 8) ? 2 : 1) gemv_ke
             }
         }
     }
+    float ss[MB];
+#pragma unroll
+    for (int m = 0; m < MB; ++m) ss[m] = 0.f;
+    __half2 h01[GPW][MB], h23[GPW][MB];
+    float gs[GPW][MB], isg[GPW][MB];
 #pragma unroll
     for (int j = 0; j < GPW; ++j) {
-        const int grp = warp + j * kGemvWarps;
         const float w0 = bf16_lo(nwv[j].x), w1 = bf16_hi(nwv[j].x), w2 = bf16_lo(nwv[j].y), w3 = bf16_hi(nwv[j].y);
 #pragma unroll
         for (int m = 0; m < MB; ++m) {
@@ -302,18 +225,34 @@ __global__ void __launch_bounds__(kGemvThreads, (MB * GPW <= 8) ? 2 : 1) gemv_ke
             // per-(row, group) power-of-two scale from the group's largest |u| (one redux:
             // the bits of non-negative floats order like unsigned integers)
             const float la = fmaxf(fmaxf(fabsf(u[0]), fabsf(u[1])), fmaxf(fabsf(u[2]), fabsf(u[3])));
-            float sig, isig;
-            pow2_scale(__reduce_max_sync(0xffffffffu, __float_as_uint(la)), sig, isig);
-            const __half2 h01 = __floats2half2_rn(__fmul_rn(u[0], sig), __fmul_rn(u[1], sig));
-            const __half2 h23 = __floats2half2_rn(__fmul_rn(u[2], sig), __fmul_rn(u[3], sig));
-            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-            const float gsum = warp_sum(__fadd_rn(__fadd_rn(f01.x, f01.y), __fadd_rn(f23.x, f23.y)));
+            float sig;
+            pow2_scale(__reduce_max_sync(0xffffffffu, __float_as_uint(la)), sig, isg[j][m]);
+            h01[j][m] = __floats2half2_rn(__fmul_rn(u[0], sig), __fmul_rn(u[1], sig));
+            h23[j][m] = __floats2half2_rn(__fmul_rn(u[2], sig), __fmul_rn(u[3], sig));
+            const float2 f01 = __half22float2(h01[j][m]), f23 = __half22float2(h23[j][m]);
+            gs[j][m] = __fadd_rn(__fadd_rn(f01.x, f01.y), __fadd_rn(f23.x, f23.y));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+        for (int j = 0; j < GPW; ++j)
+#pragma unroll
+            for (int m = 0; m < MB; ++m) gs[j][m] = __fadd_rn(gs[j][m], __shfl_xor_sync(0xffffffffu, gs[j][m], off));
+#pragma unroll
+        for (int m = 0; m < MB; ++m) ss[m] = __fadd_rn(ss[m], __shfl_xor_sync(0xffffffffu, ss[m], off));
+    }
+#pragma unroll
+    for (int j = 0; j < GPW; ++j) {
+        const int grp = warp + j * kGemvWarps;
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
             __half* blk = xw + size_t(j * MB + m) * 128;
-            *reinterpret_cast<__half2*>(blk + bpos(lane * 4)) = h01;
-            *reinterpret_cast<__half2*>(blk + bpos(lane * 4 + 2)) = h23;
+            *reinterpret_cast<__half2*>(blk + bpos(lane * 4)) = h01[j][m];
+            *reinterpret_cast<__half2*>(blk + bpos(lane * 4 + 2)) = h23[j][m];
             if (lane == 0 && grp < G) {
-                xst[j * 16 + m * 2] = gsum;
-                xst[j * 16 + m * 2 + 1] = isig;
+                xst[j * 16 + m * 2] = gs[j][m];
+                xst[j * 16 + m * 2 + 1] = isg[j][m];
             }
         }
         if (lane == 0) {
@@ -323,12 +262,7 @@ __global__ void __launch_bounds__(kGemvThreads, (MB * GPW <= 8) ? 2 : 1) gemv_ke
     }
     if (lane == 0) {
 #pragma unroll
-        for (int m = 0; m < 8; ++m) ssw[warp * 8 + m] = 0.f;
-    }
-#pragma unroll
-    for (int m = 0; m < MB; ++m) {
-        const float tot = warp_sum(ss[m]);
-        if (lane == 0) ssw[warp * 8 + m] = tot;
+        for (int m = 0; m < 8; ++m) ssw[warp * 8 + m] = m < MB ? ss[m] : 0.f;
     }
     __syncwarp();
 
@@ -359,7 +293,7 @@ __global__ void __launch_bounds__(kGemvThreads, (MB * GPW <= 8) ? 2 : 1) gemv_ke
     if (nt <= nst) {
         // every tile was requested before griddepcontrol.wait; with all of them in, the
         // product loop has no wait between tiles and the compiler may overlap them
-        for (int tl = 0; tl < nt; ++tl) mbar_wait(&bar[tl], 0u, p.err);
+        mbar_wait(&bar[0], 0u, p.err);
 #pragma unroll 1
         for (int tl = 0; tl < nt; ++tl) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};

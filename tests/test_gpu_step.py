@@ -263,6 +263,28 @@ def test_step_ignores_stale_shared_memory(torch):
     m.close()
 
 
+@pytest.mark.parametrize("nq,nkv", [(4, 2), (8, 2), (4, 4), (8, 4)])
+def test_head_layouts(torch, nq, nkv):
+    """1, 2 and 4 query heads per KV head (head_dim 64) match the oracle over 3
+    teacher-forced steps at batch 3."""
+    from workloads import Workload
+    cfg = tiny_config(n_q_heads=nq, n_kv_heads=nkv, slots=3)
+    wl = Workload("tiny heads", cfg, 5, batch=3, prefill=[9, 40, 77], rope_delta=[0, -2, -5],
+                  slot_ids=[1, 2, 0], first_tokens=[3, 500, 77], steps=3)
+    m, _ = build_model(wl, max_batch=3)
+    assert m.kernels_per_step(3) == cfg.n_layers * 5 + 1
+    o = od.OracleDecoder.for_workload(wl)
+    st = od.initial_state(wl)
+    dev = Dev(torch, *st, cfg.vocab)
+    for t in range(wl.steps):
+        res = o.step(*st)
+        dev.step(m)
+        _check_step(res, dev.host(), wl.batch)
+        st = (res.next_ids, res.positions, res.cache_position, st[3], res.finished)
+        dev.set(tok=res.next_ids, fin=res.finished)
+    m.close()
+
+
 # ------------------------------------------------------------------ 2B-shaped workloads
 def test_single_2b_layer_step(torch):
     wl = layer2b_workload()
