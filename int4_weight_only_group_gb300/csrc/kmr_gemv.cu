@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kGemvThreads, (MB * GPW <= 8) ? 2 : 1) gemv_ke
     if (GPW == 1 && warp < G) load_xfrag(xf1, xw + size_t(bload ? g : 0) * 128, bload, lane, xst);
     auto tile_products = [&](const uint8_t* st, float (&acc)[4]) {
         if constexpr (GPW == 1) {
-            if (warp < G) group_product(st + size_t(warp) * kGroupBytes, xf1, lane, acc);
+            if (warp < G) group_product<(MB > 1)>(st + size_t(warp) * kGroupBytes, xf1, lane, acc);
         } else {
 #pragma unroll
             for (int j = 0; j < GPW; ++j) {
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kGemvThreads, (MB * GPW <= 8) ? 2 : 1) gemv_ke
                 if (grp < G) {
                     XFrag xf;
                     load_xfrag(xf, xw + size_t(j * MB + (bload ? g : 0)) * 128, bload, lane, xst + j * 16);
-                    group_product(st + size_t(grp) * kGroupBytes, xf, lane, acc);
+                    group_product<(MB > 1)>(st + size_t(grp) * kGroupBytes, xf, lane, acc);
                 }
             }
         }

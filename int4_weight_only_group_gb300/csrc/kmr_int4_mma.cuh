@@ -72,7 +72,8 @@ __device__ __forceinline__ void load_xfrag(XFrag& f, const __half* xb, bool bloa
 
 // One (16-row tile, 128-input group) block: 8 tensor-core k-steps on four independent
 // accumulator chains, then the fold for rows g (x1) and g+8 (x16) and batch columns
-// 2t, 2t+1.
+// 2t, 2t+1.  ODD = false skips the odd columns (one row of x: column 2t+1 never exists).
+template <bool ODD = true>
 __device__ __forceinline__ void group_product(const uint8_t* gb, const XFrag& xf, int lane, float (&acc)[4]) {
     const int g = lane >> 2;
     float d[4][4];
@@ -92,18 +93,21 @@ __device__ __forceinline__ void group_product(const uint8_t* gb, const XFrag& xf
     }
     float D[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) D[i] = __fadd_rn(__fadd_rn(d[0][i], d[1][i]), __fadd_rn(d[2][i], d[3][i]));
+    for (int i = 0; i < 4; ++i)
+        if (ODD || (i & 1) == 0) D[i] = __fadd_rn(__fadd_rn(d[0][i], d[1][i]), __fadd_rn(d[2][i], d[3][i]));
     const uint32_t sz0 = *reinterpret_cast<const uint32_t*>(gb + 1024 + g * 4);
     const uint32_t sz1 = *reinterpret_cast<const uint32_t*>(gb + 1024 + (g + 8) * 4);
     const float4 X = xf.X;                                                // (X'_{2t}, is_{2t}, X'_{2t+1}, is_{2t+1})
     const float s0 = bf16_lo(sz0), z0 = bf16_hi(sz0), s1 = bf16_lo(sz1), z1 = bf16_hi(sz1);
     const float s1c = __fmul_rn(s1, 0.0625f);
     const float zz0 = __fmaf_rn(-8.f, s0, z0), zz1 = __fmaf_rn(-8.f, s1, z1);
-    const float x0 = 1024.f * X.x, x1 = 1024.f * X.z;
+    const float x0 = 1024.f * X.x, x1 = ODD ? 1024.f * X.z : 0.f;
     acc[0] = __fmaf_rn(__fmaf_rn(s0, __fsub_rn(D[0], x0), __fmul_rn(zz0, X.x)), X.y, acc[0]);
-    acc[1] = __fmaf_rn(__fmaf_rn(s0, __fsub_rn(D[1], x1), __fmul_rn(zz0, X.z)), X.w, acc[1]);
     acc[2] = __fmaf_rn(__fmaf_rn(s1c, __fsub_rn(D[2], x0), __fmul_rn(zz1, X.x)), X.y, acc[2]);
-    acc[3] = __fmaf_rn(__fmaf_rn(s1c, __fsub_rn(D[3], x1), __fmul_rn(zz1, X.z)), X.w, acc[3]);
+    if (ODD) {
+        acc[1] = __fmaf_rn(__fmaf_rn(s0, __fsub_rn(D[1], x1), __fmul_rn(zz0, X.z)), X.w, acc[1]);
+        acc[3] = __fmaf_rn(__fmaf_rn(s1c, __fsub_rn(D[3], x1), __fmul_rn(zz1, X.z)), X.w, acc[3]);
+    }
 }
 
 }  // namespace kmr
