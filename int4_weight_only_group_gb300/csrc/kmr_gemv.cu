@@ -104,7 +104,7 @@ __device__ __forceinline__ float norm_factor(const GemvParams& p, const float* s
 // Epilogue of one tile: fixed-order sum of the warp partials, RMSNorm factor, store / add / SiLU-mul.
 template <int MB>
 __device__ __forceinline__ void tile_epilogue(const GemvParams& p, const float* ps, int tile, int idx,
-                                              const float* ssw) {
+                                              const float* ssw, bool have_res = false, float res = 0.f) {
     constexpr int WS = 16 * MB;                     // floats per warp partial
     if (p.epi == EPI_SILU) {
         if (idx >= 8 * MB) return;
@@ -123,7 +123,7 @@ __device__ __forceinline__ void tile_epilogue(const GemvParams& p, const float* 
         if (m >= p.M || n >= p.N) return;
         float v = __fmul_rn(warp16_sum(ps + rr * MB + m, WS), norm_factor(p, ssw, m));
         float* yp = p.y + size_t(m) * p.ldy + n;
-        *yp = (p.epi == EPI_RESID) ? __fadd_rn(*yp, v) : v;
+        *yp = (p.epi == EPI_RESID) ? __fadd_rn(have_res ? res : *yp, v) : v;
     }
 }
 
@@ -200,6 +200,21 @@ __global__ void __launch_bounds__(kGemvThreads, (MB * GPW <= 8) ? 2 : 1) gemv_ke
                 if (c == 0 && p.x_out) *reinterpret_cast<float4*>(p.x_out + size_t(m) * K + k) = xv[j][m];
             } else {
                 xv[j][m] = *reinterpret_cast<const float4*>(p.x + size_t(m) * K + k);
+            }
+        }
+    }
+    // All tiles fit (the usual case): an EPI_RESID thread fetches its first residual value
+    // (written by an earlier kernel of the step) now, so the epilogue does not wait on L2.
+    const bool fast = nt <= nst;
+    const int per = (p.epi == EPI_SILU ? 8 : 16) * MB;
+    float res0 = 0.f;
+    bool have_res0 = false;
+    if (fast) {
+        if (p.epi == EPI_RESID && tid < nt * per) {
+            const int tl = tid / per, e = tid - tl * per, rr = e / MB, m = e % MB, n = (t0 + tl) * 16 + rr;
+            if (m < p.M && n < p.N) {
+                res0 = p.y[size_t(m) * p.ldy + n];
+                have_res0 = true;
             }
         }
     }
@@ -290,9 +305,9 @@ __global__ void __launch_bounds__(kGemvThreads, (MB * GPW <= 8) ? 2 : 1) gemv_ke
             }
         }
     };
-    if (nt <= nst) {
+    if (fast) {
         // every tile was requested before griddepcontrol.wait; with all of them in, the
-        // product loop has no wait between tiles and the compiler may overlap them
+        // product loop has no wait between tiles
         mbar_wait(&bar[0], 0u, p.err);
 #pragma unroll 1
         for (int tl = 0; tl < nt; ++tl) {
@@ -301,10 +316,10 @@ __global__ void __launch_bounds__(kGemvThreads, (MB * GPW <= 8) ? 2 : 1) gemv_ke
             store_part<MB>(part + (size_t(tl) * kGemvWarps + warp) * WS, lane, acc);
         }
         __syncthreads();
-        const int per = (p.epi == EPI_SILU ? 8 : 16) * MB;
         for (int idx = tid; idx < nt * per; idx += kGemvThreads) {
             const int tl = idx / per;
-            tile_epilogue<MB>(p, part + size_t(tl) * kGemvWarps * WS, t0 + tl, idx - tl * per, ssw);
+            tile_epilogue<MB>(p, part + size_t(tl) * kGemvWarps * WS, t0 + tl, idx - tl * per, ssw,
+                              idx == tid && have_res0, res0);
         }
         return;
     }
