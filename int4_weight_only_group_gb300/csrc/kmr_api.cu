@@ -459,9 +459,9 @@ int enqueue_step(kmr_model* m, const StepArgs& a, cudaStream_t st) {
         (void)qd;
     }
     // final norm + LM head + argmax + finalize, in passes of at most 8 rows
-    for (int r0 = 0; r0 < B; r0 += kMaxMB) {
-        const int mr = (B - r0) < kMaxMB ? (B - r0) : kMaxMB;
-        const int MB = gemv_pick_mb(mr);
+    for (int r0 = 0; r0 < B; r0 += kMaxHeadRows) {
+        const int mr = (B - r0) < kMaxHeadRows ? (B - r0) : kMaxHeadRows;
+        const int MB = head_pick_mb(mr);
         HeadParams hp = {};
         hp.E = m->embed;
         hp.V = c.vocab;
@@ -589,8 +589,8 @@ extern "C" int kmr_model_create(const kmr_model_config* cfg, kmr_model** out) {
         dalloc(m, &m->qkv, size_t(B) * nqkv * 4) || dalloc(m, &m->attn_out, size_t(B) * c.n_q_heads * c.head_dim * 4) ||
         dalloc(m, &m->act, size_t(B) * c.intermediate * 4) ||
         dalloc(m, &m->apart, size_t(B) * c.n_q_heads * m->tsplit * (c.head_dim + 2) * 4) ||
-        dalloc(m, &m->acount, size_t(B) * c.n_kv_heads * 4) || dalloc(m, &m->hbest_v, size_t(m->sms) * kMaxMB * 4) ||
-        dalloc(m, &m->hbest_i, size_t(m->sms) * kMaxMB * 4) || dalloc(m, &m->hcount, 16) || dalloc(m, &m->err, 16) ||
+        dalloc(m, &m->acount, size_t(B) * c.n_kv_heads * 4) || dalloc(m, &m->hbest_v, size_t(m->sms) * kMaxHeadRows * 4) ||
+        dalloc(m, &m->hbest_i, size_t(m->sms) * kMaxHeadRows * 4) || dalloc(m, &m->hcount, 16) || dalloc(m, &m->err, 16) ||
         dalloc(m, &m->d_state, size_t(B) * 32))
         return fail(KMR_ERR_CUDA);
     std::vector<float> inv(c.head_dim / 2);
@@ -809,6 +809,7 @@ extern "C" int kmr_model_sync_status(kmr_model* m, void* stream) {
 extern "C" int kmr_model_kernels_per_step(const kmr_model* m, int B) {
     if (!m || B < 1) return 0;
     const int passes = (B + kMaxMB - 1) / kMaxMB;
-    const int k = m->cfg.n_layers * (4 * passes + 1) + passes;
+    const int head_passes = (B + kMaxHeadRows - 1) / kMaxHeadRows;
+    const int k = m->cfg.n_layers * (4 * passes + 1) + head_passes;
     return m->poison ? 2 * k : k;                 // the diagnostic adds one fill per kernel
 }

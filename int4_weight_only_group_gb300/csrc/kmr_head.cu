@@ -7,13 +7,19 @@
 // logits[m, v] = sum_k rmsnorm(x[m])[k] * E[v, k]; next[m] = argmax_v (lowest
 // index on ties, NaN never wins).  The 622 MB table at vocab 151936 is 43% of
 // the step's bytes, so it is streamed once at full bandwidth: a persistent
-// grid, each CTA a contiguous range of 8-row tiles moved by cp.async.bulk into
-// a ring of shared-memory stages by a dedicated producer warp that never waits
-// on the previous kernel.  Eight consumer warps split each tile along K; the
-// last warp to finish a tile (shared-memory counter) sums the eight partials
-// in a fixed order.  The logits are never re-read: each warp keeps a running
-// (value, index) best, CTAs publish theirs, and the last CTA to finish
-// (global counter) picks the winner and advances the step state.
+// grid, each CTA a contiguous range of 8-row tiles moved by cp.async.bulk
+// (one copy per row, into rows padded by 16 bytes) into a ring of shared-memory
+// stages by a dedicated producer warp that never waits on the previous kernel.
+// Eight consumer warps split each tile along K and multiply on the tensor
+// cores (mma.m16n8k16, bf16 in, f32 accumulate): the normalised x rows are the
+// A operand (up to 16 rows, the rest zero), the tile's 8 vocabulary rows the B
+// operand, so a warp spends three instructions per 128 weights at any batch
+// size up to 16 and the kernel stays bandwidth-bound; the 16-byte row padding
+// makes the fragment loads conflict-free.  The last warp to finish a tile
+// (shared-memory counter) sums the eight partials in a fixed order.  The
+// logits are never re-read: each warp keeps a running (value, index) best,
+// CTAs publish theirs, and the last CTA to finish (global counter) picks the
+// winner and advances the step state.
 #include "kmr_internal.cuh"
 
 namespace kmr {
@@ -27,23 +33,34 @@ __host__ __device__ inline size_t al16h(size_t v) { return (v + 15) & ~size_t(15
 struct HeadSmem {
     size_t full, empty, xb, red, tsum, cnt, wbv, wbi, red2, flag, stage, total;
 };
+// Shared-memory row strides (bytes): vocabulary rows and x rows are padded by 16 bytes
+// so that the eight rows of a fragment load fall in different banks.
+__host__ __device__ inline size_t head_row_bytes(int K) { return size_t(K) * 2 + 16; }
 __host__ __device__ inline HeadSmem head_layout(int MB, int K, int nst) {
     HeadSmem L;
     size_t o = 0;
     L.full = o;  o += al16h(size_t(nst) * 8);
     L.empty = o; o += al16h(size_t(nst) * 8);
-    L.xb = o;    o += al16h(size_t(MB) * K * 2);
-    L.red = o;   o += al16h(size_t(nst) * 8 * 8 * MB * 4);
-    L.tsum = o;  o += al16h(size_t(nst) * 8 * MB * 4);
+    L.xb = o;    o += al16h(size_t(MB) * head_row_bytes(K));
+    L.red = o;   o += al16h(size_t(nst) * 8 * MB * 8 * 4);      // per stage, per warp: [MB][8] partials
+    L.tsum = o;  o += al16h(size_t(nst) * MB * 8 * 4);
     L.cnt = o;   o += al16h(size_t(nst) * 4);
     L.wbv = o;   o += al16h(size_t(8) * MB * 4);
     L.wbi = o;   o += al16h(size_t(8) * MB * 4);
     L.red2 = o;  o += al16h(size_t(8) * 4);
     L.flag = o;  o += 16;
     o = (o + 127) & ~size_t(127);
-    L.stage = o; o += size_t(nst) * 8 * K * 2;
+    L.stage = o; o += size_t(nst) * 8 * head_row_bytes(K);
     L.total = o;
     return L;
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
@@ -71,7 +88,8 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(const HeadParams 
     float* red2 = reinterpret_cast<float*>(smem + L.red2);
     int* flag = reinterpret_cast<int*>(smem + L.flag);
     uint8_t* stages = smem + L.stage;
-    const size_t tile_bytes = size_t(8) * K * 2;
+    const size_t rs = head_row_bytes(K), tile_bytes = size_t(8) * rs;
+    const int xs = int(rs / 2);                  // x row stride in bf16 elements
 
     if (tid == 0) {
         for (int s = 0; s < nst; ++s) {
@@ -86,10 +104,11 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(const HeadParams 
     auto issue = [&](int i) {
         const int s = i % nst, t = t0 + i;
         const int rows = min(8, p.V - t * 8);
-        const uint32_t bytes = uint32_t(rows) * K * 2;
-        mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_g2s_stream(stages + size_t(s) * tile_bytes, p.E + size_t(t) * 8 * K, bytes, &full[s],
-                        policy_evict_first());
+        mbar_arrive_expect_tx(&full[s], uint32_t(rows) * K * 2);
+        const uint64_t pol = policy_evict_first();
+        for (int r = 0; r < rows; ++r)
+            bulk_g2s_stream(stages + size_t(s) * tile_bytes + size_t(r) * rs, p.E + (size_t(t) * 8 + r) * K,
+                            uint32_t(K) * 2, &full[s], pol);
     };
 
     if (warp == 8) {
@@ -126,63 +145,54 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(const HeadParams 
             const float r = rsqrtf(tot / float(K) + p.eps);
             for (int k = tid; k < K; k += kThreads) {
                 const float v = real ? __fmul_rn(__fmul_rn(p.x[size_t(m) * K + k], r), bf16_to_f32(p.norm_w[k])) : 0.f;
-                xb[size_t(m) * K + k] = f32_to_bf16_rn(v);
+                xb[size_t(m) * xs + k] = f32_to_bf16_rn(v);
             }
         }
         consumers_sync();
 
         float bv = -INFINITY;
         int bi = 0x7fffffff;
-        const int cpw = K >> 6;   // 8-element chunks per warp per row
-        const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-        const int row = (lane >> 2) & 7;
+        const int g = lane >> 2, t = lane & 3;
+        const int ks_n = K >> 7;                 // 16-wide k-steps in this warp's eighth of K
+        const int kbeg = warp * (K >> 3);
+        const uint16_t* xg = xb + size_t(g) * xs;
+        const uint16_t* xg8 = xb + size_t(g + 8) * xs;
         for (int i = 0; i < nt; ++i) {
             const int s = i % nst;
             mbar_wait(&full[s], uint32_t((i / nst) & 1), p.err);
-            const uint16_t* tile = reinterpret_cast<const uint16_t*>(stages + size_t(s) * tile_bytes);
-            float acc[8][MB];
-#pragma unroll
-            for (int r = 0; r < 8; ++r)
-#pragma unroll
-                for (int m = 0; m < MB; ++m) acc[r][m] = 0.f;
-            for (int cc = lane; cc < cpw; cc += 32) {
-                const int k0 = warp * (K >> 3) + cc * 8;
-                uint4 xv[MB];
-#pragma unroll
-                for (int m = 0; m < MB; ++m) xv[m] = *reinterpret_cast<const uint4*>(xb + size_t(m) * K + k0);
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const uint4 wv = *reinterpret_cast<const uint4*>(tile + size_t(r) * K + k0);
-#pragma unroll
-                    for (int m = 0; m < MB; ++m) {
-                        fma_bf16x2_f32(acc[r][m], wv.x, xv[m].x);
-                        fma_bf16x2_f32(acc[r][m], wv.y, xv[m].y);
-                        fma_bf16x2_f32(acc[r][m], wv.z, xv[m].z);
-                        fma_bf16x2_f32(acc[r][m], wv.w, xv[m].w);
-                    }
+            const uint8_t* tile = stages + size_t(s) * tile_bytes;
+            const uint8_t* brow = tile + size_t(g) * rs;       // vocabulary row g of the tile (B column g)
+            float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            auto kstep = [&](float (&dd)[4], int ks) {
+                const int k0 = kbeg + ks * 16 + 2 * t;
+                uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+                if (g < MB) {
+                    a0 = *reinterpret_cast<const uint32_t*>(xg + k0);
+                    a2 = *reinterpret_cast<const uint32_t*>(xg + k0 + 8);
                 }
+                if (MB > 8 && g + 8 < MB) {
+                    a1 = *reinterpret_cast<const uint32_t*>(xg8 + k0);
+                    a3 = *reinterpret_cast<const uint32_t*>(xg8 + k0 + 8);
+                }
+                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(brow + size_t(k0) * 2);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(brow + size_t(k0 + 8) * 2);
+                mma_bf16_16816(dd, a0, a1, a2, a3, b0, b1);
+            };
+            int ks = 0;
+            for (; ks + 1 < ks_n; ks += 2) {     // two accumulator chains
+                kstep(d[0], ks);
+                kstep(d[1], ks + 1);
             }
-            // reduce-scatter over lanes: lane l keeps row (l >> 2) & 7
-#pragma unroll
-            for (int m = 0; m < MB; ++m) {
-                float a[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float keep = b4 ? acc[q + 4][m] : acc[q][m];
-                    const float send = b4 ? acc[q][m] : acc[q + 4][m];
-                    a[q] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-                }
-                float cc2[2];
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const float keep = b3 ? a[q + 2] : a[q];
-                    const float send = b3 ? a[q] : a[q + 2];
-                    cc2[q] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-                }
-                float e = (b2 ? cc2[1] : cc2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? cc2[0] : cc2[1], 4);
-                e += __shfl_xor_sync(0xffffffffu, e, 2);
-                e += __shfl_xor_sync(0xffffffffu, e, 1);
-                if ((lane & 3) == 0) red[((size_t(s) * 8 + warp) * 8 + row) * MB + m] = e;
+            if (ks < ks_n) kstep(d[0], ks);
+            // this warp's partials: rows g, g+8 of x, vocabulary rows 2t, 2t+1 of the tile
+            float* rp = red + (size_t(s) * 8 + warp) * MB * 8;
+            if (g < MB) {
+                rp[g * 8 + 2 * t] = __fadd_rn(d[0][0], d[1][0]);
+                rp[g * 8 + 2 * t + 1] = __fadd_rn(d[0][1], d[1][1]);
+            }
+            if (MB > 8 && g + 8 < MB) {
+                rp[(g + 8) * 8 + 2 * t] = __fadd_rn(d[0][2], d[1][2]);
+                rp[(g + 8) * 8 + 2 * t + 1] = __fadd_rn(d[0][3], d[1][3]);
             }
             __syncwarp();
             int last = 0;
@@ -195,11 +205,11 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(const HeadParams 
                 __threadfence_block();
                 const int tbase = (t0 + i) * 8;
                 for (int idx = lane; idx < 8 * MB; idx += 32) {
-                    const int r = idx / MB, m = idx % MB;
+                    const int m = idx >> 3, r = idx & 7;
                     float v = 0.f;
 #pragma unroll
-                    for (int w = 0; w < 8; ++w) v += red[((size_t(s) * 8 + w) * 8 + r) * MB + m];
-                    tsum[(size_t(s) * 8 + r) * MB + m] = v;
+                    for (int w = 0; w < 8; ++w) v = __fadd_rn(v, red[((size_t(s) * 8 + w) * MB + m) * 8 + r]);
+                    tsum[(size_t(s) * MB + m) * 8 + r] = v;
                     const int n = tbase + r;
                     if (p.logits && m < p.M && n < p.V) p.logits[size_t(m) * p.ldl + n] = v;
                 }
@@ -209,7 +219,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(const HeadParams 
                     for (int r = 0; r < 8; ++r) {
                         const int n = tbase + r;
                         if (n >= p.V) break;
-                        float v = tsum[(size_t(s) * 8 + r) * MB + lane];
+                        float v = tsum[(size_t(s) * MB + lane) * 8 + r];
                         if (v != v) v = -INFINITY;
                         if (better(v, n, bv, bi)) { bv = v; bi = n; }
                     }
@@ -294,14 +304,16 @@ cudaError_t launch_head(const HeadParams& p, int MB, int grid, cudaStream_t st, 
         case 1: return launch_head_mb<1>(p, grid, st, pdl);
         case 2: return launch_head_mb<2>(p, grid, st, pdl);
         case 4: return launch_head_mb<4>(p, grid, st, pdl);
-        default: return launch_head_mb<8>(p, grid, st, pdl);
+        case 8: return launch_head_mb<8>(p, grid, st, pdl);
+        default: return launch_head_mb<16>(p, grid, st, pdl);
     }
 }
+int head_pick_mb(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
 
 cudaError_t head_set_attributes() {
     const int mx = 227 * 1024;
-    const void* ks[4] = {(const void*)head_kernel<1>, (const void*)head_kernel<2>, (const void*)head_kernel<4>,
-                         (const void*)head_kernel<8>};
+    const void* ks[5] = {(const void*)head_kernel<1>, (const void*)head_kernel<2>, (const void*)head_kernel<4>,
+                         (const void*)head_kernel<8>, (const void*)head_kernel<16>};
     for (const void* k : ks) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
         if (e != cudaSuccess) return e;

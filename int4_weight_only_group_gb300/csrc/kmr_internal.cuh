@@ -201,6 +201,8 @@ struct HeadParams {
 };
 size_t head_smem_bytes(int MB, int K, int nstage);
 cudaError_t launch_head(const HeadParams& p, int MB, int grid, cudaStream_t st, bool pdl);
+constexpr int kMaxHeadRows = 16;     // rows of x per LM-head pass
+int head_pick_mb(int M);
 
 // ------------------------------------------------------------------ attention
 struct AttnParams {
