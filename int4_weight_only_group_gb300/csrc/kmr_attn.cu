@@ -48,8 +48,9 @@ namespace kmr {
 
 namespace {
 
-constexpr int kSub = 64;            // positions per ring stage: 8 warps x 8
-constexpr int kChunk = 8;           // positions a warp scores at once
+// A warp scores CH positions at a time (8, or 16 when a split can exceed 64 positions and a
+// KV head serves at most 2 query heads, so that NV = heads x CH stays <= 32); a ring stage
+// holds 8 warps x CH positions.
 constexpr int kMaxStages = 4;
 constexpr int kMaxRep = 4;          // query heads per KV head supported
 constexpr float kLog2e = 1.4426950408889634f;
@@ -59,14 +60,14 @@ __host__ __device__ inline size_t al16a(size_t v) { return (v + 15) & ~size_t(15
 struct AttnSmem {
     size_t bar, kst, vst, knew, vnew, qs, wml, wo, co, cml, recv, flag, total;
 };
-__host__ __device__ inline AttnSmem attn_layout(int D, int rep, int nstage) {
+__host__ __device__ inline AttnSmem attn_layout(int D, int rep, int nstage, int sub) {
     AttnSmem L;
     const int per = rep * D / 8;                                // output slice merged by each cluster rank
     size_t o = 0;
     L.bar = o;   o += al16a(kMaxStages * 8);
     o = (o + 127) & ~size_t(127);
-    L.kst = o;   o += size_t(nstage) * kSub * D * 2;
-    L.vst = o;   o += size_t(nstage) * kSub * D * 2;
+    L.kst = o;   o += size_t(nstage) * sub * D * 2;
+    L.vst = o;   o += size_t(nstage) * sub * D * 2;
     L.knew = o;  o += al16a(size_t(D) * 2);
     L.vnew = o;  o += al16a(size_t(D) * 2);
     L.qs = o;    o += al16a(size_t(rep) * D * 4);
@@ -106,17 +107,20 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
     return v[0];
 }
 
-template <int D, int REP, bool CLUSTER>
+template <int D, int REP, bool CLUSTER, int CH>
 __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int EPL = D / 32;               // contiguous dims per lane
+    constexpr int kChunk = CH;                // positions a warp scores at once
+    constexpr int kSub = 8 * CH;              // positions per ring stage
+    static_assert(REP * CH <= 32, "one score per lane after the reduce-scatter");
     constexpr int NV = REP * kChunk;          // partial scores per lane before the reduce-scatter
     constexpr int JS = 32 / NV;               // lanes sharing one score after it
     constexpr int PER = REP * D / 8;          // output slice per cluster rank
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nst = p.nstage;
-    const AttnSmem L = attn_layout(D, REP, nst);
+    const AttnSmem L = attn_layout(D, REP, nst, kSub);
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
     uint16_t* kst = reinterpret_cast<uint16_t*>(smem + L.kst);
     uint16_t* vst = reinterpret_cast<uint16_t*>(smem + L.vst);
@@ -465,28 +469,43 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     }
 }
 
-template <bool CL>
-const void* attn_fn(int d, int rep) {
+template <bool CL, int CH>
+const void* attn_fn_ch(int d, int rep) {
     if (d == 64) {
-        if (rep == 1) return (const void*)attn_kernel<64, 1, CL>;
-        if (rep == 2) return (const void*)attn_kernel<64, 2, CL>;
-        return (const void*)attn_kernel<64, 4, CL>;
+        if (rep == 1) return (const void*)attn_kernel<64, 1, CL, CH>;
+        if (rep == 2) return (const void*)attn_kernel<64, 2, CL, CH>;
+        return (const void*)attn_kernel<64, 4, CL, 8>;
     }
-    if (rep == 1) return (const void*)attn_kernel<128, 1, CL>;
-    if (rep == 2) return (const void*)attn_kernel<128, 2, CL>;
-    return (const void*)attn_kernel<128, 4, CL>;
+    if (rep == 1) return (const void*)attn_kernel<128, 1, CL, CH>;
+    if (rep == 2) return (const void*)attn_kernel<128, 2, CL, CH>;
+    return (const void*)attn_kernel<128, 4, CL, 8>;
+}
+template <bool CL>
+const void* attn_fn(int d, int rep, int ch) {
+    return ch == 16 ? attn_fn_ch<CL, 16>(d, rep) : attn_fn_ch<CL, 8>(d, rep);
 }
 
 }  // namespace
 
-// Ring depth: enough stages for the longest split the cache allows, at most kMaxStages.
-int attn_stages(int max_len, int splits) {
+// Positions a warp scores at once for a launch: 16 when the longest split the cache allows
+// exceeds 64 positions and NV = rep x 16 fits a warp, else 8.
+int attn_chunk(int max_len, int splits, int rep) {
     if (splits < 1) splits = 1;
     const int chunk = (((max_len + splits - 1) / splits) + 15) & ~15;
-    const int sub = (chunk + kSub - 1) / kSub;
-    return sub < 1 ? 1 : (sub > kMaxStages ? kMaxStages : sub);
+    return (chunk > 64 && rep <= 2) ? 16 : 8;
 }
-size_t attn_smem_bytes(int d, int rep, int nstage) { return attn_layout(d, rep, nstage).total; }
+// Ring depth: enough stages (of 8 x ch positions) for the longest split, at most kMaxStages
+// and at most 192 KB of K/V staging.
+int attn_stages(int max_len, int splits, int ch, int d) {
+    if (splits < 1) splits = 1;
+    const int chunk = (((max_len + splits - 1) / splits) + 15) & ~15;
+    int n = (chunk + 8 * ch - 1) / (8 * ch);
+    const int cap = int((192u * 1024u) / (unsigned(8 * ch) * unsigned(d) * 4u));
+    if (n > kMaxStages) n = kMaxStages;
+    if (n > cap) n = cap;
+    return n < 1 ? 1 : n;
+}
+size_t attn_smem_bytes(int d, int rep, int nstage, int ch) { return attn_layout(d, rep, nstage, 8 * ch).total; }
 int attn_default_tsplit(int nkv) {
     int t = (num_sms() + nkv - 1) / nkv;
     return t < 1 ? 1 : (t > 32 ? 32 : t);
@@ -499,11 +518,12 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t st, bool pdl) {
     const int rep = p.nq / p.nkv;
     AttnParams q = p;
     if (p.cluster) q.tsplit = kAttnClusterSplits;
-    q.nstage = attn_stages(p.S, q.tsplit);
+    const int ch = attn_chunk(p.S, q.tsplit, rep);
+    q.nstage = attn_stages(p.S, q.tsplit, ch, p.d);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(q.tsplit, p.nkv, p.B);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = attn_smem_bytes(p.d, rep, q.nstage);
+    cfg.dynamicSmemBytes = attn_smem_bytes(p.d, rep, q.nstage, ch);
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     int n = 0;
@@ -521,7 +541,7 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t st, bool pdl) {
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    const void* fn = p.cluster ? attn_fn<true>(p.d, rep) : attn_fn<false>(p.d, rep);
+    const void* fn = p.cluster ? attn_fn<true>(p.d, rep, ch) : attn_fn<false>(p.d, rep, ch);
     void* args[] = {&q};
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
@@ -531,8 +551,9 @@ cudaError_t attn_set_attributes() {
     const int reps[3] = {1, 2, 4}, ds[2] = {64, 128};
     for (int d : ds)
         for (int r : reps)
-            for (int cl = 0; cl < 2; ++cl) {
-                const void* k = cl ? attn_fn<true>(d, r) : attn_fn<false>(d, r);
+            for (int cl = 0; cl < 4; ++cl) {
+                const int ch = (cl & 2) ? 16 : 8;
+                const void* k = (cl & 1) ? attn_fn<true>(d, r, ch) : attn_fn<false>(d, r, ch);
                 cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
                 if (e != cudaSuccess) return e;
                 e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,

@@ -236,8 +236,9 @@ cudaError_t poison_set_attributes();
 cudaError_t launch_smem_poison(uint32_t pattern, int sms, cudaStream_t st);
 
 constexpr int kAttnClusterSplits = 8;     // cluster size of the DSMEM-merged attention (portable)
-size_t attn_smem_bytes(int d, int rep, int nstage);
-int attn_stages(int max_len, int splits);
+size_t attn_smem_bytes(int d, int rep, int nstage, int ch);
+int attn_stages(int max_len, int splits, int ch, int d);
+int attn_chunk(int max_len, int splits, int rep);
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t st, bool pdl);
 size_t attn_workspace_bytes(int B, int nq, int nkv, int d, int tsplit);
 int attn_default_tsplit(int nkv);

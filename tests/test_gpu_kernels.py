@@ -238,9 +238,10 @@ def test_decode_attn_single_token_and_determinism(torch):
     assert np.array_equal(out, again)
 
 
-def test_decode_attn_ignores_stale_shared_memory(torch):
-    cpos = [0, 6, 15, 16, 70, 127, 1000]          # lone last positions, exact splits, ragged tails
-    args = (torch, len(cpos), 16, 4, 128, 1024, len(cpos), cpos, list(range(len(cpos))))
+@pytest.mark.parametrize("nkv,S", [(4, 1024), (8, 4096)])   # 8- and 16-position scoring chunks
+def test_decode_attn_ignores_stale_shared_memory(torch, nkv, S):
+    cpos = [0, 6, 15, 16, 70, 127, 1000, S - 1]   # lone last positions, exact splits, ragged tails
+    args = (torch, len(cpos), 16, nkv, 128, S, len(cpos), cpos, list(range(len(cpos))))
     clean, ref, err = _attn_case(*args, seed=11)
     assert err == 0 and np.all(np.isfinite(clean)) and rel_l2(clean, ref) <= 1e-4
     for pat in POISON_PATTERNS:
