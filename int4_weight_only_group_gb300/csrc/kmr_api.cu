@@ -84,8 +84,10 @@ static int enqueue_gemv(const GemvLaunch& a, int M, int* err, cudaStream_t st, b
                         bool poison = false, uint32_t pattern = 0) {
     int launches = 0;
     const int grid = gemv_grid(a.g.tiles, sms);
-    for (int r0 = 0; r0 < M; r0 += kMaxMB) {
-        const int mr = (M - r0) < kMaxMB ? (M - r0) : kMaxMB;
+    // rows per launch: 16 (two groups of 8 from one weight fill) when the CTA's tiles stay resident
+    const int rows = gemv_two_halves_ok(a.g.tiles, grid, a.g.tile_bytes) ? 2 * kMaxMB : kMaxMB;
+    for (int r0 = 0; r0 < M; r0 += rows) {
+        const int mr = (M - r0) < rows ? (M - r0) : rows;
         const int MB = gemv_pick_mb(mr);
         GemvParams p = {};
         p.w = a.w;
@@ -107,6 +109,7 @@ static int enqueue_gemv(const GemvLaunch& a, int M, int* err, cudaStream_t st, b
         p.ldy = a.ldy;
         p.err = err;
         p.nstage = gemv_nstage(a.g.tiles, grid, a.g.tile_bytes);
+        p.halves = mr > kMaxMB ? 2 : 1;
         if (poison && launch_smem_poison(pattern, sms, st) != cudaSuccess) return KMR_ERR_CUDA;
         if (launch_gemv(p, MB, grid, st, pdl || launches > 0) != cudaSuccess) return KMR_ERR_CUDA;
         ++launches;
@@ -808,8 +811,16 @@ extern "C" int kmr_model_sync_status(kmr_model* m, void* stream) {
 
 extern "C" int kmr_model_kernels_per_step(const kmr_model* m, int B) {
     if (!m || B < 1) return 0;
-    const int passes = (B + kMaxMB - 1) / kMaxMB;
+    // GEMV launches per projection: one per 16 rows when the CTA's tiles stay resident, else per 8
+    const kmr_model_config& c = m->cfg;
+    const int grid = m->sms;
+    int gemv_launches = 0;
+    for (int w = 0; w < 4; ++w) {
+        const PackGeom& g = m->layers[0].g[w];
+        const int rows = gemv_two_halves_ok(g.tiles, gemv_grid(g.tiles, grid), g.tile_bytes) ? 2 * kMaxMB : kMaxMB;
+        gemv_launches += (B + rows - 1) / rows;
+    }
     const int head_passes = (B + kMaxHeadRows - 1) / kMaxHeadRows;
-    const int k = m->cfg.n_layers * (4 * passes + 1) + head_passes;
+    const int k = c.n_layers * (gemv_launches + 1) + head_passes;
     return m->poison ? 2 * k : k;                 // the diagnostic adds one fill per kernel
 }

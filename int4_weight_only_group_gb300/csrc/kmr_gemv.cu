@@ -129,53 +129,21 @@ __device__ __forceinline__ void tile_epilogue(const GemvParams& p, const float* 
 
 // Two CTAs per SM (so the next GEMV of the step can be resident and prefetching) where the
 // staging registers allow it.
+// Everything after griddepcontrol.wait for up to MB rows of x: stage x, run the tile products
+// on the resident weight tiles, reduce and apply the epilogue.  Called once per group of MB
+// rows (two calls let a CTA serve 16 rows from one weight fill).
 template <int MB, int GPW>
-__global__ void __launch_bounds__(kGemvThreads, (MB * GPW <= 8) ? 2 : 1) gemv_kernel(const GemvParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
+__device__ __forceinline__ void gemv_rows(const GemvParams p, uint8_t* smem, const GemvSmem& L, const uint2 (&nwv)[GPW],
+                                          int t0, int nt, int c) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int P = gridDim.x, c = blockIdx.x;
-    const int t0 = int((long long)c * p.tiles / P), t1 = int((long long)(c + 1) * p.tiles / P);
-    const int nt = t1 - t0;
     const int K = p.K, G = K >> 7, tb = p.tile_bytes, nst = p.nstage;
-    const GemvSmem L = gemv_layout(MB, GPW, tb, nst);
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
     __half* xw = reinterpret_cast<__half*>(smem + L.xw) + size_t(warp) * GPW * MB * 128;
     float* xst = reinterpret_cast<float*>(smem + L.xst) + size_t(warp) * GPW * 16;
     float* ssw = reinterpret_cast<float*>(smem + L.ssw);
     float* part = reinterpret_cast<float*>(smem + L.part);
     uint8_t* stages = smem + L.stage;
-
-    // ---- weight ring: whole fill issued before waiting on the previous kernel
-    if (tid == 0) {
-        for (int s = 0; s < nst; ++s) mbar_init(&bar[s], 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    if (tid == 0) {
-        const uint64_t pol = policy_evict_first();
-        if (nt <= nst) {
-            // every tile fits: one barrier counts all of them (nt * tb < 2^20 bytes)
-            mbar_arrive_expect_tx(&bar[0], uint32_t(nt) * tb);
-            for (int i = 0; i < nt; ++i)
-                bulk_g2s_stream(stages + size_t(i) * tb, p.w + size_t(t0 + i) * tb, tb, &bar[0], pol);
-        } else {
-            for (int i = 0; i < nst; ++i) {
-                mbar_arrive_expect_tx(&bar[i], tb);
-                bulk_g2s_stream(stages + size_t(i) * tb, p.w + size_t(t0 + i) * tb, tb, &bar[i], pol);
-            }
-        }
-    }
     const bool norm = p.in_kind != IN_F32;
-    // norm weights of this warp's groups (constants): fetched before the wait
-    uint2 nwv[GPW];
-#pragma unroll
-    for (int j = 0; j < GPW; ++j) {
-        const int grp = warp + j * kGemvWarps;
-        nwv[j] = (norm && grp < G) ? *reinterpret_cast<const uint2*>(p.norm_w + size_t(grp) * 128 + lane * 4)
-                                   : make_uint2(0, 0);
-    }
-    pdl_launch_dependents();
-    pdl_wait();
 
     // ---- stage x for this warp's groups: lane l holds inputs 4l..4l+3 of each group.
     // Loads first, then every (group, row)'s arithmetic, then all warp reductions
@@ -341,9 +309,76 @@ __global__ void __launch_bounds__(kGemvThreads, (MB * GPW <= 8) ? 2 : 1) gemv_ke
     }
 }
 
+template <int MB, int GPW, int NH>
+__global__ void __launch_bounds__(kGemvThreads, (MB * GPW * NH <= 8) ? 2 : 1) gemv_kernel(const GemvParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P = gridDim.x, c = blockIdx.x;
+    const int t0 = int((long long)c * p.tiles / P), t1 = int((long long)(c + 1) * p.tiles / P);
+    const int nt = t1 - t0;
+    const int K = p.K, G = K >> 7, tb = p.tile_bytes, nst = p.nstage;
+    const GemvSmem L = gemv_layout(MB, GPW, tb, nst);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
+    uint8_t* stages = smem + L.stage;
+
+    // ---- weight ring: whole fill issued before waiting on the previous kernel
+    if (tid == 0) {
+        for (int s = 0; s < nst; ++s) mbar_init(&bar[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const uint64_t pol = policy_evict_first();
+        if (nt <= nst) {
+            // every tile fits: one barrier counts all of them (nt * tb < 2^20 bytes)
+            mbar_arrive_expect_tx(&bar[0], uint32_t(nt) * tb);
+            for (int i = 0; i < nt; ++i)
+                bulk_g2s_stream(stages + size_t(i) * tb, p.w + size_t(t0 + i) * tb, tb, &bar[0], pol);
+        } else {
+            for (int i = 0; i < nst; ++i) {
+                mbar_arrive_expect_tx(&bar[i], tb);
+                bulk_g2s_stream(stages + size_t(i) * tb, p.w + size_t(t0 + i) * tb, tb, &bar[i], pol);
+            }
+        }
+    }
+    const bool norm = p.in_kind != IN_F32;
+    // norm weights of this warp's groups (constants): fetched before the wait
+    uint2 nwv[GPW];
+#pragma unroll
+    for (int j = 0; j < GPW; ++j) {
+        const int grp = warp + j * kGemvWarps;
+        nwv[j] = (norm && grp < G) ? *reinterpret_cast<const uint2*>(p.norm_w + size_t(grp) * 128 + lane * 4)
+                                   : make_uint2(0, 0);
+    }
+    pdl_launch_dependents();
+    pdl_wait();
+
+    if constexpr (NH == 1) {
+        gemv_rows<MB, GPW>(p, smem, L, nwv, t0, nt, c);
+    } else {
+        // rows [0, MB), then [MB, M) on the same resident weight tiles
+        GemvParams q = p;
+        q.M = MB;
+        gemv_rows<MB, GPW>(q, smem, L, nwv, t0, nt, c);
+        __syncthreads();                         // the first rows' staging and partials are consumed
+        q.x = p.x ? p.x + size_t(MB) * K : nullptr;
+        q.tokens = p.tokens ? p.tokens + MB : nullptr;
+        q.x_out = p.x_out ? p.x_out + size_t(MB) * K : nullptr;
+        q.y = p.y + size_t(MB) * p.ldy;
+        q.M = p.M - MB;
+        gemv_rows<MB, GPW>(q, smem, L, nwv, t0, nt, c);
+    }
+
+}
+
 }  // namespace
 
 int gemv_pick_mb(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
+// Two groups of 8 rows share one weight fill when every CTA's tiles stay resident (no ring).
+bool gemv_two_halves_ok(int tiles, int grid, int tile_bytes) {
+    const int tpc = (tiles + grid - 1) / grid;
+    return tpc <= gemv_nstage(tiles, grid, tile_bytes);
+}
 static int gemv_gpw(int K) { return ((K >> 7) + kGemvWarps - 1) / kGemvWarps; }
 
 // At most one CTA per SM, each owning ceil(tiles / SMs) whole tiles (the last
@@ -366,9 +401,17 @@ size_t gemv_smem_bytes(int MB, int K, int tile_bytes, int nstage) {
 }
 
 template <int MB, int GPW>
-static const void* gemv_fn() { return (const void*)gemv_kernel<MB, GPW>; }
+static const void* gemv_fn() { return (const void*)gemv_kernel<MB, GPW, 1>; }
 
-static const void* gemv_fn_for(int MB, int GPW) {
+static const void* gemv_fn_for(int MB, int GPW, int NH = 1) {
+    if (NH == 2) {
+        switch (GPW) {
+            case 1: return (const void*)gemv_kernel<8, 1, 2>;
+            case 2: return (const void*)gemv_kernel<8, 2, 2>;
+            case 3: return (const void*)gemv_kernel<8, 3, 2>;
+            default: return (const void*)gemv_kernel<8, 4, 2>;
+        }
+    }
     switch (MB * 8 + GPW) {
         case 1 * 8 + 1: return gemv_fn<1, 1>();
         case 1 * 8 + 2: return gemv_fn<1, 2>();
@@ -402,15 +445,15 @@ cudaError_t launch_gemv(const GemvParams& p, int MB, int grid, cudaStream_t st, 
     cfg.numAttrs = pdl ? 1 : 0;
     GemvParams q = p;
     void* args[] = {&q};
-    return cudaLaunchKernelExC(&cfg, gemv_fn_for(MB, gemv_gpw(p.K)), args);
+    return cudaLaunchKernelExC(&cfg, gemv_fn_for(MB, gemv_gpw(p.K), p.halves), args);
 }
 
 cudaError_t gemv_set_attributes() {
     const int mx = 227 * 1024;
-    const int mbs[4] = {1, 2, 4, 8};
+    const int mbs[5] = {1, 2, 4, 8, 16};         // 16: two groups of 8 rows per launch
     for (int mb : mbs)
         for (int gpw = 1; gpw <= 4; ++gpw) {
-            const void* k = gemv_fn_for(mb, gpw);
+            const void* k = mb == 16 ? gemv_fn_for(8, gpw, 2) : gemv_fn_for(mb, gpw);
             cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
             if (e != cudaSuccess) return e;
             e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);

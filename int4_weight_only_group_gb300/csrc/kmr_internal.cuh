@@ -12,7 +12,7 @@ namespace kmr {
 
 constexpr int kThreads = 256;        // every compute kernel uses 8 warps
 constexpr int kTileRows = 8;         // rows per packed int4 tile / LM-head tile
-constexpr int kMaxMB = 8;            // rows of x per GEMV pass
+constexpr int kMaxMB = 8;            // rows of x per GEMV staging group (a launch serves up to 2 groups)
 constexpr int kMaxBatch = 16;
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -168,10 +168,12 @@ struct GemvParams {
     int ldy;
     int* err;
     int nstage;                  // weight ring depth (tiles)
+    int halves;                  // 1, or 2: rows [0, MB) then [MB, 2 MB) from one weight fill (needs all tiles resident)
 };
 size_t gemv_smem_bytes(int MB, int K, int tile_bytes, int nstage);
 cudaError_t launch_gemv(const GemvParams& p, int MB, int grid, cudaStream_t st, bool pdl);
 int gemv_pick_mb(int M);
+bool gemv_two_halves_ok(int tiles, int grid, int tile_bytes);
 // At most one CTA per SM, each owning an equal count of whole 16-row tiles.
 int gemv_grid(int tiles, int sms);
 int gemv_nstage(int tiles, int grid, int tile_bytes);

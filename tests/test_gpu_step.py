@@ -285,6 +285,44 @@ def test_head_layouts(torch, nq, nkv):
     m.close()
 
 
+def test_sixteen_rows_one_weight_fill(torch):
+    """B = 16: each int4 GEMV serves all 16 rows from one weight fill and the LM head
+    takes them in one pass; 2 teacher-forced steps match the oracle and rows 0 and 13 equal
+    their batch-1 results bit for bit."""
+    from workloads import Workload
+    B = 16
+    cfg = tiny_config(slots=B)
+    r = np.random.default_rng(16)
+    prefill = [int(v) for v in r.integers(1, cfg.max_len - 8, B)]
+    wl = Workload("tiny b16", cfg, 7, batch=B, prefill=prefill, rope_delta=[int(v) for v in r.integers(-9, 1, B)],
+                  slot_ids=[int(v) for v in r.permutation(B)], first_tokens=[int(v) for v in r.integers(0, 1000, B)],
+                  steps=2)
+    m, _ = build_model(wl, max_batch=B)
+    assert m.kernels_per_step(B) == cfg.n_layers * 5 + 1
+    o = od.OracleDecoder.for_workload(wl)
+    st = od.initial_state(wl)
+    dev = Dev(torch, *st, cfg.vocab)
+    first = None
+    for t in range(wl.steps):
+        res = o.step(*st)
+        dev.step(m)
+        out = dev.host()
+        if first is None:
+            first = out[4].copy()
+        _check_step(res, out, B)
+        st = (res.next_ids, res.positions, res.cache_position, st[3], res.finished)
+        dev.set(tok=res.next_ids, fin=res.finished)
+    st0 = od.initial_state(wl)
+    for b in (0, 13):
+        mb, _ = build_model(wl, max_batch=B)
+        d1 = Dev(torch, st0[0][b:b + 1], st0[1][:, b:b + 1], st0[2][b:b + 1], st0[3][b:b + 1], st0[4][b:b + 1],
+                 cfg.vocab)
+        d1.step(mb)
+        assert np.array_equal(d1.host()[4][0], first[b]), f"row {b} differs between B=16 and B=1"
+        mb.close()
+    m.close()
+
+
 # ------------------------------------------------------------------ 2B-shaped workloads
 def test_single_2b_layer_step(torch):
     wl = layer2b_workload()
