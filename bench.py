@@ -2,7 +2,7 @@
 """Decode-step benchmark: int4 weight-only group-wise greedy decode of the
 28-layer 2B-shaped decoder on one GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--batch 1|4] [--impl kmr|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--batch 1|4|16] [--impl kmr|reference]
 
 A step is one pass of the whole decode path (every layer's int4 QKV / O /
 gate_up / down GEMVs, q/k norm, M-RoPE, KV write and GQA attention, final
@@ -10,7 +10,8 @@ norm, tied bf16 LM head, argmax and state advance) for the batch's rows.
 Workload (synthetic, seeded): batch 1 with 512 prefilled positions, 256
 greedy steps per generation (--batch 4: four continuous slots prefilled
 300/512/700/900, row 2 retired at step 64, row 3 length-capped at 1024,
-128 steps per generation).  The timed K steps run back to back as CUDA-graph
+128 steps per generation; --batch 16: sixteen slots prefilled 256..896, 128
+steps).  The timed K steps run back to back as CUDA-graph
 replays; the state is rewound to the generation's start every generation.
 The per-step working set (1.4 GB of weights) is far larger than L2, so
 nothing survives in L2 between steps.
@@ -110,8 +111,8 @@ def profile_traffic(kernel_file: str, summary: str):
 
 # ------------------------------------------------------------------ workloads
 def workload(batch: int):
-    from workloads import full2b_b1_workload, full2b_b4_workload
-    return full2b_b1_workload() if batch == 1 else full2b_b4_workload()
+    from workloads import full2b_b1_workload, full2b_b4_workload, full2b_b16_workload
+    return {1: full2b_b1_workload, 4: full2b_b4_workload, 16: full2b_b16_workload}[batch]()
 
 
 def tokens_per_generation(wl) -> int:
@@ -389,7 +390,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=256)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--batch", type=int, default=1, choices=(1, 4))
+    ap.add_argument("--batch", type=int, default=1, choices=(1, 4, 16))
     ap.add_argument("--impl", default="kmr", choices=("kmr", "reference"))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-extras", action="store_true",

@@ -242,6 +242,18 @@ def full2b_b4_workload(seed: int = 0) -> Workload:
                     steps=128, finish_at={2: 64})
 
 
+def full2b_b16_workload(seed: int = 0) -> Workload:
+    """Sixteen continuous slots of the 28-layer model (prefilled lengths spread over 256..896,
+    deltas in [-60, 0], 128 steps, no row finishes early): the batch 8-16 case."""
+    cfg = full2b_config(slots=16)
+    r = _rng(seed, "b16")
+    prefill = [int(v) for v in r.integers(256, 897, size=16)]
+    deltas = [int(v) for v in r.integers(-60, 1, size=16)]
+    return Workload("28-layer 2B-shaped decoder, batch 16 continuous slots (256..896 prefilled), 128 steps",
+                    cfg, seed, batch=16, prefill=prefill, rope_delta=deltas, slot_ids=list(range(16)),
+                    first_tokens=_first_tokens(seed, 16, cfg.vocab, cfg.eos_id), steps=128)
+
+
 def initial_state(wl: Workload):
     """(tokens [B], positions [3, B], cache_position [B], slot_ids [B], finished [B]) at the
     first decode step: the new token is written at the prefilled length and rotated at
