@@ -368,6 +368,12 @@ struct StepArgs {
 };
 
 // Queue the whole decode step (5 kernels per layer + the LM head) on `st`.
+// At one row the attention kernel can take over the QKV projection (whole QKV tiles per
+// cluster rank, K <= 16 groups).
+bool fused_qkv(const kmr_model_config& c) {
+    return attn_can_fuse_qkv(c.head_dim, c.n_q_heads / c.n_kv_heads, c.hidden);
+}
+
 int enqueue_step(kmr_model* m, const StepArgs& a, cudaStream_t st) {
     const kmr_model_config& c = m->cfg;
     const int B = a.B;
@@ -375,27 +381,43 @@ int enqueue_step(kmr_model* m, const StepArgs& a, cudaStream_t st) {
     const int nqkv = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
     const int grid = m->sms;
     bool pdl = false;   // the first kernel of the step has no kernel predecessor inside the graph
+    // One row: the attention kernel computes each head group's QKV rows itself (no QKV launch).
+    const bool fuse_qkv = B == 1 && fused_qkv(c);
     for (int l = 0; l < c.n_layers; ++l) {
         LayerW& L = m->layers[l];
         GemvLaunch g = {};
-        // fused QKV (+ input RMSNorm; layer 0 embeds the tokens)
-        g.w = L.w[KMR_W_QKV];
-        g.g = L.g[KMR_W_QKV];
-        g.in_kind = l == 0 ? IN_EMBED_NORM : IN_F32_NORM;
-        g.x = m->x_resid;
-        g.embed = m->embed;
-        g.tokens = a.tok;
-        g.vocab = c.vocab;
-        g.x_out = l == 0 ? m->x_resid : nullptr;
-        g.norm_w = L.norm[KMR_N_INPUT];
-        g.eps = c.eps;
-        g.epi = EPI_STORE;
-        g.y = m->qkv;
-        g.ldy = nqkv;
-        if (enqueue_gemv(g, B, m->err, st, pdl, grid, m->poison, m->poison_pattern) < 0) return KMR_ERR_CUDA;
-        pdl = true;
+        if (!fuse_qkv) {
+            // fused QKV (+ input RMSNorm; layer 0 embeds the tokens)
+            g.w = L.w[KMR_W_QKV];
+            g.g = L.g[KMR_W_QKV];
+            g.in_kind = l == 0 ? IN_EMBED_NORM : IN_F32_NORM;
+            g.x = m->x_resid;
+            g.embed = m->embed;
+            g.tokens = a.tok;
+            g.vocab = c.vocab;
+            g.x_out = l == 0 ? m->x_resid : nullptr;
+            g.norm_w = L.norm[KMR_N_INPUT];
+            g.eps = c.eps;
+            g.epi = EPI_STORE;
+            g.y = m->qkv;
+            g.ldy = nqkv;
+            if (enqueue_gemv(g, B, m->err, st, pdl, grid, m->poison, m->poison_pattern) < 0) return KMR_ERR_CUDA;
+            pdl = true;
+        }
         // attention (+ q/k norm, M-RoPE, KV write)
         AttnParams ap = {};
+        if (fuse_qkv) {
+            ap.wqkv = L.w[KMR_W_QKV];
+            ap.qkv_tile_bytes = L.g[KMR_W_QKV].tile_bytes;
+            ap.hidden = c.hidden;
+            ap.x_kind = l == 0 ? IN_EMBED_NORM : IN_F32_NORM;
+            ap.x = m->x_resid;
+            ap.embed = m->embed;
+            ap.tokens = a.tok;
+            ap.vocab = c.vocab;
+            ap.x_out = l == 0 ? m->x_resid : nullptr;
+            ap.in_norm_w = L.norm[KMR_N_INPUT];
+        }
         ap.in = m->qkv;
         ap.in_ld = nqkv;
         ap.fused = 1;
@@ -427,6 +449,7 @@ int enqueue_step(kmr_model* m, const StepArgs& a, cudaStream_t st) {
         ap.err = m->err;
         if (m->poison && launch_smem_poison(m->poison_pattern, grid, st) != cudaSuccess) return KMR_ERR_CUDA;
         if (launch_attn(ap, st, pdl) != cudaSuccess) return KMR_ERR_CUDA;
+        pdl = true;
         // O projection + residual
         g = GemvLaunch{};
         g.w = L.w[KMR_W_O];
@@ -820,6 +843,7 @@ extern "C" int kmr_model_kernels_per_step(const kmr_model* m, int B) {
         const int rows = gemv_two_halves_ok(g.tiles, gemv_grid(g.tiles, grid), g.tile_bytes) ? 2 * kMaxMB : kMaxMB;
         gemv_launches += (B + rows - 1) / rows;
     }
+    if (B == 1 && fused_qkv(c)) gemv_launches -= 1;          // QKV runs inside the attention kernel
     const int head_passes = (B + kMaxHeadRows - 1) / kMaxHeadRows;
     const int k = c.n_layers * (gemv_launches + 1) + head_passes;
     return m->poison ? 2 * k : k;                 // the diagnostic adds one fill per kernel

@@ -40,6 +40,7 @@
 #include <cooperative_groups.h>
 #include <math.h>
 
+#include "kmr_int4_mma.cuh"
 #include "kmr_internal.cuh"
 
 namespace cg = cooperative_groups;
@@ -58,13 +59,26 @@ constexpr float kLog2e = 1.4426950408889634f;
 __host__ __device__ inline size_t al16a(size_t v) { return (v + 15) & ~size_t(15); }
 
 struct AttnSmem {
-    size_t bar, kst, vst, knew, vnew, qs, wml, wo, co, cml, recv, flag, total;
+    size_t bar, kst, vst, knew, vnew, qs, wml, wo, co, cml, recv, flag;
+    size_t qbar, qw, qxw, qxst, qss, qpart, qkvh;              // fused QKV projection
+    size_t total;
 };
-__host__ __device__ inline AttnSmem attn_layout(int D, int rep, int nstage, int sub) {
+// QKV tiles (16 rows) of a head group per cluster rank: (rep q heads + k + v) x D rows / 16 / 8.
+__host__ __device__ inline int qkv_tiles_per_rank(int D, int rep) { return (rep + 2) * D / 128; }
+__host__ __device__ inline AttnSmem attn_layout(int D, int rep, int nstage, int sub, int qkv_tb) {
     AttnSmem L;
     const int per = rep * D / 8;                                // output slice merged by each cluster rank
+    const int tpr = qkv_tiles_per_rank(D, rep);
     size_t o = 0;
     L.bar = o;   o += al16a(kMaxStages * 8);
+    L.qbar = o;  o += 16;
+    o = (o + 127) & ~size_t(127);
+    L.qw = o;    o += qkv_tb ? size_t(tpr) * qkv_tb : 0;        // this rank's QKV weight tiles
+    L.qxw = o;   o += qkv_tb ? size_t(8) * 2 * 128 * 2 : 0;     // per warp: 2 staged groups of x
+    L.qxst = o;  o += qkv_tb ? size_t(16) * 16 * 4 : 0;         // per group: (X', 1/sigma) x 8 rows
+    L.qss = o;   o += qkv_tb ? 16 * 4 : 0;                       // per group: sum of x^2
+    L.qpart = o; o += qkv_tb ? size_t(tpr) * 16 * 16 * 4 : 0;   // per tile, per group: 16 rows
+    L.qkvh = o;  o += qkv_tb ? al16a(size_t(rep + 2) * D * 4) : 0;   // the head group's q, k, v
     o = (o + 127) & ~size_t(127);
     L.kst = o;   o += size_t(nstage) * sub * D * 2;
     L.vst = o;   o += size_t(nstage) * sub * D * 2;
@@ -107,7 +121,120 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
     return v[0];
 }
 
-template <int D, int REP, bool CLUSTER, int CH>
+// Fixed pairwise tree over 16 values v[i * stride] (the int4 GEMV's warp-partial order).
+__device__ __forceinline__ float tree16(const float* v, int stride) {
+    float a[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a[i] = v[i * stride];
+#pragma unroll
+    for (int n = 8; n > 0; n >>= 1)
+#pragma unroll
+        for (int i = 0; i < n; ++i) a[i] = __fadd_rn(a[2 * i], a[2 * i + 1]);
+    return a[0];
+}
+
+// Fused QKV projection of one cluster rank for one row (see AttnParams): stage the row's
+// RMSNorm input (warp w: groups w and w + 8), multiply this rank's QKV tiles on the tensor
+// cores, reduce each tile's 16 group partials in the one-row GEMV's fixed order, apply the
+// RMSNorm factor and push the rank's rows into every rank's q/k/v buffer.  Every step
+// mirrors the one-row int4 GEMV (kmr_gemv.cu), so a row's q, k, v are the same bits
+// whether the step ran it fused (batch 1) or through the GEMV (larger batches).
+template <int D, int REP>
+__device__ __forceinline__ void qkv_phase(const AttnParams& p, uint8_t* smem, const AttnSmem& L, int s, int h,
+                                          int lane, int warp, const uint2 (&nwv)[2]) {
+    constexpr int TPR = (REP + 2) * D / 128;
+    const int K = p.hidden, G = K >> 7;
+    const int tid = threadIdx.x;
+    __half* xw = reinterpret_cast<__half*>(smem + L.qxw) + warp * 2 * 128;
+    float* xst = reinterpret_cast<float*>(smem + L.qxst);
+    float* ssg = reinterpret_cast<float*>(smem + L.qss);
+    float* part = reinterpret_cast<float*>(smem + L.qpart);
+    float* qkvh = reinterpret_cast<float*>(smem + L.qkvh);
+    const uint8_t* qw = smem + L.qw;
+    uint64_t* qbar = reinterpret_cast<uint64_t*>(smem + L.qbar);
+    const bool embed = p.x_kind == IN_EMBED_NORM;
+    float4 xv[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int g = warp + 8 * j;
+        xv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (g >= G) continue;
+        const size_t k = size_t(g) * 128 + lane * 4;
+        if (embed) {
+            int tok = p.tokens[0];
+            if (tok < 0 || tok >= p.vocab) {
+                if (lane == 0 && g == 0 && s == 0 && h == 0) set_error(p.err, KMR_ERR_INVALID_ARG);
+                tok = 0;
+            }
+            const uint2 raw = *reinterpret_cast<const uint2*>(p.embed + size_t(tok) * K + k);
+            xv[j] = make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
+            if (s == 0 && h == 0 && p.x_out) *reinterpret_cast<float4*>(p.x_out + k) = xv[j];
+        } else {
+            xv[j] = *reinterpret_cast<const float4*>(p.x + k);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int g = warp + 8 * j;
+        const float w0 = bf16_lo(nwv[j].x), w1 = bf16_hi(nwv[j].x), w2 = bf16_lo(nwv[j].y), w3 = bf16_hi(nwv[j].y);
+        float u[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ss = __fmaf_rn(u[e], u[e], ss);
+        u[0] = __fmul_rn(u[0], w0);
+        u[1] = __fmul_rn(u[1], w1);
+        u[2] = __fmul_rn(u[2], w2);
+        u[3] = __fmul_rn(u[3], w3);
+        const float la = fmaxf(fmaxf(fabsf(u[0]), fabsf(u[1])), fmaxf(fabsf(u[2]), fabsf(u[3])));
+        float sig, isg;
+        pow2_scale(__reduce_max_sync(0xffffffffu, __float_as_uint(la)), sig, isg);
+        const __half2 h01 = __floats2half2_rn(__fmul_rn(u[0], sig), __fmul_rn(u[1], sig));
+        const __half2 h23 = __floats2half2_rn(__fmul_rn(u[2], sig), __fmul_rn(u[3], sig));
+        const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+        float gs = __fadd_rn(__fadd_rn(f01.x, f01.y), __fadd_rn(f23.x, f23.y));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            gs = __fadd_rn(gs, __shfl_xor_sync(0xffffffffu, gs, off));
+            ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
+        }
+        __half* blk = xw + j * 128;
+        *reinterpret_cast<__half2*>(blk + bpos(lane * 4)) = h01;
+        *reinterpret_cast<__half2*>(blk + bpos(lane * 4 + 2)) = h23;
+        if (lane < 16) xst[g * 16 + lane] = g < G ? (lane == 0 ? gs : (lane == 1 ? isg : 0.f)) : 0.f;
+        if (lane == 0) ssg[g] = g < G ? ss : 0.f;
+    }
+    __syncwarp();
+    mbar_wait(qbar, 0u, p.err);
+    const int gl = lane >> 2;
+    for (int t = 0; t < TPR; ++t) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int g = warp + 8 * j;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            if (g < G) {
+                XFrag xf;
+                load_xfrag(xf, xw + j * 128, gl == 0, lane, xst + g * 16);
+                group_product<false>(qw + size_t(t) * p.qkv_tile_bytes + size_t(g) * kGroupBytes, xf, lane, acc);
+            }
+            if ((lane & 3) == 0) {
+                part[(t * 16 + g) * 16 + gl] = acc[0];
+                part[(t * 16 + g) * 16 + gl + 8] = acc[2];
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < TPR * 16) {
+        const int t = tid >> 4, rr = tid & 15;
+        const float nf = rsqrtf(tree16(ssg, 1) / float(K) + p.eps);
+        const float v = __fmul_rn(tree16(part + t * 256 + rr, 16), nf);
+        const int hr = (s * TPR + t) * 16 + rr;              // row within the head group's q|k|v
+#pragma unroll
+        for (int r = 0; r < kAttnClusterSplits; ++r) cg::this_cluster().map_shared_rank(qkvh, r)[hr] = v;
+    }
+    cg::this_cluster().sync();
+}
+
+template <int D, int REP, bool CLUSTER, int CH, bool QKVF>
 __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int EPL = D / 32;               // contiguous dims per lane
@@ -120,7 +247,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nst = p.nstage;
-    const AttnSmem L = attn_layout(D, REP, nst, kSub);
+    const AttnSmem L = attn_layout(D, REP, nst, kSub, QKVF ? p.qkv_tile_bytes : 0);
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
     uint16_t* kst = reinterpret_cast<uint16_t*>(smem + L.kst);
     uint16_t* vst = reinterpret_cast<uint16_t*>(smem + L.vst);
@@ -147,6 +274,18 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
             pdl_wait();
             if (!fin && h == 0 && tid == 0) set_error(p.err, bad_slot ? KMR_ERR_SLOT_RANGE : KMR_ERR_CACHE_FULL);
             for (int i = tid; i < REP * D; i += kThreads) outrow[i] = 0.f;
+            if constexpr (QKVF) {
+                // the layer-0 embedding still lands in the residual, as the GEMV path stores it
+                if (h == 0 && p.x_kind == IN_EMBED_NORM && p.x_out) {
+                    int tok = p.tokens[0];
+                    if (tok < 0 || tok >= p.vocab) {
+                        if (tid == 0) set_error(p.err, KMR_ERR_INVALID_ARG);
+                        tok = 0;
+                    }
+                    for (int k = tid; k < p.hidden; k += kThreads)
+                        p.x_out[k] = bf16_to_f32(p.embed[size_t(tok) * p.hidden + k]);
+                }
+            }
         }
         return;
     }
@@ -164,6 +303,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
 
     if (tid == 0) {
         for (int i = 0; i < nst; ++i) mbar_init(&bar[i], 1);
+        if constexpr (QKVF) mbar_init(reinterpret_cast<uint64_t*>(smem + L.qbar), 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -185,6 +325,30 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
         const int n0 = nsub < nst ? nsub : nst;
         for (int i = 0; i < n0; ++i) issue(i);
     }
+    uint2 qnw[2] = {make_uint2(0, 0), make_uint2(0, 0)};
+    if constexpr (QKVF) {
+        constexpr int TPR = (REP + 2) * D / 128, QT = REP * D / 16, KT = D / 16;
+        if (tid == 0) {
+            // this rank's tiles of the head group's rows [q heads | k | v], each one contiguous copy
+            uint64_t* qbar = reinterpret_cast<uint64_t*>(smem + L.qbar);      // initialised above
+            const uint32_t tb = uint32_t(p.qkv_tile_bytes);
+            mbar_arrive_expect_tx(qbar, tb * TPR);
+            const uint64_t pol = policy_evict_first();
+            for (int t = 0; t < TPR; ++t) {
+                const int li = s * TPR + t;
+                const int gt = li < QT ? h * QT + li
+                                       : (li < QT + KT ? p.nq * D / 16 + h * KT + (li - QT)
+                                                       : (p.nq + p.nkv) * D / 16 + h * KT + (li - QT - KT));
+                bulk_g2s_stream(smem + L.qw + size_t(t) * tb, p.wqkv + size_t(gt) * tb, tb, qbar, pol);
+            }
+        }
+        const int G = p.hidden >> 7;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int g = warp + 8 * j;
+            if (g < G) qnw[j] = *reinterpret_cast<const uint2*>(p.in_norm_w + size_t(g) * 128 + lane * 4);
+        }
+    }
     // constants of the prologue, and the RoPE angles of this row's positions, before the wait
     const bool qk_warp = p.fused && warp <= REP;
     float nw[EPL], cs[EPL], sn[EPL];
@@ -202,15 +366,22 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     pdl_launch_dependents();
     pdl_wait();
 
+    if constexpr (QKVF) qkv_phase<D, REP>(p, smem, L, s, h, lane, warp, qnw);
+
     // ---- prologue: q (and, fused, the new k / v) of this KV head
     const float qscale = __fmul_rn(p.scale, kLog2e);       // scores in base 2
     const float* in = p.in + size_t(b) * p.in_ld;
     if (p.fused) {
         if (warp <= REP + 1) {
             const bool isq = warp < REP, isk = warp == REP;
-            const float* src = isq ? in + size_t(h * REP + warp) * D
-                                   : (isk ? in + size_t(p.nq) * D + size_t(h) * D
-                                          : in + size_t(p.nq + p.nkv) * D + size_t(h) * D);
+            const float* src;
+            if constexpr (QKVF) {
+                const float* qkvh = reinterpret_cast<const float*>(smem + L.qkvh);   // [q heads | k | v]
+                src = qkvh + size_t(isq ? warp : (isk ? REP : REP + 1)) * D;
+            } else {
+                src = isq ? in + size_t(h * REP + warp) * D
+                          : (isk ? in + size_t(p.nq) * D + size_t(h) * D : in + size_t(p.nq + p.nkv) * D + size_t(h) * D);
+            }
             float x[EPL];
 #pragma unroll
             for (int e = 0; e < EPL; ++e) x[e] = src[lane * EPL + e];
@@ -469,20 +640,21 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     }
 }
 
-template <bool CL, int CH>
+template <bool CL, int CH, bool QF>
 const void* attn_fn_ch(int d, int rep) {
     if (d == 64) {
-        if (rep == 1) return (const void*)attn_kernel<64, 1, CL, CH>;
-        if (rep == 2) return (const void*)attn_kernel<64, 2, CL, CH>;
-        return (const void*)attn_kernel<64, 4, CL, 8>;
+        if (rep == 1) return (const void*)attn_kernel<64, 1, CL, CH, false>;   // (REP + 2) x 64 rows: no whole tiles per rank
+        if (rep == 2) return (const void*)attn_kernel<64, 2, CL, CH, QF>;
+        return (const void*)attn_kernel<64, 4, CL, 8, QF>;
     }
-    if (rep == 1) return (const void*)attn_kernel<128, 1, CL, CH>;
-    if (rep == 2) return (const void*)attn_kernel<128, 2, CL, CH>;
-    return (const void*)attn_kernel<128, 4, CL, 8>;
+    if (rep == 1) return (const void*)attn_kernel<128, 1, CL, CH, QF>;
+    if (rep == 2) return (const void*)attn_kernel<128, 2, CL, CH, QF>;
+    return (const void*)attn_kernel<128, 4, CL, 8, QF>;
 }
 template <bool CL>
-const void* attn_fn(int d, int rep, int ch) {
-    return ch == 16 ? attn_fn_ch<CL, 16>(d, rep) : attn_fn_ch<CL, 8>(d, rep);
+const void* attn_fn(int d, int rep, int ch, bool qkv = false) {
+    if (CL && qkv) return ch == 16 ? attn_fn_ch<CL, 16, CL>(d, rep) : attn_fn_ch<CL, 8, CL>(d, rep);
+    return ch == 16 ? attn_fn_ch<CL, 16, false>(d, rep) : attn_fn_ch<CL, 8, false>(d, rep);
 }
 
 }  // namespace
@@ -505,7 +677,12 @@ int attn_stages(int max_len, int splits, int ch, int d) {
     if (n > cap) n = cap;
     return n < 1 ? 1 : n;
 }
-size_t attn_smem_bytes(int d, int rep, int nstage, int ch) { return attn_layout(d, rep, nstage, 8 * ch).total; }
+size_t attn_smem_bytes(int d, int rep, int nstage, int ch, int qkv_tb) {
+    return attn_layout(d, rep, nstage, 8 * ch, qkv_tb).total;
+}
+bool attn_can_fuse_qkv(int d, int rep, int hidden) {
+    return ((rep + 2) * d) % 128 == 0 && hidden % 128 == 0 && hidden / 128 <= 16;
+}
 int attn_default_tsplit(int nkv) {
     int t = (num_sms() + nkv - 1) / nkv;
     return t < 1 ? 1 : (t > 32 ? 32 : t);
@@ -523,7 +700,9 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t st, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(q.tsplit, p.nkv, p.B);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = attn_smem_bytes(p.d, rep, q.nstage, ch);
+    const bool qkv = p.cluster && p.wqkv != nullptr && p.B == 1 && attn_can_fuse_qkv(p.d, rep, p.hidden);
+    if (!qkv) q.wqkv = nullptr;
+    cfg.dynamicSmemBytes = attn_smem_bytes(p.d, rep, q.nstage, ch, qkv ? p.qkv_tile_bytes : 0);
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     int n = 0;
@@ -541,7 +720,7 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t st, bool pdl) {
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    const void* fn = p.cluster ? attn_fn<true>(p.d, rep, ch) : attn_fn<false>(p.d, rep, ch);
+    const void* fn = p.cluster ? attn_fn<true>(p.d, rep, ch, qkv) : attn_fn<false>(p.d, rep, ch);
     void* args[] = {&q};
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
@@ -551,9 +730,9 @@ cudaError_t attn_set_attributes() {
     const int reps[3] = {1, 2, 4}, ds[2] = {64, 128};
     for (int d : ds)
         for (int r : reps)
-            for (int cl = 0; cl < 4; ++cl) {
+            for (int cl = 0; cl < 8; ++cl) {
                 const int ch = (cl & 2) ? 16 : 8;
-                const void* k = (cl & 1) ? attn_fn<true>(d, r, ch) : attn_fn<false>(d, r, ch);
+                const void* k = (cl & 1) ? attn_fn<true>(d, r, ch, (cl & 4) != 0) : attn_fn<false>(d, r, ch);
                 cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
                 if (e != cudaSuccess) return e;
                 e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,

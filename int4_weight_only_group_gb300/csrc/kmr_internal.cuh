@@ -232,15 +232,32 @@ struct AttnParams {
     float* part;                 // [B][nkv][tsplit][rep][d+2]
     int* counters;               // [B][nkv]
     int* err;
+    // Fused QKV projection (cluster mode, one row; wqkv == null: off).  Rank s of the cluster
+    // of KV head h computes the head group's QKV rows [s, s+1) * tpr tiles itself, with the
+    // one-row int4 GEMV's arithmetic, and the cluster all-gathers them through distributed
+    // shared memory; the attention prologue then reads q, k, v from shared memory.
+    const uint8_t* wqkv;         // packed QKV weights (KMR4; N = (nq + 2 nkv) d, K = hidden)
+    int qkv_tile_bytes;          // (hidden / 128) * 1088
+    int hidden;
+    int x_kind;                  // IN_F32_NORM (x = residual row) or IN_EMBED_NORM (x = E[token])
+    const float* x;              // residual row fp32 [hidden]
+    const uint16_t* embed;       // bf16 [vocab][hidden]
+    const int32_t* tokens;       // token of the row (IN_EMBED_NORM)
+    int vocab;
+    float* x_out;                // IN_EMBED_NORM: the embedded row is stored here (one CTA)
+    const uint16_t* in_norm_w;   // bf16 [hidden]: input RMSNorm weight
 };
 // Shared-memory poisoning diagnostic (kmr_poison.cu).
 cudaError_t poison_set_attributes();
 cudaError_t launch_smem_poison(uint32_t pattern, int sms, cudaStream_t st);
 
 constexpr int kAttnClusterSplits = 8;     // cluster size of the DSMEM-merged attention (portable)
-size_t attn_smem_bytes(int d, int rep, int nstage, int ch);
+size_t attn_smem_bytes(int d, int rep, int nstage, int ch, int qkv_tb);
 int attn_stages(int max_len, int splits, int ch, int d);
 int attn_chunk(int max_len, int splits, int rep);
+// The attention kernel can take over the one-row QKV projection when a cluster rank gets whole
+// 16-row tiles of the head group's QKV rows and K fits 16 groups of 128.
+bool attn_can_fuse_qkv(int d, int rep, int hidden);
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t st, bool pdl);
 size_t attn_workspace_bytes(int B, int nq, int nkv, int d, int tsplit);
 int attn_default_tsplit(int nkv);

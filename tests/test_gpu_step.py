@@ -237,7 +237,8 @@ def test_batch_invariance_and_determinism(torch):
     m2.close()
 
 
-def test_step_ignores_stale_shared_memory(torch):
+@pytest.mark.parametrize("B", [4, 1])                 # batch 1: QKV inside the attention kernel
+def test_step_ignores_stale_shared_memory(torch, B):
     """Every kernel of the step preceded by a shared-memory fill of NaN / Inf bits gives the
     same step bit for bit (rows 1 and 2 end their last split on a lone position)."""
     from workloads import Workload
@@ -245,34 +246,37 @@ def test_step_ignores_stale_shared_memory(torch):
     wl = Workload("tiny b4", cfg, 0, batch=4, prefill=[10, 38, 70, 127], rope_delta=[0, -3, -7, 0],
                   slot_ids=[2, 0, 3, 1], first_tokens=[5, 77, 300, 1000], steps=1)
     m, _ = build_model(wl, max_batch=4)
-    st = od.initial_state(wl)
+    st = [a[..., 2:2 + B] if B == 1 else a for a in od.initial_state(wl)]
     clean = Dev(torch, *st, cfg.vocab)
     clean.step(m)
     ref = clean.host()
     assert np.all(np.isfinite(ref[4]))
-    base = m.kernels_per_step(4)
+    base = m.kernels_per_step(B)
     for pat in (0xFFFFFFFF, 0x7F807F80):
         m.set_smem_poison(True, pat)
-        assert m.kernels_per_step(4) == 2 * base
+        assert m.kernels_per_step(B) == 2 * base
         dev = Dev(torch, *st, cfg.vocab)
         dev.step(m)
         for a, b in zip(dev.host(), ref):
             assert np.array_equal(a, b), hex(pat)
     m.set_smem_poison(False)
-    assert m.kernels_per_step(4) == base
+    assert m.kernels_per_step(B) == base
     m.close()
 
 
+@pytest.mark.parametrize("B", [3, 1])
 @pytest.mark.parametrize("nq,nkv", [(4, 2), (8, 2), (4, 4), (8, 4)])
-def test_head_layouts(torch, nq, nkv):
+def test_head_layouts(torch, nq, nkv, B):
     """1, 2 and 4 query heads per KV head (head_dim 64) match the oracle over 3
-    teacher-forced steps at batch 3."""
+    teacher-forced steps at batch 3 and batch 1 (where the attention kernel computes the
+    QKV rows itself whenever a head group gives each cluster rank whole 16-row tiles)."""
     from workloads import Workload
     cfg = tiny_config(n_q_heads=nq, n_kv_heads=nkv, slots=3)
-    wl = Workload("tiny heads", cfg, 5, batch=3, prefill=[9, 40, 77], rope_delta=[0, -2, -5],
-                  slot_ids=[1, 2, 0], first_tokens=[3, 500, 77], steps=3)
+    wl = Workload("tiny heads", cfg, 5, batch=B, prefill=[9, 40, 77][:B], rope_delta=[0, -2, -5][:B],
+                  slot_ids=[1, 2, 0][:B], first_tokens=[3, 500, 77][:B], steps=3)
     m, _ = build_model(wl, max_batch=3)
-    assert m.kernels_per_step(3) == cfg.n_layers * 5 + 1
+    fused = B == 1 and ((nq // nkv + 2) * cfg.head_dim) % 128 == 0
+    assert m.kernels_per_step(B) == cfg.n_layers * (4 if fused else 5) + 1
     o = od.OracleDecoder.for_workload(wl)
     st = od.initial_state(wl)
     dev = Dev(torch, *st, cfg.vocab)
