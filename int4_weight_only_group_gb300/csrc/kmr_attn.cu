@@ -95,32 +95,6 @@ __host__ __device__ inline AttnSmem attn_layout(int D, int rep, int nstage, int 
     return L;
 }
 
-// Sum of NV per-lane values over the warp, scattered: value i's total ends on the
-// lanes l with l / (32 / NV) == i.  Fixed shuffle order, so deterministic.
-template <int NV>
-__device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
-    int n = NV;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        if (n > 1) {
-            const int half = n / 2;
-            const bool up = (lane & off) != 0;
-#pragma unroll
-            for (int i = 0; i < NV / 2; ++i) {
-                if (i < half) {
-                    const float keep = up ? v[i + half] : v[i];
-                    const float send = up ? v[i] : v[i + half];
-                    v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, off));
-                }
-            }
-            n = half;
-        } else {
-            v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xffffffffu, v[0], off));
-        }
-    }
-    return v[0];
-}
-
 // Fixed pairwise tree over 16 values v[i * stride] (the int4 GEMV's warp-partial order).
 __device__ __forceinline__ float tree16(const float* v, int stride) {
     float a[16];
@@ -173,6 +147,9 @@ __device__ __forceinline__ void qkv_phase(const AttnParams& p, uint8_t* smem, co
             xv[j] = *reinterpret_cast<const float4*>(p.x + k);
         }
     }
+    // (X' of both groups, sum of squares of both groups) in one reduce-scatter: lanes
+    // 8i..8i+7 end with value i (the butterfly's bits)
+    float rv[4];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         const int g = warp + 8 * j;
@@ -191,36 +168,46 @@ __device__ __forceinline__ void qkv_phase(const AttnParams& p, uint8_t* smem, co
         const __half2 h01 = __floats2half2_rn(__fmul_rn(u[0], sig), __fmul_rn(u[1], sig));
         const __half2 h23 = __floats2half2_rn(__fmul_rn(u[2], sig), __fmul_rn(u[3], sig));
         const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-        float gs = __fadd_rn(__fadd_rn(f01.x, f01.y), __fadd_rn(f23.x, f23.y));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            gs = __fadd_rn(gs, __shfl_xor_sync(0xffffffffu, gs, off));
-            ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
-        }
+        rv[j] = __fadd_rn(__fadd_rn(f01.x, f01.y), __fadd_rn(f23.x, f23.y));
+        rv[2 + j] = ss;
         __half* blk = xw + j * 128;
         *reinterpret_cast<__half2*>(blk + bpos(lane * 4)) = h01;
         *reinterpret_cast<__half2*>(blk + bpos(lane * 4 + 2)) = h23;
-        if (lane < 16) xst[g * 16 + lane] = g < G ? (lane == 0 ? gs : (lane == 1 ? isg : 0.f)) : 0.f;
-        if (lane == 0) ssg[g] = g < G ? ss : 0.f;
+        if (lane >= 1 && lane < 16) xst[g * 16 + lane] = (g < G && lane == 1) ? isg : 0.f;
+    }
+    const float tot = reduce_scatter<4>(rv, lane);
+    if ((lane & 7) == 0) {
+        const int i = lane >> 3, g = warp + 8 * (i & 1);
+        if (i < 2) xst[g * 16] = g < G ? tot : 0.f;
+        else ssg[g] = g < G ? tot : 0.f;
     }
     __syncwarp();
-    mbar_wait(qbar, 0u, p.err);
     const int gl = lane >> 2;
-    for (int t = 0; t < TPR; ++t) {
+    // both groups' fragments once, then all TPR x 2 block products unrolled: independent
+    // accumulator chains the scheduler can interleave
+    XFrag xf[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) load_xfrag(xf[j], xw + j * 128, gl == 0, lane, xst + (warp + 8 * j) * 16);
+    mbar_wait(qbar, 0u, p.err);
+    float acc[TPR][2][4];
+#pragma unroll
+    for (int t = 0; t < TPR; ++t)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const int g = warp + 8 * j;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            if (g < G) {
-                XFrag xf;
-                load_xfrag(xf, xw + j * 128, gl == 0, lane, xst + g * 16);
-                group_product<false>(qw + size_t(t) * p.qkv_tile_bytes + size_t(g) * kGroupBytes, xf, lane, acc);
-            }
-            if ((lane & 3) == 0) {
-                part[(t * 16 + g) * 16 + gl] = acc[0];
-                part[(t * 16 + g) * 16 + gl + 8] = acc[2];
-            }
+            acc[t][j][0] = acc[t][j][1] = acc[t][j][2] = acc[t][j][3] = 0.f;
+            if (warp + 8 * j < G)
+                group_product<false>(qw + size_t(t) * p.qkv_tile_bytes + size_t(warp + 8 * j) * kGroupBytes, xf[j],
+                                     lane, acc[t][j]);
         }
+    if ((lane & 3) == 0) {
+#pragma unroll
+        for (int t = 0; t < TPR; ++t)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int g = warp + 8 * j;
+                part[(t * 16 + g) * 16 + gl] = acc[t][j][0];
+                part[(t * 16 + g) * 16 + gl + 8] = acc[t][j][2];
+            }
     }
     __syncthreads();
     if (tid < TPR * 16) {

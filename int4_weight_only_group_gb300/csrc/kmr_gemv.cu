@@ -216,14 +216,32 @@ __device__ __forceinline__ void gemv_rows(const GemvParams p, uint8_t* smem, con
             gs[j][m] = __fadd_rn(__fadd_rn(f01.x, f01.y), __fadd_rn(f23.x, f23.y));
         }
     }
+    // the warp sums of every (group, row) X' and every row's sum of squares in one
+    // reduce-scatter (the butterfly's bits, fewer shuffles); value i lands on lanes
+    // [i * LPV, (i + 1) * LPV)
+    // (up to 40 values: the first 32 in one pass, the rest in a second)
+    constexpr int NVAL = GPW * MB + MB;
+    constexpr int NA = NVAL < 32 ? NVAL : 32, NB = NVAL - NA;
+    static_assert(NB <= 32, "two passes at most");
+    constexpr int NVA = pow2_at_least(NA), NVB = pow2_at_least(NB);
+    auto value = [&](int i) { return i < GPW * MB ? gs[i / MB][i % MB] : ss[i - GPW * MB]; };
+    auto put = [&](int vi, float tot) {
+        if (vi < GPW * MB) {
+            if (warp + (vi / MB) * kGemvWarps < G) xst[(vi / MB) * 16 + (vi % MB) * 2] = tot;
+        } else if (vi < NVAL) {
+            ssw[warp * 8 + vi - GPW * MB] = tot;
+        }
+    };
+    float va[NVA];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
+    for (int i = 0; i < NVA; ++i) va[i] = i < NA ? value(i) : 0.f;
+    const float tota = reduce_scatter<NVA>(va, lane);
+    float totb = 0.f;
+    if constexpr (NB > 0) {
+        float vb[NVB];
 #pragma unroll
-        for (int j = 0; j < GPW; ++j)
-#pragma unroll
-            for (int m = 0; m < MB; ++m) gs[j][m] = __fadd_rn(gs[j][m], __shfl_xor_sync(0xffffffffu, gs[j][m], off));
-#pragma unroll
-        for (int m = 0; m < MB; ++m) ss[m] = __fadd_rn(ss[m], __shfl_xor_sync(0xffffffffu, ss[m], off));
+        for (int i = 0; i < NVB; ++i) vb[i] = i < NB ? value(32 + i) : 0.f;
+        totb = reduce_scatter<NVB>(vb, lane);
     }
 #pragma unroll
     for (int j = 0; j < GPW; ++j) {
@@ -233,19 +251,19 @@ __device__ __forceinline__ void gemv_rows(const GemvParams p, uint8_t* smem, con
             __half* blk = xw + size_t(j * MB + m) * 128;
             *reinterpret_cast<__half2*>(blk + bpos(lane * 4)) = h01[j][m];
             *reinterpret_cast<__half2*>(blk + bpos(lane * 4 + 2)) = h23[j][m];
-            if (lane == 0 && grp < G) {
-                xst[j * 16 + m * 2] = gs[j][m];
-                xst[j * 16 + m * 2 + 1] = isg[j][m];
-            }
+            if (lane == 0 && grp < G) xst[j * 16 + m * 2 + 1] = isg[j][m];
         }
         if (lane == 0) {
 #pragma unroll
             for (int m = MB; m < 8; ++m) xst[j * 16 + m * 2] = xst[j * 16 + m * 2 + 1] = 0.f;
         }
     }
+    if (lane % (32 / NVA) == 0) put(lane / (32 / NVA), tota);
+    if constexpr (NB > 0)
+        if (lane % (32 / NVB) == 0) put(32 + lane / (32 / NVB), totb);
     if (lane == 0) {
 #pragma unroll
-        for (int m = 0; m < 8; ++m) ssw[warp * 8 + m] = m < MB ? ss[m] : 0.f;
+        for (int m = MB; m < 8; ++m) ssw[warp * 8 + m] = 0.f;
     }
     __syncwarp();
 

@@ -132,6 +132,38 @@ __device__ __forceinline__ T warp_sum(T v) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
+// Smallest power of two >= n (1 for n <= 1).
+__host__ __device__ constexpr int pow2_at_least(int n) { return n <= 1 ? 1 : 2 * pow2_at_least((n + 1) / 2); }
+
+// Sum of NV per-lane values over the warp, scattered: value i's total ends on the
+// lanes l with l / (32 / NV) == i.  Each level pairs lane l with l ^ off (off = 16 .. 1)
+// exactly as the xor butterfly of warp_sum does, and a sum is commutative, so every
+// value gets the same bits the butterfly gives it, with NV - 1 + log2(32 / NV)
+// shuffles instead of 5 NV.
+template <int NV>
+__device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
+    int n = NV;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        if (n > 1) {
+            const int half = n / 2;
+            const bool up = (lane & off) != 0;
+#pragma unroll
+            for (int i = 0; i < NV / 2; ++i) {
+                if (i < half) {
+                    const float keep = up ? v[i + half] : v[i];
+                    const float send = up ? v[i] : v[i + half];
+                    v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, off));
+                }
+            }
+            n = half;
+        } else {
+            v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xffffffffu, v[0], off));
+        }
+    }
+    return v[0];
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
