@@ -47,7 +47,7 @@ __host__ __device__ inline HeadSmem head_layout(int MB, int K, int nst) {
     L.cnt = o;   o += al16h(size_t(nst) * 4);
     L.wbv = o;   o += al16h(size_t(8) * MB * 4);
     L.wbi = o;   o += al16h(size_t(8) * MB * 4);
-    L.red2 = o;  o += al16h(size_t(8) * 4);
+    L.red2 = o;  o += al16h(size_t(MB) * 8 * 4);
     L.flag = o;  o += 16;
     o = (o + 127) & ~size_t(127);
     L.stage = o; o += size_t(nst) * 8 * head_row_bytes(K);
@@ -127,21 +127,27 @@ __global__ void __launch_bounds__(kHeadThreads, 1) head_kernel(const HeadParams 
     } else {
         pdl_launch_dependents();
         pdl_wait();
-        // ---- prologue: final RMSNorm of the residual rows, rounded to bf16
+        // ---- prologue: final RMSNorm of the residual rows, rounded to bf16.  Every row's
+        // sum of squares in one pass and one reduce-scatter (the butterfly's bits), so
+        // two barriers in all rather than two per row.
+        float ss[MB];
+#pragma unroll
+        for (int m = 0; m < MB; ++m) ss[m] = 0.f;
+        for (int k = tid; k < K; k += kThreads) {
+#pragma unroll
+            for (int m = 0; m < MB; ++m) {
+                const float v = m < p.M ? p.x[size_t(m) * K + k] : 0.f;
+                ss[m] = __fmaf_rn(v, v, ss[m]);
+            }
+        }
+        const float wsum = reduce_scatter<MB>(ss, lane);
+        if (lane % (32 / MB) == 0) red2[(lane / (32 / MB)) * 8 + warp] = wsum;
+        consumers_sync();
         for (int m = 0; m < MB; ++m) {
             const bool real = m < p.M;
-            float ss = 0.f;
-            for (int k = tid; k < K; k += kThreads) {
-                const float v = real ? p.x[size_t(m) * K + k] : 0.f;
-                ss = __fmaf_rn(v, v, ss);
-            }
-            ss = warp_sum(ss);
-            consumers_sync();
-            if (lane == 0) red2[warp] = ss;
-            consumers_sync();
             float tot = 0.f;
 #pragma unroll
-            for (int w = 0; w < 8; ++w) tot += red2[w];
+            for (int w = 0; w < 8; ++w) tot += red2[m * 8 + w];
             const float r = rsqrtf(tot / float(K) + p.eps);
             for (int k = tid; k < K; k += kThreads) {
                 const float v = real ? __fmul_rn(__fmul_rn(p.x[size_t(m) * K + k], r), bf16_to_f32(p.norm_w[k])) : 0.f;
