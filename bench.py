@@ -244,10 +244,36 @@ def run_kmr(args, rank: int, world: int) -> dict:
     out["gemv"] = time_gemv(torch, kmr, syn, cfg, B)
     # ---- end to end through the host-buffer C ABI call
     out["e2e"] = time_e2e(torch, model, wl, st0, args.steps)
+    # ---- slot migration: one whole cache row (every layer, K and V) per copy_row_from
+    out["kv_copy"] = time_kv_copy(torch, model, cfg)
     model.close()
     if not args.no_cpu_baseline:
         out["cpu"] = cpu_baseline(wl, syn)
     return out
+
+
+def time_kv_copy(torch, model, cfg, reps: int = 10) -> dict:
+    """CUDA-event time of kmr_model_copy_row_from moving a full max_len row (all layers, K and
+    V) from an external cache into slot 0; two alternating sources (> L2 together), so every
+    copy reads HBM.  Bytes = read + write of the row.  Runs after the timed decode region
+    (it overwrites slot 0)."""
+    L, nkv, S, d = cfg.n_layers, cfg.n_kv_heads, cfg.max_len, cfg.head_dim
+    srcs = [(torch.randint(-2 ** 15, 2 ** 15, (L, 1, nkv, S, d), dtype=torch.int16, device="cuda"),
+             torch.randint(-2 ** 15, 2 ** 15, (L, 1, nkv, S, d), dtype=torch.int16, device="cuda")) for _ in range(2)]
+    stream = torch.cuda.current_stream()
+    for i in range(3):
+        model.copy_row_from(0, S, 0, srcs[i % 2][0], srcs[i % 2][1], 1, S, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(reps):
+        model.copy_row_from(0, S, 0, srcs[i % 2][0], srcs[i % 2][1], 1, S, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert model.sync_status(stream) == 0
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    nbytes = 2 * (2 * L * nkv * S * d * 2)
+    return {"row_positions": S, "bytes": nbytes, "us": us, "gbs": nbytes / (us * 1e3)}
 
 
 def time_gemv(torch, kmr, syn, cfg, M: int) -> dict:
@@ -447,6 +473,8 @@ def main():
         "gemv_us": {k: round(v["us"], 2) for k, v in r["gemv"].items()},
         "gemv_gbs": {k: round(v["gbs"], 1) for k, v in r["gemv"].items()},
         "e2e": r["e2e"],
+        "kv_row_copy": {"us": round(r["kv_copy"]["us"], 2), "gbs": round(r["kv_copy"]["gbs"], 1),
+                        "frac": round(r["kv_copy"]["gbs"] / peaks["hbm_gbs"], 3), "bytes": r["kv_copy"]["bytes"]},
         "gpu_launches": r["kernels_per_step"] * args.steps,
         "clocks": r["clocks"],
         "setup_s": round(r["setup_s"], 1),

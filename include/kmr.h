@@ -239,6 +239,31 @@ int kmr_model_set_kv(kmr_model* m, int layer, int slot, int length,
 /* Device pointers of one layer's K and V cache ([slots][n_kv][max_len][d] bf16). */
 int kmr_model_kv_pointers(kmr_model* m, int layer, void** k_cache, void** v_cache);
 
+/* Row migration into the model's static cache ("kaminari", §08 The serving
+ * layer: the continuous scheduler's slot pool owns one static cache with a
+ * physical row per slot, and copy_row_from moves a row's KV state into it;
+ * §03 State model: the cache is mutated in place).
+ * Copies positions [0, length) of row src_row of a source cache into cache row
+ * dst_slot of the model, for every layer, K and V:
+ *   src_k, src_v   device pointers to layer 0 of a source cache laid out like
+ *                  the model's: [L][src_slots][n_kv][src_max_len][d] bf16 with
+ *                  the model's L, n_kv and d, 16-byte aligned, not overlapping
+ *                  the destination row.  Both NULL: the model's own cache
+ *                  (src_slots and src_max_len are then ignored), i.e. a slot to
+ *                  slot migration.
+ *   length         positions copied, 0 <= length <= min(src_max_len, max_len)
+ * Positions >= length of the destination row keep their contents.  One kernel
+ * launch queued on `stream`, no synchronisation; the source row must not be
+ * written nor the destination row used by a step until it has run.  Copying a
+ * row of the model's cache onto itself, or length 0, launches nothing.
+ * Errors: KMR_ERR_INVALID_ARG (NULL model, one source pointer NULL and not the
+ * other, misaligned source, src_slots or src_max_len <= 0, src_row outside an
+ * external source, negative length), KMR_ERR_SLOT_RANGE (dst_slot, or src_row
+ * of the model's own cache, outside [0, slots)), KMR_ERR_CACHE_FULL (length
+ * above either cache's max_len), KMR_ERR_CUDA. */
+int kmr_model_copy_row_from(kmr_model* m, int dst_slot, const uint16_t* src_k, const uint16_t* src_v,
+                            int src_slots, int src_max_len, int src_row, int length, void* stream);
+
 /* One greedy decode step for B rows ("kaminari", §04 Request lifecycle,
  * decode; §08 ContinuousBatchScheduler slots).  All pointers are device
  * memory; the step state is read and advanced in place:

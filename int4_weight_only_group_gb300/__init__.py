@@ -93,6 +93,7 @@ _SIGNATURES = {
     "kmr_model_set_embedding": (_I, [_P, _P]),
     "kmr_model_set_kv": (_I, [_P, _I, _I, _I, _P, _P]),
     "kmr_model_kv_pointers": (_I, [_P, _I, ctypes.POINTER(_P), ctypes.POINTER(_P)]),
+    "kmr_model_copy_row_from": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P]),
     "kmr_decode_step": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P]),
     "kmr_decode_step_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P]),
     "kmr_model_sync_status": (_I, [_P, _P]),
@@ -268,6 +269,14 @@ class Model:
         k, v = _P(), _P()
         _check(lib().kmr_model_kv_pointers(self._h, layer, ctypes.byref(k), ctypes.byref(v)), "kmr_model_kv_pointers")
         return k.value, v.value
+
+    def copy_row_from(self, dst_slot: int, length: int, src_row: int, src_k=None, src_v=None, src_slots: int = 0,
+                      src_max_len: int = 0, stream=None) -> None:
+        """kmr_model_copy_row_from: positions [0, length) of row src_row of a source cache (device
+        tensors or addresses of its layer 0, laid out like the model's cache; None: the model's own
+        cache) into cache row dst_slot, every layer, K and V.  Queued on `stream`."""
+        _check(lib().kmr_model_copy_row_from(self._h, dst_slot, _ptr(src_k), _ptr(src_v), src_slots, src_max_len,
+                                             src_row, length, _stream(stream)), "kmr_model_copy_row_from")
 
     def decode_step(self, token_ids, positions, cache_position, slot_ids, finished, B: int, logits=None,
                     stream=None) -> None:

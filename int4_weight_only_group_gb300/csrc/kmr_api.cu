@@ -722,6 +722,44 @@ extern "C" int kmr_model_set_kv(kmr_model* m, int layer, int slot, int length, c
     return KMR_OK;
 }
 
+extern "C" int kmr_model_copy_row_from(kmr_model* m, int dst_slot, const uint16_t* src_k, const uint16_t* src_v,
+                                       int src_slots, int src_max_len, int src_row, int length, void* stream) {
+    if (!m) return KMR_ERR_INVALID_ARG;
+    const kmr_model_config& c = m->cfg;
+    if ((src_k == nullptr) != (src_v == nullptr)) return KMR_ERR_INVALID_ARG;
+    const bool own = src_k == nullptr;
+    if (own) {
+        src_k = m->kc;
+        src_v = m->vc;
+        src_slots = c.slots;
+        src_max_len = c.max_len;
+    }
+    if ((reinterpret_cast<uintptr_t>(src_k) | reinterpret_cast<uintptr_t>(src_v)) & 15) return KMR_ERR_INVALID_ARG;
+    if (src_slots <= 0 || src_max_len <= 0) return KMR_ERR_INVALID_ARG;
+    if (src_row < 0 || src_row >= src_slots) return own ? KMR_ERR_SLOT_RANGE : KMR_ERR_INVALID_ARG;
+    if (dst_slot < 0 || dst_slot >= c.slots) return KMR_ERR_SLOT_RANGE;
+    if (length < 0) return KMR_ERR_INVALID_ARG;
+    if (length > c.max_len || length > src_max_len) return KMR_ERR_CACHE_FULL;
+    if (length == 0 || (own && src_row == dst_slot)) return KMR_OK;
+    DeviceGuard dg(m->device);
+    KvCopyParams p;
+    p.src_k = src_k;
+    p.src_v = src_v;
+    p.dst_k = m->kc;
+    p.dst_v = m->vc;
+    p.L = c.n_layers;
+    p.nkv = c.n_kv_heads;
+    p.d = c.head_dim;
+    p.src_slots = src_slots;
+    p.src_max_len = src_max_len;
+    p.src_row = src_row;
+    p.dst_slots = c.slots;
+    p.dst_max_len = c.max_len;
+    p.dst_row = dst_slot;
+    p.units = (long long)length * c.head_dim / 8;
+    return launch_kv_row_copy(p, m->sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KMR_OK : KMR_ERR_CUDA;
+}
+
 extern "C" int kmr_model_kv_pointers(kmr_model* m, int layer, void** k, void** v) {
     if (!m || !k || !v || layer < 0 || layer >= m->cfg.n_layers) return KMR_ERR_INVALID_ARG;
     *k = m->kc + size_t(layer) * m->kv_layer_elems;

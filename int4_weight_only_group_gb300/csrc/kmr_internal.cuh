@@ -280,6 +280,20 @@ struct AttnParams {
     const uint16_t* in_norm_w;   // bf16 [hidden]: input RMSNorm weight
 };
 // Shared-memory poisoning diagnostic (kmr_poison.cu).
+// KV row migration (kmr_slots.cu): positions [0, length) of one cache row, every layer,
+// K and V, from a source cache to a destination cache of the same L, n_kv and d.
+struct KvCopyParams {
+    const uint16_t* src_k;
+    const uint16_t* src_v;
+    uint16_t* dst_k;
+    uint16_t* dst_v;
+    int L, nkv, d;
+    int src_slots, src_max_len, src_row;
+    int dst_slots, dst_max_len, dst_row;
+    long long units;                        // 16-byte units per (layer, K/V, head) segment
+};
+cudaError_t launch_kv_row_copy(const KvCopyParams& p, int sms, cudaStream_t st);
+
 cudaError_t poison_set_attributes();
 cudaError_t launch_smem_poison(uint32_t pattern, int sms, cudaStream_t st);
 

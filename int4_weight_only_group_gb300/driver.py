@@ -8,7 +8,9 @@ one ``kmr_decode_step`` call.
 """
 from __future__ import annotations
 
-from typing import Dict, List, Optional, Sequence
+import collections
+import dataclasses
+from typing import Any, Callable, Dict, List, Optional, Sequence
 
 import numpy as np
 
@@ -89,3 +91,115 @@ def generate(model: Model, state: DeviceState, max_new_tokens: int, eos_id: int 
                 break
         fin_rows.append(row)
     return fin_rows
+
+
+# ------------------------------------------------------------------ continuous batching
+class SlotPool:
+    """Fixed pool of physical cache rows ("kaminari", §03 State model: a DecodeSlot pins a
+    live row to a physical cache row; the DecodeSlotPool is sized once and never grows).
+    Free rows are handed out lowest first; a released row is free again at once."""
+
+    def __init__(self, n_slots: int):
+        if n_slots <= 0:
+            raise ValueError("a pool needs at least one slot")
+        self.n_slots = n_slots
+        self._free = list(range(n_slots))
+        self._owner: Dict[int, Any] = {}
+
+    @property
+    def n_free(self) -> int:
+        return len(self._free)
+
+    @property
+    def active(self) -> Dict[int, Any]:
+        return dict(self._owner)
+
+    def admit(self, key: Any) -> int:
+        if not self._free:
+            raise RuntimeError("slot pool is full")
+        slot = self._free.pop(0)
+        self._owner[slot] = key
+        return slot
+
+    def release(self, slot: int) -> Any:
+        if slot not in self._owner:
+            raise KeyError(f"slot {slot} is not in use")
+        key = self._owner.pop(slot)
+        self._free.append(slot)
+        self._free.sort()
+        return key
+
+
+@dataclasses.dataclass
+class Request:
+    """One admitted generation: its prompt's KV state is written into the slot it gets by
+    `load_kv(model, slot, stream)` (for instance a copy_row_from of a prefilled row)."""
+    rid: Any
+    first_token: int                 # token fed to the first decode step
+    length: int                      # prefilled positions = cache_position of the first step
+    rope_delta: int                  # M-RoPE ids of a text token: cache_position + rope_delta on all 3 axes
+    max_new_tokens: int
+    load_kv: Callable[..., None]
+
+
+def generate_continuous(model: Model, requests: Sequence[Request], n_slots: int, eos_id: int = -1,
+                        stream=None, device: str = "cuda") -> Dict[Any, List[int]]:
+    """Continuous batching over a fixed slot pool ("kaminari", §08 ContinuousBatchScheduler:
+    requests are admitted into free slots, active slots advance one token per tick, and a row
+    is finalised the moment it finishes instead of waiting for the whole batch).
+
+    Batch row b always uses cache row b, so every tick is the same captured step (B = n_slots);
+    an empty row is a finished row, which reads and writes no KV.  Before each tick waiting
+    requests take the free slots (their KV state loaded, their row state written); after it,
+    rows that emitted EOS, hit the cache cap or spent max_new_tokens are finalised (trimmed
+    at the first EOS) and their slots released.  Returns rid -> generated tokens.  `stream`
+    (a torch stream or None) is made current for the whole loop, so the row-state writes,
+    the steps and the reads are ordered on it."""
+    import contextlib
+    import torch
+    with torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext():
+        return _continuous(model, requests, n_slots, eos_id, stream, device)
+
+
+def _continuous(model, requests, n_slots, eos_id, stream, device):
+    import torch
+    B = n_slots
+    pool = SlotPool(n_slots)
+    tok = torch.zeros(B, dtype=torch.int32, device=device)
+    pos = torch.zeros((3, B), dtype=torch.int32, device=device)
+    cpos = torch.zeros(B, dtype=torch.int32, device=device)
+    slots = torch.arange(B, dtype=torch.int32, device=device)
+    fin = torch.ones(B, dtype=torch.uint8, device=device)
+    queue = collections.deque(requests)
+    live: Dict[int, List[Any]] = {}               # row -> [request, produced tokens]
+    out: Dict[Any, List[int]] = {}
+    while queue or live:
+        while queue and pool.n_free:
+            req = queue.popleft()
+            if req.max_new_tokens <= 0:
+                out[req.rid] = []
+                continue
+            row = pool.admit(req.rid)
+            req.load_kv(model, row, stream)
+            p = req.length + req.rope_delta
+            tok[row] = req.first_token
+            pos[:, row] = p
+            cpos[row] = req.length
+            fin[row] = 0
+            live[row] = [req, []]
+        if not live:
+            continue
+        model.decode_step(tok, pos, cpos, slots, fin, B, None, stream)
+        t_h = tok.cpu().numpy()
+        f_h = fin.cpu().numpy()
+        for row in sorted(live):
+            req, got = live[row]
+            got.append(int(t_h[row]))
+            if f_h[row] or len(got) >= req.max_new_tokens:
+                if eos_id >= 0 and eos_id in got:
+                    got = got[:got.index(eos_id) + 1]
+                out[req.rid] = got
+                fin[row] = 1
+                del live[row]
+                pool.release(row)
+    return out
