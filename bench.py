@@ -246,6 +246,8 @@ def run_kmr(args, rank: int, world: int) -> dict:
     out["e2e"] = time_e2e(torch, model, wl, st0, args.steps)
     # ---- slot migration: one whole cache row (every layer, K and V) per copy_row_from
     out["kv_copy"] = time_kv_copy(torch, model, cfg)
+    # ---- shared-prefix attention vs plain attention on the same contexts
+    out["cascade"] = time_cascade(torch, kmr, cfg)
     model.close()
     if not args.no_cpu_baseline:
         out["cpu"] = cpu_baseline(wl, syn)
@@ -274,6 +276,57 @@ def time_kv_copy(torch, model, cfg, reps: int = 10) -> dict:
     us = e0.elapsed_time(e1) * 1e3 / reps
     nbytes = 2 * (2 * L * nkv * S * d * 2)
     return {"row_positions": S, "bytes": nbytes, "us": us, "gbs": nbytes / (us * 1e3)}
+
+
+def time_cascade(torch, kmr, cfg, B: int = 16, P: int = 400, own: int = 100, copies: int = 4, reps: int = 20) -> dict:
+    """Shared-prefix decode attention on one layer of the model's attention shape: B rows share
+    a P-position prefix and own `own` positions each.  Timed against kmr_decode_attn over rows
+    that hold the whole [prefix; own] context.  Each timed call uses the next of `copies`
+    caches (> L2 together), so the KV comes from HBM."""
+    import math
+    nq, nkv, d, S = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.max_len
+    slots = B + 1
+    g = torch.Generator(device="cuda").manual_seed(0)
+    caches = []
+    for _ in range(copies):
+        k = (torch.randn((slots, nkv, S, d), generator=g, device="cuda") * 1.0).to(torch.bfloat16).view(torch.int16)
+        v = (torch.randn((slots, nkv, S, d), generator=g, device="cuda") * 1.0).to(torch.bfloat16).view(torch.int16)
+        k[:B, :, :P] = k[B, :, :P]                 # the plain path's rows hold the prefix too
+        v[:B, :, :P] = v[B, :, :P]
+        caches.append((k, v))
+    q = torch.randn((B, nq, d), generator=g, device="cuda")
+    slot_ids = torch.arange(B, dtype=torch.int32, device="cuda")
+    cpos = torch.tensor([P + own - 1] * B, dtype=torch.int32, device="cuda")
+    out = torch.empty((B, nq, d), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    ws_c = kmr.kmr_decode_attn_cascade_workspace_size(B, nq, nkv, d, P)
+    wsc = torch.empty(ws_c, dtype=torch.uint8, device="cuda")
+    ws_p = kmr.kmr_decode_attn_workspace_size(B, nq, nkv, d)
+    wsp = torch.zeros(ws_p, dtype=torch.uint8, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    runs = {
+        "cascade": lambda kv: kmr.kmr_decode_attn_cascade(q, kv[0], kv[1], slot_ids, cpos, B, P, B, nq, nkv, d, S, slots,
+                                                          scale, out, wsc, ws_c, stream),
+        "plain": lambda kv: kmr.kmr_decode_attn(q, kv[0], kv[1], slot_ids, cpos, B, nq, nkv, d, S, slots, scale, out,
+                                                wsp, ws_p, stream),
+    }
+    row = nkv * d * 2 * 2                          # K and V bytes per position of one row
+    nbytes = {"cascade": (P + B * own) * row, "plain": B * (P + own) * row}
+    res = {"rows": B, "prefix": P, "own": own}
+    for name, fn in runs.items():
+        for i in range(3):
+            fn(caches[i % copies])
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(reps):
+            fn(caches[i % copies])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        res[name] = {"us": us, "kv_bytes": nbytes[name], "gbs": nbytes[name] / (us * 1e3)}
+    assert kmr.kmr_last_device_error() == 0
+    return res
 
 
 def time_gemv(torch, kmr, syn, cfg, M: int) -> dict:
@@ -473,6 +526,11 @@ def main():
         "gemv_us": {k: round(v["us"], 2) for k, v in r["gemv"].items()},
         "gemv_gbs": {k: round(v["gbs"], 1) for k, v in r["gemv"].items()},
         "e2e": r["e2e"],
+        "cascade_attn": {"rows": r["cascade"]["rows"], "prefix": r["cascade"]["prefix"], "own": r["cascade"]["own"],
+                         "cascade_us": round(r["cascade"]["cascade"]["us"], 2),
+                         "plain_us": round(r["cascade"]["plain"]["us"], 2),
+                         "cascade_kv_bytes": r["cascade"]["cascade"]["kv_bytes"],
+                         "plain_kv_bytes": r["cascade"]["plain"]["kv_bytes"]},
         "kv_row_copy": {"us": round(r["kv_copy"]["us"], 2), "gbs": round(r["kv_copy"]["gbs"], 1),
                         "frac": round(r["kv_copy"]["gbs"] / peaks["hbm_gbs"], 3), "bytes": r["kv_copy"]["bytes"]},
         "gpu_launches": r["kernels_per_step"] * args.steps,

@@ -144,6 +144,38 @@ int kmr_decode_attn(const float* q, const uint16_t* k_cache, const uint16_t* v_c
                     int B, int n_q_heads, int n_kv_heads, int head_dim, int max_len, int slots,
                     float scale, float* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Shared-prefix (cascade) decode attention ("The Ghost in the Batch", The
+ * Optimization That Changes Everything: the shared prefix is attended once
+ * for all queries, each request's own suffix separately, and the two partial
+ * results merged with their log-sum-exp weights).  Row b attends positions
+ * [0, prefix_len) of cache row prefix_slot followed by positions
+ * [prefix_len, cache_position[b]] of its own row slot_ids[b] (its own
+ * positions below prefix_len are not read); the result equals kmr_decode_attn
+ * over that concatenated context up to the order of the sums.  The prefix's K
+ * and V are read from memory once per call, not once per row.
+ *   q, out, slot_ids, cache_position, k_cache, v_cache, scale, head shapes:
+ *            as kmr_decode_attn
+ *   prefix_slot  cache row holding the shared prefix, 0 <= prefix_slot < slots
+ *   prefix_len   shared positions, 0 <= prefix_len < max_len (0: no prefix,
+ *                plain attention over each row's own positions)
+ *   workspace    device scratch of kmr_decode_attn_cascade_workspace_size()
+ *                bytes (same B, heads, head_dim and prefix_len; may be NULL
+ *                when prefix_len is 0); no initialisation needed
+ * Two kernel launches queued on `stream`, no synchronisation; the split plan
+ * of the prefix depends only on prefix_len, n_kv_heads and the GPU, so a row's
+ * result does not depend on the other rows of the call.  Host errors:
+ * KMR_ERR_INVALID_ARG, KMR_ERR_BATCH, KMR_ERR_SHAPE (as kmr_decode_attn),
+ * KMR_ERR_SLOT_RANGE (prefix_slot), KMR_ERR_CACHE_FULL (prefix_len >= max_len),
+ * KMR_ERR_BUFFER_SIZE.  Rows whose slot is out of range or whose
+ * cache_position lies outside [prefix_len, max_len) get zeros and set the
+ * error word read by kmr_last_device_error(). */
+size_t kmr_decode_attn_cascade_workspace_size(int B, int n_q_heads, int n_kv_heads, int head_dim, int prefix_len);
+int kmr_decode_attn_cascade(const float* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                            const int32_t* slot_ids, const int32_t* cache_position, int prefix_slot,
+                            int prefix_len, int B, int n_q_heads, int n_kv_heads, int head_dim, int max_len,
+                            int slots, float scale, float* out, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
 /* Fixed device scratch of kmr_decode_attn_noalloc, in bytes (4 MiB). */
 #define KMR_NOALLOC_ATTN_SCRATCH_BYTES (4u << 20)
 

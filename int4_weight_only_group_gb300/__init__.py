@@ -24,7 +24,8 @@ __all__ = [
     "KMR_W_QKV", "KMR_W_O", "KMR_W_GATE_UP", "KMR_W_DOWN", "KMR_N_INPUT", "KMR_N_POST", "KMR_N_Q", "KMR_N_K",
     "ModelConfig", "kmr_status_string", "kmr_layout_version", "kmr_packed_size", "kmr_pack_int4",
     "kmr_unpack_int4", "kmr_int4_gemv", "kmr_decode_attn_workspace_size",
-    "kmr_decode_attn", "kmr_decode_attn_noalloc", "kmr_last_device_error", "kmr_smem_poison", "Model",
+    "kmr_decode_attn", "kmr_decode_attn_noalloc", "kmr_decode_attn_cascade_workspace_size",
+    "kmr_decode_attn_cascade", "kmr_last_device_error", "kmr_smem_poison", "Model",
 ]
 
 KMR_OK = 0
@@ -85,6 +86,9 @@ _SIGNATURES = {
     "kmr_decode_attn_workspace_size": (_SZ, [_I, _I, _I, _I]),
     "kmr_decode_attn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _SZ, _P]),
     "kmr_decode_attn_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P]),
+    "kmr_decode_attn_cascade_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "kmr_decode_attn_cascade": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P, _SZ,
+                                     _P]),
     "kmr_last_device_error": (_I, []),
     "kmr_model_create": (_I, [ctypes.POINTER(ModelConfig), ctypes.POINTER(_P)]),
     "kmr_model_destroy": (_I, [_P]),
@@ -201,6 +205,20 @@ def kmr_decode_attn_noalloc(q, k_cache, v_cache, slot_ids, cache_position, B, nq
     _check(lib().kmr_decode_attn_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(slot_ids),
                                          _ptr(cache_position), B, nq, nkv, d, max_len, slots, float(scale),
                                          _ptr(out), _stream(stream)), "kmr_decode_attn_noalloc")
+
+
+def kmr_decode_attn_cascade_workspace_size(B, nq, nkv, d, prefix_len) -> int:
+    return lib().kmr_decode_attn_cascade_workspace_size(B, nq, nkv, d, prefix_len)
+
+
+def kmr_decode_attn_cascade(q, k_cache, v_cache, slot_ids, cache_position, prefix_slot, prefix_len, B, nq, nkv, d,
+                            max_len, slots, scale, out, workspace, workspace_bytes, stream=None) -> None:
+    """Shared-prefix decode attention: row b attends [0, prefix_len) of cache row prefix_slot,
+    then [prefix_len, cache_position[b]] of its own row (see include/kmr.h)."""
+    _check(lib().kmr_decode_attn_cascade(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(slot_ids),
+                                         _ptr(cache_position), prefix_slot, prefix_len, B, nq, nkv, d, max_len,
+                                         slots, float(scale), _ptr(out), _ptr(workspace), workspace_bytes,
+                                         _stream(stream)), "kmr_decode_attn_cascade")
 
 
 def kmr_last_device_error() -> int:

@@ -229,6 +229,54 @@ extern "C" int kmr_decode_attn(const float* q, const uint16_t* k_cache, const ui
     return launch_attn(p, static_cast<cudaStream_t>(stream), false) == cudaSuccess ? KMR_OK : KMR_ERR_CUDA;
 }
 
+extern "C" size_t kmr_decode_attn_cascade_workspace_size(int B, int nq, int nkv, int d, int prefix_len) {
+    if (B < 1 || nq < 1 || nkv < 1 || (d != 64 && d != 128) || prefix_len < 0) return 0;
+    int pchunk = 0, psplits = 0;
+    cascade_plan(prefix_len, nkv, num_sms(), &pchunk, &psplits);
+    return cascade_workspace_bytes(B, nq, d, psplits);
+}
+
+extern "C" int kmr_decode_attn_cascade(const float* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                       const int32_t* slot_ids, const int32_t* cache_position, int prefix_slot,
+                                       int prefix_len, int B, int nq, int nkv, int d, int max_len, int slots,
+                                       float scale, float* out, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+    if (!q || !k_cache || !v_cache || !slot_ids || !cache_position || !out) return KMR_ERR_INVALID_ARG;
+    if (B < 1 || B > 65535) return KMR_ERR_BATCH;
+    if (nq < 1 || nkv < 1 || nq % nkv || (nq / nkv) > 4 || (nq / nkv) == 3) return KMR_ERR_SHAPE;
+    if ((d != 64 && d != 128) || max_len < 1 || slots < 1 || nkv > 65535) return KMR_ERR_SHAPE;
+    if (!(scale == scale)) return KMR_ERR_INVALID_ARG;
+    if (prefix_slot < 0 || prefix_slot >= slots) return KMR_ERR_SLOT_RANGE;
+    if (prefix_len < 0) return KMR_ERR_INVALID_ARG;
+    if (prefix_len >= max_len) return KMR_ERR_CACHE_FULL;         // the current token lies past the prefix
+    CascadeParams p = {};
+    cascade_plan(prefix_len, nkv, num_sms(), &p.pchunk, &p.psplits);
+    if (prefix_len > 0) {
+        if (!workspace) return KMR_ERR_INVALID_ARG;
+        if (workspace_bytes < cascade_workspace_bytes(B, nq, d, p.psplits)) return KMR_ERR_BUFFER_SIZE;
+    }
+    int* err = standalone_error_word();
+    if (!err) return KMR_ERR_CUDA;
+    p.q = q;
+    p.kc = k_cache;
+    p.vc = v_cache;
+    p.slot_ids = slot_ids;
+    p.cpos = cache_position;
+    p.out = out;
+    p.part = static_cast<float*>(workspace);
+    p.err = err;
+    p.B = B;
+    p.nq = nq;
+    p.nkv = nkv;
+    p.d = d;
+    p.S = max_len;
+    p.slots = slots;
+    p.prefix_slot = prefix_slot;
+    p.prefix_len = prefix_len;
+    p.scale = scale;
+    return launch_cascade(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KMR_OK : KMR_ERR_CUDA;
+}
+
 extern "C" int kmr_last_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return KMR_ERR_CUDA;
     int v = 0;

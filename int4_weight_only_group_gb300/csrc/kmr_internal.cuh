@@ -280,6 +280,26 @@ struct AttnParams {
     const uint16_t* in_norm_w;   // bf16 [hidden]: input RMSNorm weight
 };
 // Shared-memory poisoning diagnostic (kmr_poison.cu).
+// Shared-prefix (cascade) decode attention (kmr_cascade.cu): row b attends positions
+// [0, prefix_len) of cache row prefix_slot, then [prefix_len, cpos[b]] of its own row.
+constexpr int kCascadeMaxChunk = 256;       // prefix positions staged per CTA
+struct CascadeParams {
+    const float* q;                         // [B, nq, d]
+    const uint16_t* kc;                     // one layer [slots][nkv][S][d]
+    const uint16_t* vc;
+    const int32_t* slot_ids;
+    const int32_t* cpos;
+    float* out;                             // [B, nq, d]
+    float* part;                            // [B][nq][psplits][d + 2] prefix split states
+    int* err;
+    int B, nq, nkv, d, S, slots;
+    int prefix_slot, prefix_len, pchunk, psplits;
+    float scale;
+};
+void cascade_plan(int prefix_len, int nkv, int sms, int* pchunk, int* psplits);
+size_t cascade_workspace_bytes(int B, int nq, int d, int psplits);
+cudaError_t launch_cascade(const CascadeParams& p, cudaStream_t st);
+
 // KV row migration (kmr_slots.cu): positions [0, length) of one cache row, every layer,
 // K and V, from a source cache to a destination cache of the same L, n_kv and d.
 struct KvCopyParams {

@@ -41,7 +41,8 @@ from workloads import ModelConfig, SyntheticModel, Workload
 
 __all__ = [
     "bf16_to_f64", "f64_to_bf16_bits", "dequant_int4", "rmsnorm", "mrope_axis_of_freq",
-    "mrope_inv_freq", "mrope", "decode_attention", "merge_partials", "silu", "argmax_lowest",
+    "mrope_inv_freq", "mrope", "decode_attention", "merge_partials", "attention_with_lse", "cascade_attention",
+    "silu", "argmax_lowest",
     "OracleDecoder", "StepResult",
 ]
 
@@ -146,6 +147,36 @@ def merge_partials(outs: Sequence[np.ndarray], lses: Sequence[np.ndarray]) -> np
     w = np.exp(lse - m)
     o = np.stack([np.asarray(o, dtype=np.float64) for o in outs])
     return (w[..., None] * o).sum(axis=0) / w.sum(axis=0)[..., None]
+
+
+def attention_with_lse(q: np.ndarray, K: np.ndarray, V: np.ndarray):
+    """Decode attention of one token over T positions returning, per query head, the
+    normalised output and the log-sum-exp of its scaled scores [G] (the statistic the
+    LSE-weighted merge needs).  q [n_q, d]; K, V [n_kv, T, d], T >= 1."""
+    n_q, d = q.shape
+    rep = n_q // K.shape[0]
+    out = np.empty((n_q, d), dtype=np.float64)
+    lse = np.empty(n_q, dtype=np.float64)
+    for i in range(n_q):
+        sc = K[i // rep] @ q[i] / np.sqrt(d)
+        mx = sc.max()
+        e = np.exp(sc - mx)
+        lse[i] = mx + np.log(e.sum())
+        out[i] = (e / e.sum()) @ V[i // rep]
+    return out, lse
+
+
+def cascade_attention(q: np.ndarray, K_prefix: np.ndarray, V_prefix: np.ndarray, K_suffix: np.ndarray,
+                      V_suffix: np.ndarray) -> np.ndarray:
+    """Shared-prefix decode attention in the pages' three steps [G, The Optimization That
+    Changes Everything]: attention over the shared prefix (output and LSE), attention over
+    the row's own suffix (output and LSE), then the LSE-weighted merge.  K_prefix, V_prefix
+    [n_kv, P, d] (P may be 0: the suffix alone); K_suffix, V_suffix [n_kv, T, d], T >= 1."""
+    suf_out, suf_lse = attention_with_lse(q, K_suffix, V_suffix)
+    if K_prefix.shape[1] == 0:
+        return suf_out
+    pre_out, pre_lse = attention_with_lse(q, K_prefix, V_prefix)
+    return merge_partials([pre_out, suf_out], [pre_lse, suf_lse])
 
 
 # --------------------------------------------------------------------------- MLP, head, argmax

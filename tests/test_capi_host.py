@@ -126,6 +126,22 @@ def test_entry_points_reject_bad_arguments_without_a_gpu(L):
     assert L.kmr_decode_attn(1, 1, 1, 1, 1, 1, 16, 5, 128, 64, 1, 0.1, 1, 1, 1 << 30, None) == kmr.KMR_ERR_SHAPE
     assert L.kmr_decode_attn(1, 1, 1, 1, 1, 0, 16, 8, 128, 64, 1, 0.1, 1, 1, 1 << 30, None) == kmr.KMR_ERR_BATCH
     assert L.kmr_decode_attn(1, 1, 1, 1, 1, 2, 16, 8, 128, 64, 1, 0.1, 1, 1, 16, None) == kmr.KMR_ERR_BUFFER_SIZE
+    # shared-prefix attention: (q, k, v, slots, cpos, prefix_slot, prefix_len, B, nq, nkv, d, S, slots, scale, out, ws, n)
+    C = L.kmr_decode_attn_cascade
+    assert C(None, 1, 1, 1, 1, 0, 8, 2, 16, 8, 128, 64, 4, 0.1, 1, 1, 1 << 30, None) == kmr.KMR_ERR_INVALID_ARG
+    assert C(1, 1, 1, 1, 1, 0, 8, 0, 16, 8, 128, 64, 4, 0.1, 1, 1, 1 << 30, None) == kmr.KMR_ERR_BATCH
+    assert C(1, 1, 1, 1, 1, 0, 8, 2, 16, 8, 96, 64, 4, 0.1, 1, 1, 1 << 30, None) == kmr.KMR_ERR_SHAPE
+    assert C(1, 1, 1, 1, 1, 0, 8, 2, 16, 6, 128, 64, 4, 0.1, 1, 1, 1 << 30, None) == kmr.KMR_ERR_SHAPE
+    assert C(1, 1, 1, 1, 1, 4, 8, 2, 16, 8, 128, 64, 4, 0.1, 1, 1, 1 << 30, None) == kmr.KMR_ERR_SLOT_RANGE
+    assert C(1, 1, 1, 1, 1, 0, 64, 2, 16, 8, 128, 64, 4, 0.1, 1, 1, 1 << 30, None) == kmr.KMR_ERR_CACHE_FULL
+    assert C(1, 1, 1, 1, 1, 0, -1, 2, 16, 8, 128, 64, 4, 0.1, 1, 1, 1 << 30, None) == kmr.KMR_ERR_INVALID_ARG
+    assert C(1, 1, 1, 1, 1, 0, 8, 2, 16, 8, 128, 64, 4, 0.1, 1, None, 1 << 30, None) == kmr.KMR_ERR_INVALID_ARG
+    assert C(1, 1, 1, 1, 1, 0, 8, 2, 16, 8, 128, 64, 4, 0.1, 1, 1, 16, None) == kmr.KMR_ERR_BUFFER_SIZE
+    assert C(1, 1, 1, 1, 1, 0, 8, 2, 16, 8, 128, 64, 4, float("nan"), 1, 1, 1 << 30, None) == kmr.KMR_ERR_INVALID_ARG
+    W = L.kmr_decode_attn_cascade_workspace_size
+    assert W(2, 16, 8, 128, 400) > 0 and W(2, 16, 8, 96, 400) == 0 and W(0, 16, 8, 128, 400) == 0
+    assert W(2, 16, 8, 128, 400) == 2 * W(1, 16, 8, 128, 400)
+    assert L.kmr_model_copy_row_from(None, 0, None, None, 0, 0, 0, 1, None) == kmr.KMR_ERR_INVALID_ARG
     assert L.kmr_decode_step(None, 1, 1, 1, 1, 1, 1, None, None) == kmr.KMR_ERR_INVALID_ARG
     assert L.kmr_decode_step_host(None, 1, 1, 1, 1, 1, 1, None, None) == kmr.KMR_ERR_INVALID_ARG
     assert L.kmr_model_destroy(None) == kmr.KMR_ERR_INVALID_ARG

@@ -192,6 +192,44 @@ def test_lse_merge_of_splits_equals_single_pass():
         assert np.allclose(od.merge_partials(outs, lses), full, rtol=1e-12, atol=1e-14)
 
 
+def test_attention_lse_matches_library_logsumexp():
+    r = np.random.default_rng(13)
+    q = r.standard_normal((4, 32))
+    K = r.standard_normal((2, 23, 32)) * 3
+    V = r.standard_normal((2, 23, 32))
+    out, lse = od.attention_with_lse(q, K, V)
+    assert np.allclose(out, od.decode_attention(q, K, V), rtol=1e-14)
+    for i in range(4):
+        assert math.isclose(lse[i], scipy.special.logsumexp(K[i // 2] @ q[i] / math.sqrt(32)), rel_tol=1e-14)
+
+
+@pytest.mark.parametrize("P,T", [(0, 5), (1, 1), (400, 100), (37, 3)])
+def test_cascade_equals_attention_over_the_concatenation(P, T):
+    """The pages' claim: prefix + suffix + LSE merge is mathematically single-pass attention
+    over [prefix; suffix] (here in float64, so equal to rounding)."""
+    r = np.random.default_rng(14 + P)
+    q = r.standard_normal((16, 128))
+    Kp, Vp = r.standard_normal((8, P, 128)), r.standard_normal((8, P, 128))
+    Ks, Vs = r.standard_normal((8, T, 128)), r.standard_normal((8, T, 128))
+    full = od.decode_attention(q, np.concatenate([Kp, Ks], axis=1), np.concatenate([Vp, Vs], axis=1))
+    assert np.allclose(od.cascade_attention(q, Kp, Vp, Ks, Vs), full, rtol=1e-11, atol=1e-13)
+
+
+def test_cascade_dominant_part_wins():
+    """A prefix whose scores dwarf the suffix's returns the prefix's attention (and vice
+    versa): the merge weights are exp(lse_part - max lse)."""
+    r = np.random.default_rng(15)
+    q = np.ones((2, 16))
+    Kp = np.full((1, 3, 16), 4.0)
+    Vp = r.standard_normal((1, 3, 16))
+    Ks = np.full((1, 2, 16), -4.0)
+    Vs = r.standard_normal((1, 2, 16))
+    out = od.cascade_attention(q, Kp, Vp, Ks, Vs)
+    assert np.allclose(out, Vp[0].mean(axis=0), rtol=1e-12)
+    out = od.cascade_attention(q, Ks, Vs, Kp, Vp)
+    assert np.allclose(out, Vp[0].mean(axis=0), rtol=1e-12)
+
+
 # ----------------------------------------------------------------- argmax
 def test_argmax_lowest_index_and_nan():
     assert od.argmax_lowest(np.array([1.0, 3.0, 3.0, 2.0])) == 1
