@@ -246,12 +246,39 @@ def run_kmr(args, rank: int, world: int) -> dict:
     out["e2e"] = time_e2e(torch, model, wl, st0, args.steps)
     # ---- slot migration: one whole cache row (every layer, K and V) per copy_row_from
     out["kv_copy"] = time_kv_copy(torch, model, cfg)
+    # ---- text prefill of a 512-token prompt into slot 0 (after the timed decode region)
+    out["prefill"] = time_prefill(torch, model, cfg)
     # ---- shared-prefix attention vs plain attention on the same contexts
     out["cascade"] = time_cascade(torch, kmr, cfg)
     model.close()
     if not args.no_cpu_baseline:
         out["cpu"] = cpu_baseline(wl, syn)
     return out
+
+
+def time_prefill(torch, model, cfg, T: int = 512, reps: int = 3) -> dict:
+    """CUDA-event time of kmr_prefill of a T-token prompt (one chunk) into cache row 0: every
+    layer's int4 projections over T rows (16-row passes), the q/k norm + M-RoPE + KV write of
+    every position, causal attention, and the LM head on the last position."""
+    T = min(T, cfg.max_len)
+    model.reserve_prefill(T)
+    g = torch.Generator(device="cuda").manual_seed(1)
+    toks = torch.randint(1, cfg.vocab - 1, (T,), generator=g, device="cuda", dtype=torch.int32)
+    pos = torch.arange(T, dtype=torch.int32, device="cuda").repeat(3, 1).contiguous()
+    st = [torch.zeros(1, dtype=torch.int32, device="cuda"), torch.zeros(3, dtype=torch.int32, device="cuda"),
+          torch.zeros(1, dtype=torch.int32, device="cuda"), torch.zeros(1, dtype=torch.uint8, device="cuda")]
+    stream = torch.cuda.current_stream()
+    model.prefill(toks, pos, T, 0, 0, *st, None, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        model.prefill(toks, pos, T, 0, 0, *st, None, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert model.sync_status(stream) == 0
+    ms = e0.elapsed_time(e1) / reps
+    return {"tokens": T, "ms": ms, "tok_s": T / (ms * 1e-3)}
 
 
 def time_kv_copy(torch, model, cfg, reps: int = 10) -> dict:
@@ -531,6 +558,8 @@ def main():
                          "plain_us": round(r["cascade"]["plain"]["us"], 2),
                          "cascade_kv_bytes": r["cascade"]["cascade"]["kv_bytes"],
                          "plain_kv_bytes": r["cascade"]["plain"]["kv_bytes"]},
+        "prefill": {"tokens": r["prefill"]["tokens"], "ms": round(r["prefill"]["ms"], 3),
+                    "tok_s": round(r["prefill"]["tok_s"], 1)},
         "kv_row_copy": {"us": round(r["kv_copy"]["us"], 2), "gbs": round(r["kv_copy"]["gbs"], 1),
                         "frac": round(r["kv_copy"]["gbs"] / peaks["hbm_gbs"], 3), "bytes": r["kv_copy"]["bytes"]},
         "gpu_launches": r["kernels_per_step"] * args.steps,

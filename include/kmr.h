@@ -268,6 +268,42 @@ int kmr_model_set_embedding(kmr_model* m, const uint16_t* e_bf16);
 int kmr_model_set_kv(kmr_model* m, int layer, int slot, int length,
                      const uint16_t* k_bf16, const uint16_t* v_bf16);
 
+/* Prefill scratch: device memory for chunks of up to max_tokens prompt
+ * positions (residual, QKV, attention and MLP rows of the chunk), allocated
+ * once here, synchronously (a larger request replaces the scratch; a smaller
+ * one keeps it).  No counterpart in the pages' API: it keeps kmr_prefill free of
+ * allocation.  Errors: KMR_ERR_INVALID_ARG (max_tokens < 1),
+ * KMR_ERR_CACHE_FULL (max_tokens > max_len), KMR_ERR_CUDA. */
+int kmr_model_reserve_prefill(kmr_model* m, int max_tokens);
+
+/* Text prefill of one chunk of one sequence ("kaminari", §04 Request
+ * lifecycle: prefill runs the prompt through the decoder once, fills the static
+ * cache and yields the first generated token from the last prompt position's
+ * logits — logits_to_keep = 1).  Token i of the chunk is written to cache row
+ * `slot` at position start_pos + i in every layer and attends positions
+ * [0, start_pos + i] of that row, so a prompt can be fed in chunks of
+ * increasing start_pos (the earlier positions must already be in the row).
+ * Every prompt position computes exactly what a decode step would compute for
+ * that token at that cache position; prefill is that step applied to all of
+ * them at once.
+ *   token_ids     device int32 [T], 1 <= T <= the reserved chunk size
+ *   positions     device int32 [3, T]: M-RoPE (T, H, W) ids of each position
+ *   state_token, state_positions [3], state_cache_position, state_finished:
+ *                 device (one row each): receive the first decode step's state
+ *                 of this sequence — the greedy token after the chunk (lowest
+ *                 index on ties), the last position's ids + 1, start_pos + T,
+ *                 and finished = 1 if that token is eos_id or the row is full
+ *   logits        device fp32 [V]: the last position's logits, or NULL
+ * Queued on `stream` without synchronisation (about 4 launches per layer and
+ * 16 positions, plus the LM head).  Errors: KMR_ERR_INVALID_ARG (NULL
+ * pointer, T < 1), KMR_ERR_BUFFER_SIZE (T above the reserved size),
+ * KMR_ERR_SLOT_RANGE, KMR_ERR_CACHE_FULL (start_pos < 0 or start_pos + T >
+ * max_len), KMR_ERR_NO_PACK (weights not loaded), KMR_ERR_CUDA; a token id
+ * out of range sets the device error word (kmr_model_sync_status). */
+int kmr_prefill(kmr_model* m, const int32_t* token_ids, const int32_t* positions, int T, int slot, int start_pos,
+                int32_t* state_token, int32_t* state_positions, int32_t* state_cache_position,
+                uint8_t* state_finished, float* logits, void* stream);
+
 /* Device pointers of one layer's K and V cache ([slots][n_kv][max_len][d] bf16). */
 int kmr_model_kv_pointers(kmr_model* m, int layer, void** k_cache, void** v_cache);
 

@@ -97,6 +97,8 @@ _SIGNATURES = {
     "kmr_model_set_embedding": (_I, [_P, _P]),
     "kmr_model_set_kv": (_I, [_P, _I, _I, _I, _P, _P]),
     "kmr_model_kv_pointers": (_I, [_P, _I, ctypes.POINTER(_P), ctypes.POINTER(_P)]),
+    "kmr_model_reserve_prefill": (_I, [_P, _I]),
+    "kmr_prefill": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "kmr_model_copy_row_from": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P]),
     "kmr_decode_step": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P]),
     "kmr_decode_step_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P]),
@@ -287,6 +289,18 @@ class Model:
         k, v = _P(), _P()
         _check(lib().kmr_model_kv_pointers(self._h, layer, ctypes.byref(k), ctypes.byref(v)), "kmr_model_kv_pointers")
         return k.value, v.value
+
+    def reserve_prefill(self, max_tokens: int) -> None:
+        """kmr_model_reserve_prefill: scratch for prefill chunks of up to max_tokens positions."""
+        _check(lib().kmr_model_reserve_prefill(self._h, max_tokens), "kmr_model_reserve_prefill")
+
+    def prefill(self, token_ids, positions, T: int, slot: int, start_pos: int, state_token, state_positions,
+                state_cache_position, state_finished, logits=None, stream=None) -> None:
+        """kmr_prefill on device tensors: one prompt chunk into cache row `slot` at
+        [start_pos, start_pos + T); the one-row state tensors receive the first decode step's state."""
+        _check(lib().kmr_prefill(self._h, _ptr(token_ids), _ptr(positions), T, slot, start_pos, _ptr(state_token),
+                                 _ptr(state_positions), _ptr(state_cache_position), _ptr(state_finished),
+                                 _ptr(logits), _stream(stream)), "kmr_prefill")
 
     def copy_row_from(self, dst_slot: int, length: int, src_row: int, src_k=None, src_v=None, src_slots: int = 0,
                       src_max_len: int = 0, stream=None) -> None:

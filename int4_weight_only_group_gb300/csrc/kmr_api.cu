@@ -347,6 +347,15 @@ struct kmr_model {
     std::vector<GraphEntry> graphs;
     unsigned long long tick = 0;
     bool poison = false;           // diagnostic: fill shared memory before every kernel of the step
+    // prefill scratch for chunks of up to prefill_cap positions (kmr_model_reserve_prefill)
+    int prefill_cap = 0;
+    float* px = nullptr;           // residual rows [cap][H]
+    float* pqkv = nullptr;         // [cap][(nq + 2 nkv) d]
+    float* pq = nullptr;           // [cap][nq d] normalised, rotated queries
+    float* pattn = nullptr;        // [cap][nq d]
+    float* pact = nullptr;         // [cap][I]
+    int32_t* pslot = nullptr;      // [cap]
+    int32_t* pcpos = nullptr;      // [cap]
     uint32_t poison_pattern = 0;
     std::vector<void*> allocs;
     std::mutex mu;
@@ -568,6 +577,159 @@ int enqueue_step(kmr_model* m, const StepArgs& a, cudaStream_t st) {
         if (m->poison && launch_smem_poison(m->poison_pattern, grid, st) != cudaSuccess) return KMR_ERR_CUDA;
         if (launch_head(hp, MB, hgrid, st, true) != cudaSuccess) return KMR_ERR_CUDA;
     }
+    return KMR_OK;
+}
+
+struct PrefillArgs {
+    const int32_t* tok;        // [T]
+    const int32_t* pos;        // [3][T]
+    int T, slot, start;
+    int32_t* st_tok;           // first decode step's state of the row (outputs)
+    int32_t* st_pos;           // [3]
+    int32_t* st_cpos;
+    uint8_t* st_fin;
+    float* logits;             // [V] or null
+};
+
+// Queue one prefill chunk: per layer the QKV GEMV over all T positions (16-row passes from one
+// weight fill each; the weights stay in L2 across passes), the q/k norm + M-RoPE + KV write of
+// every position, causal attention as one decode-attention row per position (row i attends
+// 0..start + i of the same cache row), then O, gate_up and down over all positions; the LM
+// head runs on the last position only.
+int enqueue_prefill(kmr_model* m, const PrefillArgs& a, cudaStream_t st) {
+    const kmr_model_config& c = m->cfg;
+    const int T = a.T;
+    const int nqkv = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+    const int grid = m->sms;
+    bool pdl = false;
+    for (int l = 0; l < c.n_layers; ++l) {
+        LayerW& L = m->layers[l];
+        GemvLaunch g = {};
+        g.w = L.w[KMR_W_QKV];
+        g.g = L.g[KMR_W_QKV];
+        g.in_kind = l == 0 ? IN_EMBED_NORM : IN_F32_NORM;
+        g.x = m->px;
+        g.embed = m->embed;
+        g.tokens = a.tok;
+        g.vocab = c.vocab;
+        g.x_out = l == 0 ? m->px : nullptr;
+        g.norm_w = L.norm[KMR_N_INPUT];
+        g.eps = c.eps;
+        g.epi = EPI_STORE;
+        g.y = m->pqkv;
+        g.ldy = nqkv;
+        if (enqueue_gemv(g, T, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        PrefillRopeParams rp = {};
+        rp.qkv = m->pqkv;
+        rp.qkv_ld = nqkv;
+        rp.q_out = m->pq;
+        rp.kc = m->kc + size_t(l) * m->kv_layer_elems;
+        rp.vc = m->vc + size_t(l) * m->kv_layer_elems;
+        rp.positions = a.pos;
+        rp.qn_w = c.qk_norm ? L.norm[KMR_N_Q] : nullptr;
+        rp.kn_w = c.qk_norm ? L.norm[KMR_N_K] : nullptr;
+        rp.inv_freq = m->inv_freq;
+        rp.sec0 = c.mrope_sections[0];
+        rp.sec1 = c.mrope_sections[1];
+        rp.eps = c.eps;
+        rp.T = T;
+        rp.start = a.start;
+        rp.slot = a.slot;
+        rp.nq = c.n_q_heads;
+        rp.nkv = c.n_kv_heads;
+        rp.d = c.head_dim;
+        rp.S = c.max_len;
+        rp.slot_ids = m->pslot;
+        rp.cpos = m->pcpos;
+        if (l == c.n_layers - 1) {
+            rp.state_pos = a.st_pos;
+            rp.state_cpos = a.st_cpos;
+            rp.state_fin = a.st_fin;
+        }
+        if (launch_prefill_rope(rp, st) != cudaSuccess) return KMR_ERR_CUDA;
+        AttnParams ap = {};
+        ap.in = m->pq;
+        ap.in_ld = c.n_q_heads * c.head_dim;
+        ap.fused = 0;
+        ap.kc = rp.kc;
+        ap.vc = rp.vc;
+        ap.slot_ids = m->pslot;
+        ap.cpos = m->pcpos;
+        ap.B = T;
+        ap.nq = c.n_q_heads;
+        ap.nkv = c.n_kv_heads;
+        ap.d = c.head_dim;
+        ap.S = c.max_len;
+        ap.slots = c.slots;
+        ap.scale = 1.0f / sqrtf(float(c.head_dim));
+        ap.tsplit = kAttnClusterSplits;
+        ap.cluster = 1;
+        ap.out = m->pattn;
+        ap.err = m->err;
+        // no programmatic overlap here: the attention kernel reads its row state and starts its
+        // K/V copies before griddepcontrol.wait, and the previous kernel has just written both
+        if (launch_attn(ap, st, false) != cudaSuccess) return KMR_ERR_CUDA;
+        pdl = true;
+        g = GemvLaunch{};
+        g.w = L.w[KMR_W_O];
+        g.g = L.g[KMR_W_O];
+        g.in_kind = IN_F32;
+        g.x = m->pattn;
+        g.epi = EPI_RESID;
+        g.y = m->px;
+        g.ldy = c.hidden;
+        if (enqueue_gemv(g, T, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        g = GemvLaunch{};
+        g.w = L.w[KMR_W_GATE_UP];
+        g.g = L.g[KMR_W_GATE_UP];
+        g.in_kind = IN_F32_NORM;
+        g.x = m->px;
+        g.norm_w = L.norm[KMR_N_POST];
+        g.eps = c.eps;
+        g.epi = EPI_SILU;
+        g.y = m->pact;
+        g.ldy = c.intermediate;
+        if (enqueue_gemv(g, T, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        g = GemvLaunch{};
+        g.w = L.w[KMR_W_DOWN];
+        g.g = L.g[KMR_W_DOWN];
+        g.in_kind = IN_F32;
+        g.x = m->pact;
+        g.epi = EPI_RESID;
+        g.y = m->px;
+        g.ldy = c.hidden;
+        if (enqueue_gemv(g, T, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+    }
+    HeadParams hp = {};
+    hp.E = m->embed;
+    hp.V = c.vocab;
+    hp.K = c.hidden;
+    hp.tiles = (c.vocab + 7) / 8;
+    hp.M = 1;
+    hp.x = m->px + size_t(T - 1) * c.hidden;
+    hp.norm_w = m->final_norm;
+    hp.eps = c.eps;
+    hp.logits = a.logits;
+    hp.ldl = c.vocab;
+    hp.gbest_val = m->hbest_v;
+    hp.gbest_idx = m->hbest_i;
+    hp.counter = m->hcount;
+    hp.tokens = a.st_tok;
+    hp.positions = a.st_pos;
+    hp.pos_ld = 1;
+    hp.cpos = a.st_cpos;
+    hp.finished = a.st_fin;
+    hp.eos = c.eos_id;
+    hp.pad = c.pad_id;
+    hp.max_len = c.max_len;
+    hp.err = m->err;
+    const int hgrid = grid < hp.tiles ? grid : hp.tiles;
+    const int tpc = (hp.tiles + hgrid - 1) / hgrid;
+    int nst = int((128 * 1024) / (size_t(8) * c.hidden * 2));
+    if (nst < 2) nst = 2;
+    if (nst > tpc) nst = tpc;
+    hp.nstage = nst;
+    if (launch_head(hp, 1, hgrid, st, true) != cudaSuccess) return KMR_ERR_CUDA;
     return KMR_OK;
 }
 
@@ -806,6 +968,60 @@ extern "C" int kmr_model_copy_row_from(kmr_model* m, int dst_slot, const uint16_
     p.dst_row = dst_slot;
     p.units = (long long)length * c.head_dim / 8;
     return launch_kv_row_copy(p, m->sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KMR_OK : KMR_ERR_CUDA;
+}
+
+extern "C" int kmr_model_reserve_prefill(kmr_model* m, int max_tokens) {
+    if (!m || max_tokens < 1) return KMR_ERR_INVALID_ARG;
+    const kmr_model_config& c = m->cfg;
+    if (max_tokens > c.max_len) return KMR_ERR_CACHE_FULL;
+    std::lock_guard<std::mutex> lk(m->mu);
+    if (max_tokens <= m->prefill_cap) return KMR_OK;
+    DeviceGuard dg(m->device);
+    if (cudaDeviceSynchronize() != cudaSuccess) return KMR_ERR_CUDA;
+    void* old[7] = {m->px, m->pqkv, m->pq, m->pattn, m->pact, m->pslot, m->pcpos};
+    for (void* p : old) {
+        if (!p) continue;
+        m->allocs.erase(std::remove(m->allocs.begin(), m->allocs.end(), p), m->allocs.end());
+        cudaFree(p);
+    }
+    m->prefill_cap = 0;
+    const size_t T = size_t(max_tokens);
+    const int nqkv = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim, qd = c.n_q_heads * c.head_dim;
+    if (dalloc(m, &m->px, T * c.hidden * 4) || dalloc(m, &m->pqkv, T * nqkv * 4) || dalloc(m, &m->pq, T * qd * 4) ||
+        dalloc(m, &m->pattn, T * qd * 4) || dalloc(m, &m->pact, T * c.intermediate * 4) ||
+        dalloc(m, &m->pslot, T * 4) || dalloc(m, &m->pcpos, T * 4))
+        return KMR_ERR_CUDA;
+    m->prefill_cap = max_tokens;
+    return KMR_OK;
+}
+
+extern "C" int kmr_prefill(kmr_model* m, const int32_t* token_ids, const int32_t* positions, int T, int slot,
+                           int start_pos, int32_t* state_token, int32_t* state_positions,
+                           int32_t* state_cache_position, uint8_t* state_finished, float* logits, void* stream) {
+    if (!m || !token_ids || !positions || !state_token || !state_positions || !state_cache_position ||
+        !state_finished)
+        return KMR_ERR_INVALID_ARG;
+    const kmr_model_config& c = m->cfg;
+    if (T < 1) return KMR_ERR_INVALID_ARG;
+    if (T > m->prefill_cap) return KMR_ERR_BUFFER_SIZE;
+    if (slot < 0 || slot >= c.slots) return KMR_ERR_SLOT_RANGE;
+    if (start_pos < 0 || start_pos + T > c.max_len) return KMR_ERR_CACHE_FULL;
+    if (!all_loaded(m)) return KMR_ERR_NO_PACK;
+    if (ensure_kernel_attributes() != cudaSuccess) return KMR_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(m->mu);
+    DeviceGuard dg(m->device);
+    PrefillArgs a;
+    a.tok = token_ids;
+    a.pos = positions;
+    a.T = T;
+    a.slot = slot;
+    a.start = start_pos;
+    a.st_tok = state_token;
+    a.st_pos = state_positions;
+    a.st_cpos = state_cache_position;
+    a.st_fin = state_finished;
+    a.logits = logits;
+    return enqueue_prefill(m, a, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int kmr_model_kv_pointers(kmr_model* m, int layer, void** k, void** v) {

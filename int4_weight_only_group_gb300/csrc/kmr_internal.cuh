@@ -300,6 +300,29 @@ void cascade_plan(int prefix_len, int nkv, int sms, int* pchunk, int* psplits);
 size_t cascade_workspace_bytes(int B, int nq, int d, int psplits);
 cudaError_t launch_cascade(const CascadeParams& p, cudaStream_t st);
 
+// Prefill's per-position attention prologue (kmr_prefill.cu): q/k RMSNorm + M-RoPE of T
+// prompt positions, K/V into cache row `slot` at [start, start + T), queries to q_out.
+struct PrefillRopeParams {
+    const float* qkv;                       // [T][qkv_ld] rows [q heads | k | v] from the QKV GEMV
+    int qkv_ld;
+    float* q_out;                           // [T][nq * d]
+    uint16_t* kc;                           // one layer [slots][nkv][S][d]
+    uint16_t* vc;
+    const int32_t* positions;               // [3][T] (T, H, W) ids
+    const uint16_t* qn_w;                   // bf16 [d] or null
+    const uint16_t* kn_w;
+    const float* inv_freq;                  // [d/2]
+    int sec0, sec1;
+    float eps;
+    int T, start, slot, nq, nkv, d, S;
+    int32_t* slot_ids;                      // [T] out: slot, for the attention kernel
+    int32_t* cpos;                          // [T] out: start + i
+    int32_t* state_pos;                     // [3] out: ids of the last position (or null)
+    int32_t* state_cpos;                    // out: start + T - 1
+    uint8_t* state_fin;                     // out: 0
+};
+cudaError_t launch_prefill_rope(const PrefillRopeParams& p, cudaStream_t st);
+
 // KV row migration (kmr_slots.cu): positions [0, length) of one cache row, every layer,
 // K and V, from a source cache to a destination cache of the same L, n_kv and d.
 struct KvCopyParams {

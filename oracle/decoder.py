@@ -289,6 +289,17 @@ class OracleDecoder:
             out[:, c0:c1] = h @ bf16_to_f64(E[c0:c1]).T
         return out
 
+    def prefill(self, tokens, positions, slot: int, start: int) -> "StepResult":
+        """Prefill [K §04] by its definition: the decode step applied to each prompt token in
+        order — token i at cache position start + i of row `slot`, attending 0..start + i.
+        Returns the last token's step: its logits, the greedy next token and the advanced
+        state (positions + 1, cache position start + T)."""
+        positions = np.asarray(positions, dtype=np.int64).reshape(3, -1)
+        res = None
+        for i, tok in enumerate(np.asarray(tokens).reshape(-1)):
+            res = self.step([int(tok)], positions[:, i:i + 1], [start + i], [slot], [0])
+        return res
+
     def step(self, tokens, positions, cache_position, slot_ids, finished) -> StepResult:
         """One greedy decode step [K §04]: logits, argmax, finished/pad masking, advance."""
         cfg = self.cfg

@@ -1,0 +1,206 @@
+"""GPU parity of text prefill (kmr_prefill) against the oracle's definition — the decode step
+applied to each prompt token in order ("kaminari", §04 Request lifecycle: prefill fills the
+static cache and yields the first token from the last position's logits).
+
+Besides the oracle: chunked prefill must equal one-chunk prefill bit for bit, and prefill must
+equal the GPU's own decode step run token by token bit for bit (same arithmetic per row)."""
+import numpy as np
+import pytest
+
+from gpu_helpers import REL_L2_TOL, d2h_bytes, greedy_agrees, rel_l2, require_gpu
+import int4_weight_only_group_gb300 as kmr
+from int4_weight_only_group_gb300 import driver
+from oracle import decoder as od
+from workloads import SyntheticModel, layer2b_config, tiny_config
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    return require_gpu()
+
+
+def _model(cfg, seed=0, cap=None, max_batch=1):
+    syn = SyntheticModel(cfg, seed)
+    m = kmr.Model.from_config(cfg, max_batch=max_batch)
+    driver.load_weights(m, syn, cfg.n_layers, cfg.qk_norm)
+    if cap:
+        m.reserve_prefill(cap)
+    return m, syn
+
+
+def _prompt(cfg, T, seed, start=0, delta=0):
+    r = np.random.default_rng(seed)
+    toks = r.integers(1, cfg.vocab - 1, size=T).astype(np.int32)
+    p = np.arange(start, start + T, dtype=np.int32) + delta
+    return toks, np.stack([p, p, p]).astype(np.int32)
+
+
+class State:
+    def __init__(self, torch, V):
+        self.t = torch
+        self.tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.pos = torch.zeros(3, dtype=torch.int32, device="cuda")
+        self.cpos = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.fin = torch.ones(1, dtype=torch.uint8, device="cuda")
+        self.logits = torch.zeros(V, dtype=torch.float32, device="cuda")
+
+
+def _prefill(torch, m, toks, pos, slot, start, st):
+    T = len(toks)
+    dt = torch.from_numpy(toks).cuda()
+    dp = torch.from_numpy(np.ascontiguousarray(pos)).cuda()
+    m.prefill(dt, dp, T, slot, start, st.tok, st.pos, st.cpos, st.fin, st.logits)
+    torch.cuda.synchronize()
+    assert m.sync_status() == 0
+
+
+def _cache(m, cfg, slot):
+    n = cfg.slots * cfg.n_kv_heads * cfg.max_len * cfg.head_dim
+    out = []
+    for l in range(cfg.n_layers):
+        for p in m.kv_pointers(l):
+            a = d2h_bytes(p, n * 2).view(np.uint16).reshape(cfg.slots, cfg.n_kv_heads, cfg.max_len, cfg.head_dim)
+            out.append(a[slot].copy())
+    return out
+
+
+@pytest.mark.parametrize("T,start,slot", [(40, 0, 1), (1, 0, 0), (23, 17, 1), (128, 0, 0), (16, 112, 1)])
+def test_tiny_prefill_matches_oracle(torch, T, start, slot):
+    cfg = tiny_config(slots=2)
+    m, syn = _model(cfg, cap=128)
+    o = od.OracleDecoder(cfg, 0)
+    if start:
+        # earlier chunk already in the row (same on both sides)
+        for l in range(cfg.n_layers):
+            k = syn.kv_prefill(l, slot, start, "k")[:, :start]
+            v = syn.kv_prefill(l, slot, start, "v")[:, :start]
+            m.set_kv(l, slot, start, np.ascontiguousarray(k), np.ascontiguousarray(v))
+        o.prefill_cache(slot, start)
+    toks, pos = _prompt(cfg, T, seed=T + start, start=start, delta=-3)
+    st = State(torch, cfg.vocab)
+    _prefill(torch, m, toks, pos, slot, start, st)
+    res = o.prefill(toks, pos, slot, start)
+    logits = st.logits.cpu().numpy()
+    assert rel_l2(logits, res.logits[0]) <= REL_L2_TOL
+    tok = int(st.tok.cpu()[0])
+    assert greedy_agrees(tok, res.logits[0])
+    assert int(st.cpos.cpu()[0]) == start + T and np.array_equal(st.pos.cpu().numpy(), pos[:, -1] + 1)
+    assert int(st.fin.cpu()[0]) == int(res.finished[0])
+    gpu = _cache(m, cfg, slot)
+    for l in range(cfg.n_layers):
+        for j, ref in enumerate((o.K[l][slot], o.V[l][slot])):
+            got = gpu[2 * l + j]
+            sl = slice(start, start + T)
+            assert rel_l2(od.bf16_to_f64(got[:, sl]), od.bf16_to_f64(ref[:, sl])) <= REL_L2_TOL, (l, j)
+            if start:
+                assert np.array_equal(got[:, :start], ref[:, :start])     # earlier positions untouched
+    m.close()
+
+
+def test_chunked_prefill_equals_one_chunk_bitwise(torch):
+    cfg = tiny_config(slots=2)
+    toks, pos = _prompt(cfg, 70, seed=9)
+    a, _ = _model(cfg, cap=70)
+    b, _ = _model(cfg, cap=32)
+    sa, sb = State(torch, cfg.vocab), State(torch, cfg.vocab)
+    _prefill(torch, a, toks, pos, 1, 0, sa)
+    for c0, c1 in ((0, 32), (32, 40), (40, 70)):
+        _prefill(torch, b, toks[c0:c1], pos[:, c0:c1], 1, c0, sb)
+    assert np.array_equal(sa.logits.cpu().numpy(), sb.logits.cpu().numpy())
+    assert int(sa.tok.cpu()[0]) == int(sb.tok.cpu()[0])
+    for x, y in zip(_cache(a, cfg, 1), _cache(b, cfg, 1)):
+        assert np.array_equal(x, y)
+    a.close()
+    b.close()
+
+
+def test_prefill_equals_decode_steps_bitwise_and_decoding_continues(torch):
+    """Prefill of T tokens = the decode step fed the same T tokens one at a time (bit for bit:
+    K/V cache, last logits, next token); then decoding from the prefill's state follows the
+    oracle under the gap rule."""
+    cfg = tiny_config(slots=2)
+    T = 37
+    toks, pos = _prompt(cfg, T, seed=4, delta=5)
+    a, _ = _model(cfg, cap=T)
+    sa = State(torch, cfg.vocab)
+    _prefill(torch, a, toks, pos, 0, 0, sa)
+    b, _ = _model(cfg)
+    d = driver.DeviceState([int(toks[0])], pos[:, :1], [0], [0])
+    lg = torch.zeros((1, cfg.vocab), dtype=torch.float32, device="cuda")
+    for i in range(T):
+        d.tokens[0] = int(toks[i])                       # teacher forcing with the prompt
+        d.step(b, logits=lg)
+    torch.cuda.synchronize()
+    assert np.array_equal(sa.logits.cpu().numpy(), lg[0].cpu().numpy())
+    assert int(sa.tok.cpu()[0]) == int(d.tokens.cpu()[0])
+    assert int(sa.cpos.cpu()[0]) == int(d.cache_position.cpu()[0]) == T
+    for x, y in zip(_cache(a, cfg, 0), _cache(b, cfg, 0)):
+        assert np.array_equal(x, y)
+    # decode on from the prefill's state, against the oracle
+    o = od.OracleDecoder(cfg, 0)
+    res = o.prefill(toks, pos, 0, 0)
+    st = (res.next_ids, res.positions, res.cache_position, np.array([0], np.int32), res.finished)
+    dev = driver.DeviceState([int(sa.tok.cpu()[0])], sa.pos.cpu().numpy().reshape(3, 1), [T], [0])
+    for t in range(8):
+        res = o.step(*st)
+        dev.step(a, logits=lg)
+        tok = int(dev.tokens.cpu()[0])
+        assert rel_l2(lg[0].cpu().numpy(), res.logits[0]) <= REL_L2_TOL
+        if tok != int(res.next_ids[0]):
+            assert greedy_agrees(tok, res.logits[0])
+            break
+        st = (res.next_ids, res.positions, res.cache_position, st[3], res.finished)
+    a.close()
+    b.close()
+
+
+def test_prefill_single_2b_layer_matches_oracle(torch):
+    cfg = layer2b_config(slots=1)
+    T = 48
+    m, _ = _model(cfg, cap=64)
+    o = od.OracleDecoder(cfg, 0)
+    toks, pos = _prompt(cfg, T, seed=2, delta=-40)
+    st = State(torch, cfg.vocab)
+    _prefill(torch, m, toks, pos, 0, 0, st)
+    res = o.prefill(toks, pos, 0, 0)
+    assert rel_l2(st.logits.cpu().numpy(), res.logits[0]) <= REL_L2_TOL
+    assert greedy_agrees(int(st.tok.cpu()[0]), res.logits[0])
+    gpu = _cache(m, cfg, 0)
+    assert rel_l2(od.bf16_to_f64(gpu[0][:, :T]), od.bf16_to_f64(o.K[0][0][:, :T])) <= REL_L2_TOL
+    assert rel_l2(od.bf16_to_f64(gpu[1][:, :T]), od.bf16_to_f64(o.V[0][0][:, :T])) <= REL_L2_TOL
+    m.close()
+
+
+def test_prefill_argument_errors(torch):
+    cfg = tiny_config(slots=2)
+    m, _ = _model(cfg)
+    st = State(torch, cfg.vocab)
+    toks, pos = _prompt(cfg, 8, seed=1)
+    dt, dp = torch.from_numpy(toks).cuda(), torch.from_numpy(pos).cuda()
+    L, h = kmr.lib(), m.handle
+    call = lambda T, slot, start: L.kmr_prefill(h, dt.data_ptr(), dp.data_ptr(), T, slot, start, st.tok.data_ptr(),
+                                               st.pos.data_ptr(), st.cpos.data_ptr(), st.fin.data_ptr(), None, None)
+    assert call(8, 0, 0) == kmr.KMR_ERR_BUFFER_SIZE                 # nothing reserved yet
+    assert L.kmr_model_reserve_prefill(h, 0) == kmr.KMR_ERR_INVALID_ARG
+    assert L.kmr_model_reserve_prefill(h, cfg.max_len + 1) == kmr.KMR_ERR_CACHE_FULL
+    m.reserve_prefill(8)
+    assert call(0, 0, 0) == kmr.KMR_ERR_INVALID_ARG
+    assert call(9, 0, 0) == kmr.KMR_ERR_BUFFER_SIZE
+    assert call(8, 2, 0) == kmr.KMR_ERR_SLOT_RANGE
+    assert call(8, 0, cfg.max_len - 7) == kmr.KMR_ERR_CACHE_FULL
+    assert call(8, 0, -1) == kmr.KMR_ERR_CACHE_FULL
+    assert L.kmr_prefill(h, None, dp.data_ptr(), 8, 0, 0, st.tok.data_ptr(), st.pos.data_ptr(),
+                         st.cpos.data_ptr(), st.fin.data_ptr(), None, None) == kmr.KMR_ERR_INVALID_ARG
+    empty = kmr.Model.from_config(cfg)
+    empty.reserve_prefill(8)
+    assert L.kmr_prefill(empty.handle, dt.data_ptr(), dp.data_ptr(), 8, 0, 0, st.tok.data_ptr(), st.pos.data_ptr(),
+                         st.cpos.data_ptr(), st.fin.data_ptr(), None, None) == kmr.KMR_ERR_NO_PACK
+    # a full row: the next token is emitted and the row is finished (cache cap)
+    m.reserve_prefill(cfg.max_len)
+    toks, pos = _prompt(cfg, cfg.max_len, seed=3)
+    _prefill(torch, m, toks, pos, 1, 0, st)
+    assert int(st.fin.cpu()[0]) == 1 and int(st.cpos.cpu()[0]) == cfg.max_len
+    empty.close()
+    m.close()

@@ -122,3 +122,26 @@ def test_tiny_workload_greedy_16_steps_runs():
         st = (r.next_ids, r.positions, r.cache_position, st[3], r.finished)
     assert len(toks) == 16 and all(0 <= t < wl.cfg.vocab for t in toks)
     assert st[2][0] == 32 + 16
+
+
+def test_oracle_prefill_is_causal_and_chunkable():
+    """Prefill [K §04] as the step applied to each prompt token: a chunked prefill equals one
+    prefill, and a later prompt token changes neither the K/V nor the hidden state of the
+    earlier positions (causal attention)."""
+    from workloads import tiny_config
+    cfg = tiny_config(slots=2)
+    toks = [5, 77, 300, 12, 999, 64]
+    pos = np.array([list(range(3, 9))] * 3)
+    a = od.OracleDecoder(cfg, 0)
+    ra = a.prefill(toks, pos, 1, 3)
+    b = od.OracleDecoder(cfg, 0)
+    b.prefill(toks[:4], pos[:, :4], 1, 3)
+    rb = b.prefill(toks[4:], pos[:, 4:], 1, 7)
+    assert np.array_equal(ra.logits, rb.logits) and ra.next_ids[0] == rb.next_ids[0]
+    for l in range(cfg.n_layers):
+        assert np.array_equal(a.K[l], b.K[l]) and np.array_equal(a.V[l], b.V[l])
+    assert int(ra.cache_position[0]) == 9 and np.array_equal(ra.positions[:, 0], [9, 9, 9])
+    c = od.OracleDecoder(cfg, 0)
+    c.prefill(toks[:-1] + [1], pos, 1, 3)                      # only the last token differs
+    for l in range(cfg.n_layers):
+        assert np.array_equal(a.K[l][1, :, :8], c.K[l][1, :, :8]) and not np.array_equal(a.K[l][1, :, 8], c.K[l][1, :, 8])
