@@ -112,10 +112,10 @@ __device__ __forceinline__ float tree16(const float* v, int stride) {
 // cores, reduce each tile's 16 group partials in the one-row GEMV's fixed order, apply the
 // RMSNorm factor and push the rank's rows into every rank's q/k/v buffer.  Every step
 // mirrors the one-row int4 GEMV (kmr_gemv.cu), so a row's q, k, v are the same bits
-// whether the step ran it fused (batch 1) or through the GEMV (larger batches).
+// whether the step ran it fused (small batches) or through the GEMV (larger ones).
 template <int D, int REP>
 __device__ __forceinline__ void qkv_phase(const AttnParams& p, uint8_t* smem, const AttnSmem& L, int s, int h,
-                                          int lane, int warp, const uint2 (&nwv)[2]) {
+                                          int b, int lane, int warp, const uint2 (&nwv)[2]) {
     constexpr int TPR = (REP + 2) * D / 128;
     const int K = p.hidden, G = K >> 7;
     const int tid = threadIdx.x;
@@ -135,16 +135,16 @@ __device__ __forceinline__ void qkv_phase(const AttnParams& p, uint8_t* smem, co
         if (g >= G) continue;
         const size_t k = size_t(g) * 128 + lane * 4;
         if (embed) {
-            int tok = p.tokens[0];
+            int tok = p.tokens[b];
             if (tok < 0 || tok >= p.vocab) {
                 if (lane == 0 && g == 0 && s == 0 && h == 0) set_error(p.err, KMR_ERR_INVALID_ARG);
                 tok = 0;
             }
             const uint2 raw = *reinterpret_cast<const uint2*>(p.embed + size_t(tok) * K + k);
             xv[j] = make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
-            if (s == 0 && h == 0 && p.x_out) *reinterpret_cast<float4*>(p.x_out + k) = xv[j];
+            if (s == 0 && h == 0 && p.x_out) *reinterpret_cast<float4*>(p.x_out + size_t(b) * K + k) = xv[j];
         } else {
-            xv[j] = *reinterpret_cast<const float4*>(p.x + k);
+            xv[j] = *reinterpret_cast<const float4*>(p.x + size_t(b) * K + k);
         }
     }
     // (X' of both groups, sum of squares of both groups) in one reduce-scatter: lanes
@@ -264,13 +264,13 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
             if constexpr (QKVF) {
                 // the layer-0 embedding still lands in the residual, as the GEMV path stores it
                 if (h == 0 && p.x_kind == IN_EMBED_NORM && p.x_out) {
-                    int tok = p.tokens[0];
+                    int tok = p.tokens[b];
                     if (tok < 0 || tok >= p.vocab) {
                         if (tid == 0) set_error(p.err, KMR_ERR_INVALID_ARG);
                         tok = 0;
                     }
                     for (int k = tid; k < p.hidden; k += kThreads)
-                        p.x_out[k] = bf16_to_f32(p.embed[size_t(tok) * p.hidden + k]);
+                        p.x_out[size_t(b) * p.hidden + k] = bf16_to_f32(p.embed[size_t(tok) * p.hidden + k]);
                 }
             }
         }
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     pdl_launch_dependents();
     pdl_wait();
 
-    if constexpr (QKVF) qkv_phase<D, REP>(p, smem, L, s, h, lane, warp, qnw);
+    if constexpr (QKVF) qkv_phase<D, REP>(p, smem, L, s, h, b, lane, warp, qnw);
 
     // ---- prologue: q (and, fused, the new k / v) of this KV head
     const float qscale = __fmul_rn(p.scale, kLog2e);       // scores in base 2
@@ -687,7 +687,7 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t st, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(q.tsplit, p.nkv, p.B);
     cfg.blockDim = dim3(kThreads);
-    const bool qkv = p.cluster && p.wqkv != nullptr && p.B == 1 && attn_can_fuse_qkv(p.d, rep, p.hidden);
+    const bool qkv = p.cluster && p.wqkv != nullptr && attn_can_fuse_qkv(p.d, rep, p.hidden);
     if (!qkv) q.wqkv = nullptr;
     cfg.dynamicSmemBytes = attn_smem_bytes(p.d, rep, q.nstage, ch, qkv ? p.qkv_tile_bytes : 0);
     cfg.stream = st;

@@ -264,19 +264,19 @@ struct AttnParams {
     float* part;                 // [B][nkv][tsplit][rep][d+2]
     int* counters;               // [B][nkv]
     int* err;
-    // Fused QKV projection (cluster mode, one row; wqkv == null: off).  Rank s of the cluster
-    // of KV head h computes the head group's QKV rows [s, s+1) * tpr tiles itself, with the
+    // Fused QKV projection (cluster mode; wqkv == null: off).  Rank s of the cluster of
+    // (KV head h, row b) computes the head group's QKV rows [s, s+1) * tpr tiles of row b itself, with the
     // one-row int4 GEMV's arithmetic, and the cluster all-gathers them through distributed
     // shared memory; the attention prologue then reads q, k, v from shared memory.
     const uint8_t* wqkv;         // packed QKV weights (KMR4; N = (nq + 2 nkv) d, K = hidden)
     int qkv_tile_bytes;          // (hidden / 128) * 1088
     int hidden;
     int x_kind;                  // IN_F32_NORM (x = residual row) or IN_EMBED_NORM (x = E[token])
-    const float* x;              // residual row fp32 [hidden]
+    const float* x;              // residual rows fp32 [B][hidden]
     const uint16_t* embed;       // bf16 [vocab][hidden]
-    const int32_t* tokens;       // token of the row (IN_EMBED_NORM)
+    const int32_t* tokens;       // token of each row (IN_EMBED_NORM)
     int vocab;
-    float* x_out;                // IN_EMBED_NORM: the embedded row is stored here (one CTA)
+    float* x_out;                // IN_EMBED_NORM: the embedded rows are stored here (one CTA per row)
     const uint16_t* in_norm_w;   // bf16 [hidden]: input RMSNorm weight
 };
 // Shared-memory poisoning diagnostic (kmr_poison.cu).
