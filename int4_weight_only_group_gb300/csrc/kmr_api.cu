@@ -57,6 +57,7 @@ cudaError_t ensure_kernel_attributes() {
     if ((e = head_set_attributes()) != cudaSuccess) return e;
     if ((e = attn_set_attributes()) != cudaSuccess) return e;
     if ((e = poison_set_attributes()) != cudaSuccess) return e;
+    if ((e = gemm_set_attributes()) != cudaSuccess) return e;
     done[dev] = true;
     return cudaSuccess;
 }
@@ -356,6 +357,9 @@ struct kmr_model {
     float* pact = nullptr;         // [cap][I]
     int32_t* pslot = nullptr;      // [cap]
     int32_t* pcpos = nullptr;      // [cap]
+    uint16_t* pxs = nullptr;       // staged rows fp16 [Gmax][Mpad][128] (Gmax = largest K / 128)
+    float2* pxst = nullptr;        // [Gmax][Mpad] (X', 1/sigma)
+    float* prn = nullptr;          // [Mpad] RMSNorm factors
     uint32_t poison_pattern = 0;
     std::vector<void*> allocs;
     std::mutex mu;
@@ -596,17 +600,52 @@ struct PrefillArgs {
     float* logits;             // [V] or null
 };
 
-// Queue one prefill chunk: per layer the QKV GEMV over all T positions (16-row passes from one
-// weight fill each; the weights stay in L2 across passes), the q/k norm + M-RoPE + KV write of
-// every position, causal attention as one decode-attention row per position (row i attends
-// 0..start + i of the same cache row), then O, gate_up and down over all positions; the LM
-// head runs on the last position only.
+// One int4 projection of all T rows of a prefill chunk: stage the rows once, then the
+// weight-stationary GEMM (each unpacked weight fragment serves 64 rows).
+int enqueue_projection(kmr_model* m, const GemvLaunch& g, int T, cudaStream_t st) {
+    StageParams sp = {};
+    sp.in_kind = g.in_kind;
+    sp.x = g.x;
+    sp.embed = g.embed;
+    sp.tokens = g.tokens;
+    sp.vocab = g.vocab;
+    sp.x_out = g.x_out;
+    sp.norm_w = g.norm_w;
+    sp.eps = g.eps;
+    sp.M = T;
+    sp.Mpad = gemm_rows_pad(T);
+    sp.K = g.g.K;
+    sp.xs = m->pxs;
+    sp.xst = m->pxst;
+    sp.rnorm = m->prn;
+    sp.err = m->err;
+    if (launch_stage(sp, st) != cudaSuccess) return KMR_ERR_CUDA;
+    GemmParams gp = {};
+    gp.w = g.w;
+    gp.N = g.g.N;
+    gp.K = g.g.K;
+    gp.tiles = g.g.tiles;
+    gp.xs = m->pxs;
+    gp.xst = m->pxst;
+    gp.rnorm = m->prn;
+    gp.M = T;
+    gp.Mpad = sp.Mpad;
+    gp.epi = g.epi;
+    gp.y = g.y;
+    gp.ldy = g.ldy;
+    gp.err = m->err;
+    return launch_gemm(gp, st) == cudaSuccess ? KMR_OK : KMR_ERR_CUDA;
+}
+
+// Queue one prefill chunk: per layer the QKV projection of all T positions, the q/k norm +
+// M-RoPE + KV write of every position, causal attention as one decode-attention row per
+// position (row i attends 0..start + i of the same cache row), then O, gate_up and down over
+// all positions; the LM head runs on the last position only.
 int enqueue_prefill(kmr_model* m, const PrefillArgs& a, cudaStream_t st) {
     const kmr_model_config& c = m->cfg;
     const int T = a.T;
     const int nqkv = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
     const int grid = m->sms;
-    bool pdl = false;
     for (int l = 0; l < c.n_layers; ++l) {
         LayerW& L = m->layers[l];
         GemvLaunch g = {};
@@ -623,7 +662,7 @@ int enqueue_prefill(kmr_model* m, const PrefillArgs& a, cudaStream_t st) {
         g.epi = EPI_STORE;
         g.y = m->pqkv;
         g.ldy = nqkv;
-        if (enqueue_gemv(g, T, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        if (enqueue_projection(m, g, T, st) != KMR_OK) return KMR_ERR_CUDA;
         PrefillRopeParams rp = {};
         rp.qkv = m->pqkv;
         rp.qkv_ld = nqkv;
@@ -667,14 +706,13 @@ int enqueue_prefill(kmr_model* m, const PrefillArgs& a, cudaStream_t st) {
         ap.S = c.max_len;
         ap.slots = c.slots;
         ap.scale = 1.0f / sqrtf(float(c.head_dim));
-        ap.tsplit = kAttnClusterSplits;
-        ap.cluster = 1;
+        ap.tsplit = 1;                   // one CTA per (position, KV head): a whole causal row, no merge
+        ap.cluster = 0;
         ap.out = m->pattn;
         ap.err = m->err;
         // no programmatic overlap here: the attention kernel reads its row state and starts its
         // K/V copies before griddepcontrol.wait, and the previous kernel has just written both
         if (launch_attn(ap, st, false) != cudaSuccess) return KMR_ERR_CUDA;
-        pdl = true;
         g = GemvLaunch{};
         g.w = L.w[KMR_W_O];
         g.g = L.g[KMR_W_O];
@@ -683,7 +721,7 @@ int enqueue_prefill(kmr_model* m, const PrefillArgs& a, cudaStream_t st) {
         g.epi = EPI_RESID;
         g.y = m->px;
         g.ldy = c.hidden;
-        if (enqueue_gemv(g, T, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        if (enqueue_projection(m, g, T, st) != KMR_OK) return KMR_ERR_CUDA;
         g = GemvLaunch{};
         g.w = L.w[KMR_W_GATE_UP];
         g.g = L.g[KMR_W_GATE_UP];
@@ -694,7 +732,7 @@ int enqueue_prefill(kmr_model* m, const PrefillArgs& a, cudaStream_t st) {
         g.epi = EPI_SILU;
         g.y = m->pact;
         g.ldy = c.intermediate;
-        if (enqueue_gemv(g, T, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        if (enqueue_projection(m, g, T, st) != KMR_OK) return KMR_ERR_CUDA;
         g = GemvLaunch{};
         g.w = L.w[KMR_W_DOWN];
         g.g = L.g[KMR_W_DOWN];
@@ -703,7 +741,7 @@ int enqueue_prefill(kmr_model* m, const PrefillArgs& a, cudaStream_t st) {
         g.epi = EPI_RESID;
         g.y = m->px;
         g.ldy = c.hidden;
-        if (enqueue_gemv(g, T, m->err, st, pdl, grid) < 0) return KMR_ERR_CUDA;
+        if (enqueue_projection(m, g, T, st) != KMR_OK) return KMR_ERR_CUDA;
     }
     HeadParams hp = {};
     hp.E = m->embed;
@@ -734,7 +772,7 @@ int enqueue_prefill(kmr_model* m, const PrefillArgs& a, cudaStream_t st) {
     if (nst < 2) nst = 2;
     if (nst > tpc) nst = tpc;
     hp.nstage = nst;
-    if (launch_head(hp, 1, hgrid, st, true) != cudaSuccess) return KMR_ERR_CUDA;
+    if (launch_head(hp, 1, hgrid, st, false) != cudaSuccess) return KMR_ERR_CUDA;
     return KMR_OK;
 }
 
@@ -983,7 +1021,7 @@ extern "C" int kmr_model_reserve_prefill(kmr_model* m, int max_tokens) {
     if (max_tokens <= m->prefill_cap) return KMR_OK;
     DeviceGuard dg(m->device);
     if (cudaDeviceSynchronize() != cudaSuccess) return KMR_ERR_CUDA;
-    void* old[7] = {m->px, m->pqkv, m->pq, m->pattn, m->pact, m->pslot, m->pcpos};
+    void* old[10] = {m->px, m->pqkv, m->pq, m->pattn, m->pact, m->pslot, m->pcpos, m->pxs, m->pxst, m->prn};
     for (void* p : old) {
         if (!p) continue;
         m->allocs.erase(std::remove(m->allocs.begin(), m->allocs.end(), p), m->allocs.end());
@@ -995,6 +1033,11 @@ extern "C" int kmr_model_reserve_prefill(kmr_model* m, int max_tokens) {
     if (dalloc(m, &m->px, T * c.hidden * 4) || dalloc(m, &m->pqkv, T * nqkv * 4) || dalloc(m, &m->pq, T * qd * 4) ||
         dalloc(m, &m->pattn, T * qd * 4) || dalloc(m, &m->pact, T * c.intermediate * 4) ||
         dalloc(m, &m->pslot, T * 4) || dalloc(m, &m->pcpos, T * 4))
+        return KMR_ERR_CUDA;
+    const size_t Mpad = size_t(gemm_rows_pad(max_tokens));
+    const size_t Gmax = size_t(std::max(std::max(c.hidden, qd), c.intermediate) / 128);
+    if (dalloc(m, &m->pxs, Gmax * Mpad * 128 * 2) || dalloc(m, &m->pxst, Gmax * Mpad * 8) ||
+        dalloc(m, &m->prn, Mpad * 4))
         return KMR_ERR_CUDA;
     m->prefill_cap = max_tokens;
     return KMR_OK;

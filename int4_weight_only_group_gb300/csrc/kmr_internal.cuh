@@ -300,6 +300,39 @@ void cascade_plan(int prefix_len, int nkv, int sms, int* pchunk, int* psplits);
 size_t cascade_workspace_bytes(int B, int nq, int d, int psplits);
 cudaError_t launch_cascade(const CascadeParams& p, cudaStream_t st);
 
+// Prefill's int4 projections (kmr_gemm.cu): rows staged once, then a weight-stationary GEMM.
+struct StageParams {
+    int in_kind;                            // IN_F32, IN_F32_NORM or IN_EMBED_NORM
+    const float* x;                         // [M][K]
+    const uint16_t* embed;                  // bf16 [vocab][K] (IN_EMBED_NORM)
+    const int32_t* tokens;
+    int vocab;
+    float* x_out;                           // IN_EMBED_NORM: embedded rows [M][K] (or null)
+    const uint16_t* norm_w;                 // bf16 [K] (IN_*_NORM)
+    float eps;
+    int M, Mpad, K;
+    uint16_t* xs;                           // fp16 [K/128][Mpad][128] in B-fragment order
+    float2* xst;                            // [K/128][Mpad]: (X', 1/sigma)
+    float* rnorm;                           // [Mpad]: RMSNorm factor (1 without norm)
+    int* err;
+};
+struct GemmParams {
+    const uint8_t* w;                       // packed KMR4
+    int N, K, tiles;
+    const uint16_t* xs;
+    const float2* xst;
+    const float* rnorm;
+    int M, Mpad, epi;
+    float* y;
+    int ldy;
+    int* err;
+};
+size_t gemm_smem_bytes();
+int gemm_rows_pad(int M);
+cudaError_t gemm_set_attributes();
+cudaError_t launch_stage(const StageParams& p, cudaStream_t st);
+cudaError_t launch_gemm(const GemmParams& p, cudaStream_t st);
+
 // Prefill's per-position attention prologue (kmr_prefill.cu): q/k RMSNorm + M-RoPE of T
 // prompt positions, K/V into cache row `slot` at [start, start + T), queries to q_out.
 struct PrefillRopeParams {

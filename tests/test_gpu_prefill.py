@@ -2,8 +2,10 @@
 applied to each prompt token in order ("kaminari", §04 Request lifecycle: prefill fills the
 static cache and yields the first token from the last position's logits).
 
-Besides the oracle: chunked prefill must equal one-chunk prefill bit for bit, and prefill must
-equal the GPU's own decode step run token by token bit for bit (same arithmetic per row)."""
+Besides the oracle: chunked prefill must equal one-chunk prefill bit for bit (a row's result
+depends only on that row), and prefill must agree with the GPU's own decode step run token by
+token (the prefill GEMM sums the 128-input groups in order where the decode GEMV uses a
+pairwise tree, so the two differ by rounding only)."""
 import numpy as np
 import pytest
 
@@ -116,10 +118,13 @@ def test_chunked_prefill_equals_one_chunk_bitwise(torch):
     b.close()
 
 
-def test_prefill_equals_decode_steps_bitwise_and_decoding_continues(torch):
-    """Prefill of T tokens = the decode step fed the same T tokens one at a time (bit for bit:
-    K/V cache, last logits, next token); then decoding from the prefill's state follows the
-    oracle under the gap rule."""
+def test_prefill_agrees_with_decode_steps_and_decoding_continues(torch):
+    """Prefill of T tokens = the decode step fed the same T tokens one at a time, up to the
+    order of fp32 sums: a sum that lands on the other side of a bf16 rounding boundary changes
+    one cached value by a bf16 step, and the last logits move by ~1e-3 (relative L2) — within
+    the parity bar both paths keep against the oracle; the same token unless the decode logits
+    have a near tie.  Then decoding from the prefill's state follows the oracle under the gap
+    rule."""
     cfg = tiny_config(slots=2)
     T = 37
     toks, pos = _prompt(cfg, T, seed=4, delta=5)
@@ -133,11 +138,12 @@ def test_prefill_equals_decode_steps_bitwise_and_decoding_continues(torch):
         d.tokens[0] = int(toks[i])                       # teacher forcing with the prompt
         d.step(b, logits=lg)
     torch.cuda.synchronize()
-    assert np.array_equal(sa.logits.cpu().numpy(), lg[0].cpu().numpy())
-    assert int(sa.tok.cpu()[0]) == int(d.tokens.cpu()[0])
+    dec = lg[0].cpu().numpy()
+    assert rel_l2(sa.logits.cpu().numpy(), dec) <= REL_L2_TOL
+    assert greedy_agrees(int(sa.tok.cpu()[0]), dec)
     assert int(sa.cpos.cpu()[0]) == int(d.cache_position.cpu()[0]) == T
     for x, y in zip(_cache(a, cfg, 0), _cache(b, cfg, 0)):
-        assert np.array_equal(x, y)
+        assert rel_l2(od.bf16_to_f64(x[:, :T]), od.bf16_to_f64(y[:, :T])) <= REL_L2_TOL
     # decode on from the prefill's state, against the oracle
     o = od.OracleDecoder(cfg, 0)
     res = o.prefill(toks, pos, 0, 0)
