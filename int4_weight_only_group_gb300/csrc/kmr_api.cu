@@ -634,7 +634,7 @@ int enqueue_projection(kmr_model* m, const GemvLaunch& g, int T, cudaStream_t st
     gp.y = g.y;
     gp.ldy = g.ldy;
     gp.err = m->err;
-    return launch_gemm(gp, st) == cudaSuccess ? KMR_OK : KMR_ERR_CUDA;
+    return launch_gemm(gp, m->sms, st) == cudaSuccess ? KMR_OK : KMR_ERR_CUDA;
 }
 
 // Queue one prefill chunk: per layer the QKV projection of all T positions, the q/k norm +

@@ -11,14 +11,14 @@
 //                 batch instead of once per CTA — plus (X', 1/sigma) per (row, group) and
 //                 the row's RMSNorm factor.  Layout [group][row][...] so that a group's block
 //                 of rows is one contiguous copy.
-//   gemm_kernel   CTA tile: 8 weight tiles (128 output features) x 128 rows.  A producer
-//                 warp streams, per 128-input group, the 8 tiles' 1088-byte blocks and the
-//                 rows' staged block into a 4-stage ring (cp.async.bulk, mbarriers); each of
-//                 16 consumer warps owns one weight tile and 64 rows, unpacks the tile's A
-//                 fragments once per group and runs them against 8 row-blocks
-//                 (mma.sync m16n8k16), folding each group into fp32 accumulators
-//                 (s (D - 1024 X') / c + (z - 8 s) X') / sigma.  Groups are summed in order;
-//                 a row's result depends on nothing but that row.
+//   gemm_kernel   CTA tile: TW = 8 (or 4, when 8 would leave most SMs idle) weight tiles x
+//                 128 rows.  A producer warp streams, per 128-input group, the tiles' 1088-byte
+//                 blocks and the rows' staged block into a 4-stage ring (cp.async.bulk,
+//                 mbarriers); each of 8 consumer warps owns a pair of tiles and TW row-blocks
+//                 of 8 rows, unpacks the pair's A fragments once per group, and loads each
+//                 row-block's B fragments once for both tiles (mma.sync m16n8k16), folding
+//                 each group into fp32 accumulators (s (D - 1024 X') / c + (z - 8 s) X') / sigma.
+//                 Groups are summed in order; a row's result depends on nothing but that row.
 #include <cuda_fp16.h>
 
 #include "kmr_int4_mma.cuh"
@@ -27,15 +27,13 @@
 namespace kmr {
 namespace {
 
-constexpr int kGemmTiles = 8;               // weight tiles per CTA (128 output features)
 constexpr int kGemmRows = 128;              // rows per CTA
 constexpr int kGemmStages = 4;
-constexpr int kGemmConsumers = 16;          // consumer warps
-constexpr int kGemmThreads = (kGemmConsumers + 1) * 32;
-constexpr int kStageW = kGemmTiles * kGroupBytes;            // 8704
+constexpr int kGemmConsumers = 8;           // warps (all compute; lane 0 of warp 0 also refills the ring)
+constexpr int kGemmThreads = kGemmConsumers * 32;
 constexpr int kStageX = kGemmRows * 128 * 2;                 // 32768
 constexpr int kStageS = kGemmRows * 8;                       // 1024: (X', 1/sigma) per row
-constexpr int kStageBytes = kStageW + kStageX + kStageS;     // 42496
+constexpr int stage_bytes(int tw) { return tw * kGroupBytes + kStageX + kStageS; }
 
 // ---- staging: one CTA per row, 8 warps; warp w takes groups w, w + 8, ...
 __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
@@ -108,12 +106,18 @@ __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
     }
 }
 
-// ---- GEMM
+// ---- GEMM: TW weight tiles x 128 rows per CTA; warp w takes tile pair w % (TW / 2) and the
+// TW row-blocks starting at TW * (w / (TW / 2)) (8 warps cover TW / 2 pairs x 16 row-blocks).
+// Two warps per SM sub-partition leave up to 255 registers per thread: 64 accumulators and
+// the pair's 64 A-fragment registers stay resident.
+template <int TW>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const GemmParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int PAIRS = TW / 2, RBW = 2 * PAIRS;           // row-blocks per warp (16 in all)
+    constexpr int SW = TW * kGroupBytes, SB = SW + kStageX + kStageS;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = p.K >> 7;
-    const int tile0 = blockIdx.x * kGemmTiles, r0 = blockIdx.y * kGemmRows;
+    const int tile0 = blockIdx.x * TW, r0 = blockIdx.y * kGemmRows;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + kGemmStages;
     uint8_t* stages = smem + 128;
@@ -125,65 +129,69 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const GemmParams 
         fence_mbar_init();
     }
     __syncthreads();
-    const int ntl = min(kGemmTiles, p.tiles - tile0);         // tiles this CTA owns (>= 1)
+    const int ntl = min(TW, p.tiles - tile0);                 // tiles this CTA owns (>= 1)
 
-    if (warp == kGemmConsumers) {
-        // ---- producer: one lane streams group after group
-        if (lane == 0) {
-            for (int g = 0; g < G; ++g) {
-                const int s = g % kGemmStages;
-                if (g >= kGemmStages && !mbar_wait(&empty[s], uint32_t(((g / kGemmStages) - 1) & 1), p.err)) break;
-                uint8_t* st = stages + size_t(s) * kStageBytes;
-                mbar_arrive_expect_tx(&full[s], uint32_t(ntl * kGroupBytes + kStageX + kStageS));
-                for (int t = 0; t < ntl; ++t)
-                    bulk_g2s(st + t * kGroupBytes, p.w + (size_t(tile0 + t) * G + g) * kGroupBytes, kGroupBytes, &full[s]);
-                bulk_g2s(st + kStageW, p.xs + (size_t(g) * p.Mpad + r0) * 128, kStageX, &full[s]);
-                bulk_g2s(st + kStageW + kStageX, p.xst + size_t(g) * p.Mpad + r0, kStageS, &full[s]);
-            }
-        }
-        return;
-    }
-    // ---- consumers: warp w owns tile (w % 8) and row-blocks [8 (w / 8), 8 (w / 8) + 8)
-    const int tl = warp % kGemmTiles, rb0 = (warp / kGemmTiles) * 8;
-    const bool active = tl < ntl;
+    // the ring is filled by lane 0 of warp 0: groups 0..stages-1 now, group g + stages once
+    // every warp has released group g
+    auto issue = [&](int g) {
+        const int s = g % kGemmStages;
+        uint8_t* st = stages + size_t(s) * SB;
+        mbar_arrive_expect_tx(&full[s], uint32_t(ntl * kGroupBytes + kStageX + kStageS));
+        for (int t = 0; t < ntl; ++t)
+            bulk_g2s(st + t * kGroupBytes, p.w + (size_t(tile0 + t) * G + g) * kGroupBytes, kGroupBytes, &full[s]);
+        bulk_g2s(st + SW, p.xs + (size_t(g) * p.Mpad + r0) * 128, kStageX, &full[s]);
+        bulk_g2s(st + SW + kStageX, p.xst + size_t(g) * p.Mpad + r0, kStageS, &full[s]);
+    };
+    if (tid == 0)
+        for (int g = 0; g < G && g < kGemmStages; ++g) issue(g);
+    const int pr = warp % PAIRS, rb0 = (warp / PAIRS) * RBW;
+    const int ta = 2 * pr;                                   // tiles ta, ta + 1 of the CTA
+    const bool act0 = ta < ntl, act1 = ta + 1 < ntl;
     const int g8 = lane >> 2, t4 = lane & 3;
-    float acc[8][4];
+    float acc[RBW][2][4];
 #pragma unroll
-    for (int rb = 0; rb < 8; ++rb) acc[rb][0] = acc[rb][1] = acc[rb][2] = acc[rb][3] = 0.f;
+    for (int rb = 0; rb < RBW; ++rb)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) acc[rb][u][0] = acc[rb][u][1] = acc[rb][u][2] = acc[rb][u][3] = 0.f;
     for (int g = 0; g < G; ++g) {
         const int s = g % kGemmStages;
         mbar_wait(&full[s], uint32_t((g / kGemmStages) & 1), p.err);
-        const uint8_t* st = stages + size_t(s) * kStageBytes;
-        if (active) {
-            const uint8_t* gb = st + tl * kGroupBytes;
-            const __half* xb = reinterpret_cast<const __half*>(st + kStageW);
-            const float2* xsc = reinterpret_cast<const float2*>(st + kStageW + kStageX);
-            // this tile's A fragments for the 8 k-steps of the group, unpacked once
-            uint32_t a[8][4];
+        const uint8_t* st = stages + size_t(s) * SB;
+        if (act0) {
+            const __half* xb = reinterpret_cast<const __half*>(st + SW);
+            const float2* xsc = reinterpret_cast<const float2*>(st + SW + kStageX);
+            // both tiles' A fragments for the group's 8 k-steps, unpacked once (a missing second
+            // tile repeats the first; its results are never stored)
+            uint32_t a[2][8][4];
+            float s0[2], s1c[2], zz0[2], zz1[2];
 #pragma unroll
-            for (int blk = 0; blk < 2; ++blk) {
-                const uint4 wq = *reinterpret_cast<const uint4*>(gb + blk * 512 + lane * 16);
-                const uint32_t w4[4] = {wq.x, wq.y, wq.z, wq.w};
+            for (int u = 0; u < 2; ++u) {
+                const uint8_t* gb = st + (act1 ? ta + u : ta) * kGroupBytes;
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t w = w4[ks], w2 = w >> 8;
-                    a[blk * 4 + ks][0] = and_or(w, 0x000F000Fu, 0x64006400u);
-                    a[blk * 4 + ks][1] = and_or(w, 0x00F000F0u, 0x64006400u);
-                    a[blk * 4 + ks][2] = and_or(w2, 0x000F000Fu, 0x64006400u);
-                    a[blk * 4 + ks][3] = and_or(w2, 0x00F000F0u, 0x64006400u);
+                for (int blk = 0; blk < 2; ++blk) {
+                    const uint4 wq = *reinterpret_cast<const uint4*>(gb + blk * 512 + lane * 16);
+                    const uint32_t w4[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint32_t w = w4[ks], w2 = w >> 8;
+                        a[u][blk * 4 + ks][0] = and_or(w, 0x000F000Fu, 0x64006400u);
+                        a[u][blk * 4 + ks][1] = and_or(w, 0x00F000F0u, 0x64006400u);
+                        a[u][blk * 4 + ks][2] = and_or(w2, 0x000F000Fu, 0x64006400u);
+                        a[u][blk * 4 + ks][3] = and_or(w2, 0x00F000F0u, 0x64006400u);
+                    }
                 }
+                const uint32_t sz0 = *reinterpret_cast<const uint32_t*>(gb + 1024 + g8 * 4);
+                const uint32_t sz1 = *reinterpret_cast<const uint32_t*>(gb + 1024 + (g8 + 8) * 4);
+                s0[u] = bf16_lo(sz0);
+                s1c[u] = __fmul_rn(bf16_lo(sz1), 0.0625f);
+                zz0[u] = __fmaf_rn(-8.f, s0[u], bf16_hi(sz0));
+                zz1[u] = __fmaf_rn(-8.f, bf16_lo(sz1), bf16_hi(sz1));
             }
-            const uint32_t sz0 = *reinterpret_cast<const uint32_t*>(gb + 1024 + g8 * 4);
-            const uint32_t sz1 = *reinterpret_cast<const uint32_t*>(gb + 1024 + (g8 + 8) * 4);
-            const float s0 = bf16_lo(sz0), z0 = bf16_hi(sz0), s1 = bf16_lo(sz1), z1 = bf16_hi(sz1);
-            const float s1c = __fmul_rn(s1, 0.0625f);
-            const float zz0 = __fmaf_rn(-8.f, s0, z0), zz1 = __fmaf_rn(-8.f, s1, z1);
 #pragma unroll
-            for (int rb = 0; rb < 8; ++rb) {
+            for (int rb = 0; rb < RBW; ++rb) {
                 const int rbase = (rb0 + rb) * 8;
-                // B fragments of rows rbase + g8 (this lane's column)
-                const __half* xr = xb + size_t(rbase + g8) * 128 + t4 * 16;
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                const __half* xr = xb + size_t(rbase + g8) * 128 + t4 * 16;     // this lane's column
+                float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int blk = 0; blk < 2; ++blk) {
                     const uint4 xa = *reinterpret_cast<const uint4*>(xr + blk * 64);
@@ -191,41 +199,52 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const GemmParams 
                     const uint32_t bb[8] = {xa.x, xa.y, xa.z, xa.w, xc.x, xc.y, xc.z, xc.w};
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma16816(d, a[blk * 4 + ks][0], a[blk * 4 + ks][1], a[blk * 4 + ks][2], a[blk * 4 + ks][3],
-                                 bb[2 * ks], bb[2 * ks + 1]);
+#pragma unroll
+                        for (int u = 0; u < 2; ++u)
+                            mma16816(d[u], a[u][blk * 4 + ks][0], a[u][blk * 4 + ks][1], a[u][blk * 4 + ks][2],
+                                     a[u][blk * 4 + ks][3], bb[2 * ks], bb[2 * ks + 1]);
                 }
                 const float2 X0 = xsc[rbase + 2 * t4], X1 = xsc[rbase + 2 * t4 + 1];   // (X', 1/sigma)
                 const float x0 = 1024.f * X0.x, x1 = 1024.f * X1.x;
-                acc[rb][0] = __fmaf_rn(__fmaf_rn(s0, __fsub_rn(d[0], x0), __fmul_rn(zz0, X0.x)), X0.y, acc[rb][0]);
-                acc[rb][1] = __fmaf_rn(__fmaf_rn(s0, __fsub_rn(d[1], x1), __fmul_rn(zz0, X1.x)), X1.y, acc[rb][1]);
-                acc[rb][2] = __fmaf_rn(__fmaf_rn(s1c, __fsub_rn(d[2], x0), __fmul_rn(zz1, X0.x)), X0.y, acc[rb][2]);
-                acc[rb][3] = __fmaf_rn(__fmaf_rn(s1c, __fsub_rn(d[3], x1), __fmul_rn(zz1, X1.x)), X1.y, acc[rb][3]);
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    acc[rb][u][0] = __fmaf_rn(__fmaf_rn(s0[u], __fsub_rn(d[u][0], x0), __fmul_rn(zz0[u], X0.x)), X0.y, acc[rb][u][0]);
+                    acc[rb][u][1] = __fmaf_rn(__fmaf_rn(s0[u], __fsub_rn(d[u][1], x1), __fmul_rn(zz0[u], X1.x)), X1.y, acc[rb][u][1]);
+                    acc[rb][u][2] = __fmaf_rn(__fmaf_rn(s1c[u], __fsub_rn(d[u][2], x0), __fmul_rn(zz1[u], X0.x)), X0.y, acc[rb][u][2]);
+                    acc[rb][u][3] = __fmaf_rn(__fmaf_rn(s1c[u], __fsub_rn(d[u][3], x1), __fmul_rn(zz1[u], X1.x)), X1.y, acc[rb][u][3]);
+                }
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
+        if (tid == 0 && g + kGemmStages < G) {
+            // every warp is done with this stage: refill it
+            if (mbar_wait(&empty[s], uint32_t((g / kGemmStages) & 1), p.err)) issue(g + kGemmStages);
+        }
     }
-    if (!active) return;
-    // ---- epilogue: lane holds tile rows g8 (acc[.][0..1]) and g8 + 8 (acc[.][2..3]) for
-    // x rows rbase + 2 t4 and rbase + 2 t4 + 1
-    const int tile = tile0 + tl;
+    // ---- epilogue: tile rows g8 ([0..1]) and g8 + 8 ([2..3]) for x rows rbase + 2 t4 (+1)
 #pragma unroll
-    for (int rb = 0; rb < 8; ++rb) {
+    for (int u = 0; u < 2; ++u) {
+        if (!(u == 0 ? act0 : act1)) continue;
+        const int tile = tile0 + ta + u;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const int m = r0 + (rb0 + rb) * 8 + 2 * t4 + c;
-            if (m >= p.M) continue;
-            const float r = p.rnorm[m];
-            const float v0 = __fmul_rn(acc[rb][c], r), v1 = __fmul_rn(acc[rb][2 + c], r);
-            float* yr = p.y + size_t(m) * p.ldy;
-            if (p.epi == EPI_SILU) {
-                // gate rows 8 tile .. + 7 are tile rows 0..7, the matching up rows are tile rows 8..15
-                const int j = tile * 8 + g8;
-                if (j < p.N / 2) yr[j] = __fmul_rn(__fdiv_rn(v0, __fadd_rn(1.f, expf(-v0))), v1);
-            } else {
-                const int n0 = tile * 16 + g8, n1 = n0 + 8;
-                if (n0 < p.N) yr[n0] = p.epi == EPI_RESID ? __fadd_rn(yr[n0], v0) : v0;
-                if (n1 < p.N) yr[n1] = p.epi == EPI_RESID ? __fadd_rn(yr[n1], v1) : v1;
+        for (int rb = 0; rb < RBW; ++rb) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int m = r0 + (rb0 + rb) * 8 + 2 * t4 + c;
+                if (m >= p.M) continue;
+                const float r = p.rnorm[m];
+                const float v0 = __fmul_rn(acc[rb][u][c], r), v1 = __fmul_rn(acc[rb][u][2 + c], r);
+                float* yr = p.y + size_t(m) * p.ldy;
+                if (p.epi == EPI_SILU) {
+                    // gate rows 8 tile .. + 7 are tile rows 0..7, the matching up rows tile rows 8..15
+                    const int j = tile * 8 + g8;
+                    if (j < p.N / 2) yr[j] = __fmul_rn(__fdiv_rn(v0, __fadd_rn(1.f, expf(-v0))), v1);
+                } else {
+                    const int n0 = tile * 16 + g8, n1 = n0 + 8;
+                    if (n0 < p.N) yr[n0] = p.epi == EPI_RESID ? __fadd_rn(yr[n0], v0) : v0;
+                    if (n1 < p.N) yr[n1] = p.epi == EPI_RESID ? __fadd_rn(yr[n1], v1) : v1;
+                }
             }
         }
     }
@@ -233,11 +252,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const GemmParams 
 
 }  // namespace
 
-size_t gemm_smem_bytes() { return 128 + size_t(kGemmStages) * kStageBytes; }
+size_t gemm_smem_bytes(int tw) { return 128 + size_t(kGemmStages) * stage_bytes(tw); }
 int gemm_rows_pad(int M) { return (M + kGemmRows - 1) / kGemmRows * kGemmRows; }
 
 cudaError_t gemm_set_attributes() {
-    return cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(gemm_smem_bytes()));
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(gemm_smem_bytes(8)));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(gemm_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(gemm_smem_bytes(4)));
 }
 
 cudaError_t launch_stage(const StageParams& p, cudaStream_t st) {
@@ -245,9 +266,15 @@ cudaError_t launch_stage(const StageParams& p, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(const GemmParams& p, cudaStream_t st) {
-    const dim3 grid((p.tiles + kGemmTiles - 1) / kGemmTiles, p.Mpad / kGemmRows);
-    gemm_kernel<<<grid, kGemmThreads, gemm_smem_bytes(), st>>>(p);
+cudaError_t launch_gemm(const GemmParams& p, int sms, cudaStream_t st) {
+    // 8 tiles per CTA unless that leaves more than half of the SMs without a CTA
+    const int rows = p.Mpad / kGemmRows;
+    const int tw = ((p.tiles + 7) / 8) * rows * 2 >= sms ? 8 : 4;
+    const dim3 grid((p.tiles + tw - 1) / tw, rows);
+    if (tw == 8)
+        gemm_kernel<8><<<grid, kGemmThreads, gemm_smem_bytes(8), st>>>(p);
+    else
+        gemm_kernel<4><<<grid, kGemmThreads, gemm_smem_bytes(4), st>>>(p);
     return cudaGetLastError();
 }
 

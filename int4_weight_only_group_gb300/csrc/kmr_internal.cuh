@@ -327,11 +327,11 @@ struct GemmParams {
     int ldy;
     int* err;
 };
-size_t gemm_smem_bytes();
+size_t gemm_smem_bytes(int tiles_per_cta);
 int gemm_rows_pad(int M);
 cudaError_t gemm_set_attributes();
 cudaError_t launch_stage(const StageParams& p, cudaStream_t st);
-cudaError_t launch_gemm(const GemmParams& p, cudaStream_t st);
+cudaError_t launch_gemm(const GemmParams& p, int sms, cudaStream_t st);
 
 // Prefill's per-position attention prologue (kmr_prefill.cu): q/k RMSNorm + M-RoPE of T
 // prompt positions, K/V into cache row `slot` at [start, start + T), queries to q_out.
