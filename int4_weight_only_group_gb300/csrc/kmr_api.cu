@@ -638,9 +638,9 @@ int enqueue_projection(kmr_model* m, const GemvLaunch& g, int T, cudaStream_t st
 }
 
 // Queue one prefill chunk: per layer the QKV projection of all T positions, the q/k norm +
-// M-RoPE + KV write of every position, causal attention as one decode-attention row per
-// position (row i attends 0..start + i of the same cache row), then O, gate_up and down over
-// all positions; the LM head runs on the last position only.
+// M-RoPE + KV write of every position, causal attention (position i attends 0..start + i of
+// the same cache row), then O, gate_up and down over all positions; the LM head runs on the
+// last position only.
 int enqueue_prefill(kmr_model* m, const PrefillArgs& a, cudaStream_t st) {
     const kmr_model_config& c = m->cfg;
     const int T = a.T;
@@ -691,28 +691,21 @@ int enqueue_prefill(kmr_model* m, const PrefillArgs& a, cudaStream_t st) {
             rp.state_fin = a.st_fin;
         }
         if (launch_prefill_rope(rp, st) != cudaSuccess) return KMR_ERR_CUDA;
-        AttnParams ap = {};
-        ap.in = m->pq;
-        ap.in_ld = c.n_q_heads * c.head_dim;
-        ap.fused = 0;
-        ap.kc = rp.kc;
-        ap.vc = rp.vc;
-        ap.slot_ids = m->pslot;
-        ap.cpos = m->pcpos;
-        ap.B = T;
-        ap.nq = c.n_q_heads;
-        ap.nkv = c.n_kv_heads;
-        ap.d = c.head_dim;
-        ap.S = c.max_len;
-        ap.slots = c.slots;
-        ap.scale = 1.0f / sqrtf(float(c.head_dim));
-        ap.tsplit = 1;                   // one CTA per (position, KV head): a whole causal row, no merge
-        ap.cluster = 0;
-        ap.out = m->pattn;
-        ap.err = m->err;
-        // no programmatic overlap here: the attention kernel reads its row state and starts its
-        // K/V copies before griddepcontrol.wait, and the previous kernel has just written both
-        if (launch_attn(ap, st, false) != cudaSuccess) return KMR_ERR_CUDA;
+        // causal attention of every position on the tensor cores
+        PrefillAttnParams pa = {};
+        pa.q = m->pq;
+        pa.kc = rp.kc;
+        pa.vc = rp.vc;
+        pa.slot = a.slot;
+        pa.start = a.start;
+        pa.T = T;
+        pa.nq = c.n_q_heads;
+        pa.nkv = c.n_kv_heads;
+        pa.d = c.head_dim;
+        pa.S = c.max_len;
+        pa.scale = 1.0f / sqrtf(float(c.head_dim));
+        pa.out = m->pattn;
+        if (launch_prefill_attn(pa, st) != cudaSuccess) return KMR_ERR_CUDA;
         g = GemvLaunch{};
         g.w = L.w[KMR_W_O];
         g.g = L.g[KMR_W_O];

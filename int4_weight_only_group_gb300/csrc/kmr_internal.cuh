@@ -355,6 +355,17 @@ struct PrefillRopeParams {
     uint8_t* state_fin;                     // out: 0
 };
 cudaError_t launch_prefill_rope(const PrefillRopeParams& p, cudaStream_t st);
+// Causal attention of a prefill chunk on the tensor cores (kmr_prefill.cu): prompt position i
+// of the chunk attends cache positions [0, start + i] of row `slot`.
+struct PrefillAttnParams {
+    const float* q;                         // [T][nq * d] normalised, rotated queries
+    const uint16_t* kc;                     // one layer [slots][nkv][S][d]
+    const uint16_t* vc;
+    int slot, start, T, nq, nkv, d, S;
+    float scale;
+    float* out;                             // [T][nq * d]
+};
+cudaError_t launch_prefill_attn(const PrefillAttnParams& p, cudaStream_t st);
 
 // KV row migration (kmr_slots.cu): positions [0, length) of one cache row, every layer,
 // K and V, from a source cache to a destination cache of the same L, n_kv and d.

@@ -89,3 +89,232 @@ cudaError_t launch_prefill_rope(const PrefillRopeParams& p, cudaStream_t st) {
 }
 
 }  // namespace kmr
+
+// ---------------------------------------------------------------------------------------------
+// Causal attention of a prefill chunk on the tensor cores ("The Ghost in the Batch", What
+// Attention Does: out = softmax(q K^T / sqrt(d)) V; prompt position i attends cache positions
+// 0..start + i).  Grid (position blocks, KV head): a CTA of 4 warps takes BQ = 4 * 16 / rep
+// consecutive positions and the rep query heads of its KV head; warp w owns 16 query rows
+// (row r: position w * 16 / rep + r / rep, head r % rep).  K and V blocks of 64 positions are
+// double-buffered in shared memory (cp.async, rows padded to d + 8 halves so that ldmatrix is
+// conflict-free); per block a warp forms S = Q K^T (mma.sync bf16, queries rounded to bf16
+// after the scale), applies the causal mask, updates its base-2 online softmax, and adds P V
+// with P rounded to bf16 straight from the S accumulators.
+namespace kmr {
+namespace {
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    return uint32_t(f32_to_bf16_rn(lo)) | (uint32_t(f32_to_bf16_rn(hi)) << 16);
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool fill) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(fill ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+constexpr int kPaBK = 64;                   // key positions per block
+constexpr float kLog2eP = 1.4426950408889634f;
+
+template <int D>
+__host__ __device__ constexpr int pa_pitch() { return D + 8; }  // halves per staged row
+
+template <int D, int REP>
+__global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int PPT = 16 / REP, BQ = 4 * PPT, KT = D / 16, NT = D / 8, P = pa_pitch<D>();
+    uint16_t* ks = reinterpret_cast<uint16_t*>(smem);                       // [2][64][P]
+    uint16_t* vs = ks + 2 * kPaBK * P;                                        // [2][64][P]
+    const int qb = blockIdx.x, h = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int q0 = qb * BQ;
+    const int qlast = min(p.T, q0 + BQ) - 1;                                  // last chunk position here
+    const int kv_end = p.start + qlast + 1;                                   // positions [0, kv_end)
+    const int nkb = (kv_end + kPaBK - 1) / kPaBK;
+    const size_t base = (size_t(p.slot) * p.nkv + h) * p.S * D;
+    const uint16_t* kg = p.kc + base;
+    const uint16_t* vg = p.vc + base;
+
+    auto load_block = [&](int kb, int buf) {
+        constexpr int CPR = D / 8;                                            // 16-byte chunks per row
+        for (int c = tid; c < kPaBK * CPR; c += 128) {
+            const int r = c / CPR, ch = c % CPR, pos = kb * kPaBK + r;
+            const bool ok = pos < kv_end;
+            const size_t src = size_t(ok ? pos : 0) * D + ch * 8;
+            cp_async16(ks + (size_t(buf) * kPaBK + r) * P + ch * 8, kg + src, ok);
+            cp_async16(vs + (size_t(buf) * kPaBK + r) * P + ch * 8, vg + src, ok);
+        }
+        cp_async_commit();
+    };
+    load_block(0, 0);
+
+    // the warp's 16 query rows (g and g + 8 for this lane), scaled to base 2 and rounded to bf16
+    const float qscale = __fmul_rn(p.scale, kLog2eP);
+    int pl[2], hd[2];
+    bool live[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int r = g + 8 * i;
+        pl[i] = q0 + warp * PPT + r / REP;
+        hd[i] = h * REP + r % REP;
+        live[i] = pl[i] < p.T;
+    }
+    uint32_t qf[KT][4];
+#pragma unroll
+    for (int ks_ = 0; ks_ < KT; ++ks_) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float* src = p.q + (size_t(live[i] ? pl[i] : 0) * p.nq + hd[i]) * D + ks_ * 16 + 2 * t;
+            const float2 lo = live[i] ? *reinterpret_cast<const float2*>(src) : make_float2(0.f, 0.f);
+            const float2 hi = live[i] ? *reinterpret_cast<const float2*>(src + 8) : make_float2(0.f, 0.f);
+            qf[ks_][i] = pack_bf16x2(__fmul_rn(lo.x, qscale), __fmul_rn(lo.y, qscale));
+            qf[ks_][2 + i] = pack_bf16x2(__fmul_rn(hi.x, qscale), __fmul_rn(hi.y, qscale));
+        }
+    }
+    float o[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    const int qabs0 = p.start + pl[0], qabs1 = p.start + pl[1];
+    const int lm = lane >> 3, lr = lane & 7;                                  // ldmatrix: matrix, row
+
+    for (int kb = 0; kb < nkb; ++kb) {
+        const int buf = kb & 1;
+        if (kb + 1 < nkb) {
+            load_block(kb + 1, buf ^ 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        const uint16_t* kb_s = ks + size_t(buf) * kPaBK * P;
+        const uint16_t* vb_s = vs + size_t(buf) * kPaBK * P;
+        // ---- S = Q K^T for 64 keys: 8 n-tiles of 8 keys
+        float s[8][4];
+#pragma unroll
+        for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+        for (int ks_ = 0; ks_ < KT; ++ks_) {
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                uint32_t b[4];
+                ldsm_x4(b, kb_s + size_t(np * 16 + (lm >> 1) * 8 + lr) * P + ks_ * 16 + (lm & 1) * 8);
+                mma_bf16(s[2 * np], qf[ks_], b[0], b[1]);
+                mma_bf16(s[2 * np + 1], qf[ks_], b[2], b[3]);
+            }
+        }
+        // ---- causal mask, online softmax (rows g: elements 0, 1; rows g + 8: elements 2, 3)
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int n = 0; n < 8; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int kpos = kb * kPaBK + n * 8 + 2 * t + (e & 1);
+                const int i = e >> 1;
+                if (kpos > (i ? qabs1 : qabs0) || !live[i]) s[n][e] = -INFINITY;
+                mx[i] = fmaxf(mx[i], s[n][e]);
+            }
+        float alpha[2], mref[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
+            mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
+            const float mn = fmaxf(m[i], mx[i]);
+            mref[i] = mn == -INFINITY ? 0.f : mn;
+            alpha[i] = m[i] == -INFINITY ? 0.f : exp2f(__fsub_rn(m[i], mref[i]));
+            m[i] = mn;
+            l[i] = __fmul_rn(l[i], alpha[i]);
+        }
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            o[n][0] = __fmul_rn(o[n][0], alpha[0]);
+            o[n][1] = __fmul_rn(o[n][1], alpha[0]);
+            o[n][2] = __fmul_rn(o[n][2], alpha[1]);
+            o[n][3] = __fmul_rn(o[n][3], alpha[1]);
+        }
+#pragma unroll
+        for (int n = 0; n < 8; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = e >> 1;
+                const float pe = s[n][e] == -INFINITY ? 0.f : exp2f(__fsub_rn(s[n][e], mref[i]));
+                s[n][e] = pe;
+                l[i] = __fadd_rn(l[i], pe);
+            }
+        // ---- O += P V: 4 k-steps of 16 keys; P's A fragment comes from two S tiles
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t a[4] = {pack_bf16x2(s[2 * j][0], s[2 * j][1]), pack_bf16x2(s[2 * j][2], s[2 * j][3]),
+                                   pack_bf16x2(s[2 * j + 1][0], s[2 * j + 1][1]),
+                                   pack_bf16x2(s[2 * j + 1][2], s[2 * j + 1][3])};
+#pragma unroll
+            for (int dp = 0; dp < NT / 2; ++dp) {
+                uint32_t b[4];
+                ldsm_x4_t(b, vb_s + size_t(j * 16 + (lm & 1) * 8 + lr) * P + dp * 16 + (lm >> 1) * 8);
+                mma_bf16(o[2 * dp], a, b[0], b[1]);
+                mma_bf16(o[2 * dp + 1], a, b[2], b[3]);
+            }
+        }
+        __syncthreads();                                                      // the buffer is refilled next
+    }
+    // ---- normalise and store: lane holds dims n * 8 + 2t, +1 of rows g and g + 8
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        float lt = l[i];
+        lt = __fadd_rn(lt, __shfl_xor_sync(0xffffffffu, lt, 1));
+        lt = __fadd_rn(lt, __shfl_xor_sync(0xffffffffu, lt, 2));
+        if (!live[i]) continue;
+        float* dst = p.out + (size_t(pl[i]) * p.nq + hd[i]) * D;
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+            *reinterpret_cast<float2*>(dst + n * 8 + 2 * t) =
+                make_float2(__fdiv_rn(o[n][2 * i], lt), __fdiv_rn(o[n][2 * i + 1], lt));
+    }
+}
+
+template <int D, int REP>
+cudaError_t launch_pa(const PrefillAttnParams& p, cudaStream_t st) {
+    constexpr int BQ = 4 * (16 / REP);
+    const size_t smem = size_t(4) * kPaBK * pa_pitch<D>() * 2;
+    static bool attr = false;
+    if (!attr) {
+        const cudaError_t e = cudaFuncSetAttribute(prefill_attn_kernel<D, REP>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    prefill_attn_kernel<D, REP><<<dim3((p.T + BQ - 1) / BQ, p.nkv), 128, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_attn(const PrefillAttnParams& p, cudaStream_t st) {
+    const int rep = p.nq / p.nkv;
+    if (p.d == 128) {
+        if (rep == 1) return launch_pa<128, 1>(p, st);
+        if (rep == 2) return launch_pa<128, 2>(p, st);
+        return launch_pa<128, 4>(p, st);
+    }
+    if (rep == 1) return launch_pa<64, 1>(p, st);
+    if (rep == 2) return launch_pa<64, 2>(p, st);
+    return launch_pa<64, 4>(p, st);
+}
+
+}  // namespace kmr
