@@ -35,6 +35,11 @@ constexpr int kStageX = kGemmRows * 128 * 2;                 // 32768
 constexpr int kStageS = kGemmRows * 8;                       // 1024: (X', 1/sigma) per row
 constexpr int stage_bytes(int tw) { return tw * kGroupBytes + kStageX + kStageS; }
 
+// A staged row's 16-byte chunks are stored XOR-swizzled by the row's low 3 bits, so that the
+// 8 rows of a row-block, read at the same chunk by the GEMM's B-fragment loads, fall in
+// different shared-memory banks.
+__device__ __forceinline__ int swz(int q, int row) { return (((q >> 3) ^ (row & 7)) << 3) | (q & 7); }
+
 // ---- staging: one CTA per row, 8 warps; warp w takes groups w, w + 8, ...
 __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
     const int row = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -88,8 +93,8 @@ __global__ void __launch_bounds__(256) stage_kernel(const StageParams p) {
         const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
         const float gs = warp_sum(__fadd_rn(__fadd_rn(f01.x, f01.y), __fadd_rn(f23.x, f23.y)));
         __half* blk = xs + (size_t(g) * p.Mpad + row) * 128;
-        *reinterpret_cast<__half2*>(blk + bpos(lane * 4)) = h01;
-        *reinterpret_cast<__half2*>(blk + bpos(lane * 4 + 2)) = h23;
+        *reinterpret_cast<__half2*>(blk + swz(bpos(lane * 4), row)) = h01;
+        *reinterpret_cast<__half2*>(blk + swz(bpos(lane * 4 + 2), row)) = h23;
         if (lane == 0) xst[size_t(g) * p.Mpad + row] = make_float2(gs, isg);
     }
     if (norm) {
@@ -119,20 +124,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const GemmParams 
     const int G = p.K >> 7;
     const int tile0 = blockIdx.x * TW, r0 = blockIdx.y * kGemmRows;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full + kGemmStages;
+    int* released = reinterpret_cast<int*>(smem + 64);          // per stage: warps done with it
     uint8_t* stages = smem + 128;
     if (tid == 0) {
         for (int s = 0; s < kGemmStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kGemmConsumers);
+            released[s] = 0;
         }
         fence_mbar_init();
     }
     __syncthreads();
     const int ntl = min(TW, p.tiles - tile0);                 // tiles this CTA owns (>= 1)
 
-    // the ring is filled by lane 0 of warp 0: groups 0..stages-1 now, group g + stages once
-    // every warp has released group g
+    // the ring: groups 0..stages-1 are requested now; group g + stages by the last warp to
+    // release group g's stage (no warp waits for another)
     auto issue = [&](int g) {
         const int s = g % kGemmStages;
         uint8_t* st = stages + size_t(s) * SB;
@@ -190,12 +195,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const GemmParams 
 #pragma unroll
             for (int rb = 0; rb < RBW; ++rb) {
                 const int rbase = (rb0 + rb) * 8;
-                const __half* xr = xb + size_t(rbase + g8) * 128 + t4 * 16;     // this lane's column
+                const __half* xr = xb + size_t(rbase + g8) * 128;                // this lane's column
                 float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int blk = 0; blk < 2; ++blk) {
-                    const uint4 xa = *reinterpret_cast<const uint4*>(xr + blk * 64);
-                    const uint4 xc = *reinterpret_cast<const uint4*>(xr + blk * 64 + 8);
+                    // chunks blk * 8 + 2 t4 and + 1 of the row, swizzled by the row's low bits (g8)
+                    const uint4 xa = *reinterpret_cast<const uint4*>(xr + (((blk * 8 + 2 * t4) ^ g8) << 3));
+                    const uint4 xc = *reinterpret_cast<const uint4*>(xr + (((blk * 8 + 2 * t4 + 1) ^ g8) << 3));
                     const uint32_t bb[8] = {xa.x, xa.y, xa.z, xa.w, xc.x, xc.y, xc.z, xc.w};
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
@@ -216,10 +222,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const GemmParams 
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if (tid == 0 && g + kGemmStages < G) {
-            // every warp is done with this stage: refill it
-            if (mbar_wait(&empty[s], uint32_t((g / kGemmStages) & 1), p.err)) issue(g + kGemmStages);
+        if (lane == 0 && g + kGemmStages < G) {
+            // this warp's reads of the stage are done (their values are in registers); the
+            // counter only grows, so the warp that completes a multiple of 8 refills the stage
+            __threadfence_block();
+            if (atomicAdd(&released[s], 1) % kGemmConsumers == kGemmConsumers - 1) {
+                __threadfence_block();
+                fence_proxy_async_smem();
+                issue(g + kGemmStages);
+            }
         }
     }
     // ---- epilogue: tile rows g8 ([0..1]) and g8 + 8 ([2..3]) for x rows rbase + 2 t4 (+1)
