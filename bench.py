@@ -491,6 +491,32 @@ def run_reference(args) -> dict:
 
 
 # ------------------------------------------------------------------ main
+def prefill_only(T: int) -> None:
+    """Two kmr_prefill calls of T seeded tokens into slot 0 of the batch-1 model (a fixed
+    command for ncu launch lists of prefill); prints one status line."""
+    import torch
+    import int4_weight_only_group_gb300 as kmr
+    from int4_weight_only_group_gb300 import driver
+    from workloads import SyntheticModel
+    wl = workload(1)
+    cfg = wl.cfg
+    model = kmr.Model.from_config(cfg, max_batch=1)
+    driver.load_weights(model, SyntheticModel(cfg, wl.seed), cfg.n_layers, cfg.qk_norm)
+    T = min(T, cfg.max_len)
+    model.reserve_prefill(T)
+    g = torch.Generator(device="cuda").manual_seed(1)
+    toks = torch.randint(1, cfg.vocab - 1, (T,), generator=g, device="cuda", dtype=torch.int32)
+    pos = torch.arange(T, dtype=torch.int32, device="cuda").repeat(3, 1).contiguous()
+    st = [torch.zeros(1, dtype=torch.int32, device="cuda"), torch.zeros(3, dtype=torch.int32, device="cuda"),
+          torch.zeros(1, dtype=torch.int32, device="cuda"), torch.zeros(1, dtype=torch.uint8, device="cuda")]
+    for _ in range(2):
+        model.prefill(toks, pos, T, 0, 0, *st)
+    torch.cuda.synchronize()
+    assert model.sync_status() == 0
+    model.close()
+    print(json.dumps({"prefill_tokens": T, "calls": 2, "status": "ok"}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -501,7 +527,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-extras", action="store_true",
                     help="time only the decode steps (no standalone GEMV timing, e2e or CPU legs; for launch lists)")
+    ap.add_argument("--prefill-only", type=int, default=0, metavar="T",
+                    help="only run two T-token prefills on the batch-1 model and exit (for profiling)")
     args = ap.parse_args()
+    if args.prefill_only:
+        prefill_only(args.prefill_only)
+        return
     if args.skip_extras:
         args.no_cpu_baseline = True
     if args.warmup < 3:
