@@ -11,8 +11,10 @@
 //      warp per row at a time; each (row, query head, split) leaves an unnormalised state
 //      (m, l, o) in base 2 in the workspace.  The prefix is read from HBM once per call,
 //      not once per row.
-//   2. suffix + merge: grid (KV head, row).  A CTA streams the row's own positions through
-//      a two-stage ring (8 warps x 8 positions per stage), then merges, for each output,
+//   2. suffix + merge: grid (KV head, row), launched as a programmatic dependent of the prefix
+//      pass so that the two run together.  A CTA streams the row's own positions through
+//      a two-stage ring (8 warps x 8 positions per stage), waits for the prefix pass
+//      (griddepcontrol.wait), then merges, for each output,
 //      the prefix split states in split order followed by its 8 warp states in warp order,
 //      and divides.  The prefix split plan depends only on P and the KV head count, so a
 //      row's result does not depend on which other rows share the call.
@@ -125,6 +127,7 @@ __global__ void __launch_bounds__(kCasThreads) cascade_prefix_kernel(const Casca
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_launch_dependents();                    // the suffix pass needs the states only at its merge
     if (tid == 0) {
         const size_t base = ((size_t(p.prefix_slot) * p.nkv + h) * p.S + c0) * D;
         const uint32_t bytes = uint32_t(n) * D * 2;
@@ -230,6 +233,7 @@ __global__ void __launch_bounds__(kCasThreads) cascade_suffix_kernel(const Casca
         for (int e = 0; e < EPL; ++e) wo[(warp * REP + hh) * D + lane * EPL + e] = o[hh][e];
     }
     __syncthreads();
+    pdl_wait();                                 // the prefix pass's states are complete from here
     // merge: prefix split states in split order, then the 8 warp states in warp order
     for (int i = tid; i < REP * D; i += kCasThreads) {
         const int hh = i / D, dim = i % D;
@@ -277,8 +281,19 @@ cudaError_t launch_cascade_t(const CascadeParams& p, cudaStream_t st) {
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    cascade_suffix_kernel<D, REP><<<dim3(p.nkv, p.B), kCasThreads, suffix_smem<D, REP>(), st>>>(p);
-    return cudaGetLastError();
+    // the suffix pass overlaps the prefix pass (programmatic dependent launch) and waits for it
+    // only before its merge
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.nkv, p.B);
+    cfg.blockDim = dim3(kCasThreads);
+    cfg.dynamicSmemBytes = suffix_smem<D, REP>();
+    cfg.stream = st;
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = la;
+    cfg.numAttrs = p.prefix_len > 0 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, cascade_suffix_kernel<D, REP>, p);
 }
 
 }  // namespace
