@@ -132,14 +132,20 @@ class SlotPool:
 
 @dataclasses.dataclass
 class Request:
-    """One admitted generation: its prompt's KV state is written into the slot it gets by
-    `load_kv(model, slot, stream)` (for instance a copy_row_from of a prefilled row)."""
+    """One generation.  Either its prompt's KV state is already prefilled elsewhere and
+    `load_kv(model, slot, stream)` writes it into the slot it gets (for instance a
+    copy_row_from of a prefilled row; decoding starts from `first_token` at cache position
+    `length`), or `prompt` holds the prompt's token ids and the slot is prefilled on
+    admission (kmr_prefill; the prefill's greedy token is the first generated token, and
+    `first_token` / `length` / `load_kv` are ignored).  Text M-RoPE ids are the cache position
+    plus `rope_delta` on all three axes."""
     rid: Any
-    first_token: int                 # token fed to the first decode step
-    length: int                      # prefilled positions = cache_position of the first step
-    rope_delta: int                  # M-RoPE ids of a text token: cache_position + rope_delta on all 3 axes
+    first_token: int
+    length: int
+    rope_delta: int
     max_new_tokens: int
-    load_kv: Callable[..., None]
+    load_kv: Optional[Callable[..., None]] = None
+    prompt: Optional[Sequence[int]] = None
 
 
 def generate_continuous(model: Model, requests: Sequence[Request], n_slots: int, eos_id: int = -1,
@@ -173,6 +179,14 @@ def _continuous(model, requests, n_slots, eos_id, stream, device):
     queue = collections.deque(requests)
     live: Dict[int, List[Any]] = {}               # row -> [request, produced tokens]
     out: Dict[Any, List[int]] = {}
+
+    def finalize(row, req, got):
+        if eos_id >= 0 and eos_id in got:
+            got = got[:got.index(eos_id) + 1]
+        out[req.rid] = got
+        fin[row] = 1
+        pool.release(row)
+
     while queue or live:
         while queue and pool.n_free:
             req = queue.popleft()
@@ -180,6 +194,22 @@ def _continuous(model, requests, n_slots, eos_id, stream, device):
                 out[req.rid] = []
                 continue
             row = pool.admit(req.rid)
+            if req.prompt is not None:
+                # prefill the prompt into the slot; the row's state becomes the first decode step's
+                T = len(req.prompt)
+                ptok = torch.tensor(np.asarray(req.prompt, np.int32), device=device)
+                ppos = (torch.arange(T, dtype=torch.int32, device=device) + req.rope_delta).repeat(3, 1).contiguous()
+                spos = torch.empty(3, dtype=torch.int32, device=device)
+                model.reserve_prefill(T)
+                model.prefill(ptok, ppos, T, row, 0, tok[row:row + 1], spos, cpos[row:row + 1], fin[row:row + 1],
+                              None, stream)
+                pos[:, row] = spos
+                first = int(tok[row].item())
+                if bool(fin[row].item()) or req.max_new_tokens == 1:
+                    finalize(row, req, [first])
+                    continue
+                live[row] = [req, [first]]
+                continue
             req.load_kv(model, row, stream)
             p = req.length + req.rope_delta
             tok[row] = req.first_token
@@ -196,10 +226,6 @@ def _continuous(model, requests, n_slots, eos_id, stream, device):
             req, got = live[row]
             got.append(int(t_h[row]))
             if f_h[row] or len(got) >= req.max_new_tokens:
-                if eos_id >= 0 and eos_id in got:
-                    got = got[:got.index(eos_id) + 1]
-                out[req.rid] = got
-                fin[row] = 1
                 del live[row]
-                pool.release(row)
+                finalize(row, req, got)
     return out

@@ -98,3 +98,38 @@ def test_continuous_row_state_written_at_admission():
     assert seen["cpos"].tolist() == [20, 30, 0]
     assert np.array_equal(seen["pos"].numpy(), np.array([[15, 32, 0]] * 3))
     assert seen["fin"].tolist() == [0, 0, 1]                 # the empty row is a finished row
+
+
+class FakePrefillModel(FakeModel):
+    """FakeModel plus a scripted prefill: the first token of slot s is 50 + s, the row state
+    advances to the first decode step's (cache position T, ids last + 1)."""
+
+    def __init__(self, *a, **kw):
+        super().__init__(*a, **kw)
+        self.prefilled = []
+
+    def reserve_prefill(self, T):
+        pass
+
+    def prefill(self, ptok, ppos, T, slot, start, st_tok, st_pos, st_cpos, st_fin, logits, stream):
+        self.prefilled.append((slot, T, ptok.tolist(), ppos[:, -1].tolist()))
+        self.age[slot] = 0
+        st_tok[0] = 50 + slot
+        st_pos.copy_(ppos[:, -1] + 1)
+        st_cpos[0] = start + T
+        st_fin[0] = 1 if start + T >= self.max_len else 0
+
+
+def test_continuous_prefills_prompts_on_admission():
+    eos, pad = 99, 0
+    m = FakePrefillModel({s: (lambda a: 10 + a) for s in range(2)}, eos, pad, 64)
+    reqs = [Request("p", 0, 0, 2, 3, prompt=[7, 8, 9]),
+            Request("q", 0, 0, -1, 1, prompt=[4]),                  # one token: the prefill's alone
+            Request("r", 0, 0, 0, 2, prompt=list(range(64))),      # fills the row: finished at once
+            Request("s", 0, 0, 0, 2, prompt=[5, 6])]
+    out = generate_continuous(m, reqs, n_slots=2, eos_id=eos, device="cpu")
+    # p: prefill token 50 (slot 0), then decode 10, 11; q: 51 alone (slot 1); r: slot 1, full;
+    # s: slot 1 after r, 51 then 10
+    assert out == {"p": [50, 10, 11], "q": [51], "r": [51], "s": [51, 10]}
+    assert m.prefilled[0] == (0, 3, [7, 8, 9], [4, 4, 4])      # ids = position + rope_delta
+    assert [x[0] for x in m.prefilled] == [0, 1, 1, 1]

@@ -180,3 +180,55 @@ def test_continuous_batching_matches_each_request_alone(torch):
             st = (res.next_ids, res.positions, res.cache_position, st[3], res.finished)
     m.close()
     solo.close()
+
+
+def test_continuous_batching_prefills_prompts_on_admission(torch):
+    """Requests that carry their prompt: each is prefilled into its slot on admission and
+    decoded in the shared batch.  Every request's tokens equal that request prefilled and
+    decoded alone on the GPU, and agree with the oracle's prefill + steps under the gap rule."""
+    cfg = tiny_config(slots=2)
+    seed = 3
+    syn = SyntheticModel(cfg, seed)
+    rng = np.random.default_rng(11)
+    lengths = [12, 1, 57, 30, 128]
+    deltas = [0, 4, -7, 0, 2]
+    budgets = [5, 3, 1, 7, 4]
+    prompts = [rng.integers(1, cfg.vocab - 1, size=n).astype(np.int32) for n in lengths]
+    m = kmr.Model.from_config(cfg, max_batch=2)
+    driver.load_weights(m, syn, cfg.n_layers, cfg.qk_norm)
+    reqs = [driver.Request(r, 0, 0, deltas[r], budgets[r], prompt=prompts[r].tolist()) for r in range(len(lengths))]
+    out = driver.generate_continuous(m, reqs, n_slots=2, eos_id=cfg.eos_id)
+    assert sorted(out) == list(range(len(lengths)))
+
+    solo = kmr.Model.from_config(cfg, max_batch=1)
+    driver.load_weights(solo, syn, cfg.n_layers, cfg.qk_norm)
+    solo.reserve_prefill(max(lengths))
+    for r, T in enumerate(lengths):
+        tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+        spos = torch.zeros(3, dtype=torch.int32, device="cuda")
+        cpos = torch.zeros(1, dtype=torch.int32, device="cuda")
+        fin = torch.zeros(1, dtype=torch.uint8, device="cuda")
+        p = np.arange(T, dtype=np.int32) + deltas[r]
+        solo.prefill(torch.from_numpy(prompts[r]).cuda(), torch.from_numpy(np.stack([p, p, p])).cuda(), T, 0, 0,
+                     tok, spos, cpos, fin, None)
+        first = int(tok.cpu()[0])
+        got = [first]
+        if budgets[r] > 1 and not int(fin.cpu()[0]):
+            st = driver.DeviceState([first], spos.cpu().numpy().reshape(3, 1), [T], [0])
+            got += driver.generate(solo, st, budgets[r] - 1, eos_id=cfg.eos_id)[0]
+        if cfg.eos_id in got:
+            got = got[:got.index(cfg.eos_id) + 1]
+        assert got == out[r], (r, got, out[r])
+
+    for r, T in enumerate(lengths):
+        o = od.OracleDecoder(cfg, seed)
+        p = np.arange(T, dtype=np.int32) + deltas[r]
+        res = o.prefill(prompts[r], np.stack([p, p, p]), 0, 0)
+        for t, tok in enumerate(out[r]):
+            if tok != int(res.next_ids[0]):
+                assert greedy_agrees(tok, res.logits[0]), (r, t)
+                break
+            st = (res.next_ids, res.positions, res.cache_position, np.array([0], np.int32), res.finished)
+            res = o.step(*st)
+    m.close()
+    solo.close()
