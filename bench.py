@@ -3,6 +3,8 @@
 28-layer 2B-shaped decoder on one GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--batch 1|4|16] [--impl kmr|reference]
+    python bench.py --sweep          # standalone int4 GEMV / decode-attention sweeps
+    python bench.py --prefill-only T # two T-token prefills (a fixed command for launch lists)
 
 A step is one pass of the whole decode path (every layer's int4 QKV / O /
 gate_up / down GEMVs, q/k norm, M-RoPE, KV write and GQA attention, final
@@ -256,6 +258,32 @@ def run_kmr(args, rank: int, world: int) -> dict:
     return out
 
 
+def launch_time_us(torch, fn, copies: int, reps: int) -> float:
+    """Mean CUDA-event microseconds per call of fn(i % copies) over `reps` back-to-back calls on
+    the current stream, after warm-up.  A sleep kernel holds the stream while the host queues
+    the calls, so the events see the launches' own device time, not the host's rate of issuing
+    them (a Python-side call costs several microseconds, more than a small launch runs)."""
+    stream = torch.cuda.current_stream()
+    for i in range(max(3, copies)):
+        fn(i % copies)
+    torch.cuda.synchronize()
+    hold = torch.cuda.Event(enable_timing=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    hold.record(stream)
+    torch.cuda._sleep(int(2e6 + reps * 60e3))           # ~1 ms + 30 us per queued call at ~2 GHz
+    e0.record(stream)
+    t0 = time.perf_counter()
+    for i in range(reps):
+        fn(i % copies)
+    t_host = time.perf_counter() - t0
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if t_host * 1e3 > hold.elapsed_time(e0):
+        print(f"launch_time_us: queueing took {t_host * 1e3:.2f} ms, longer than the hold; "
+              "the figure includes host issue time", file=sys.stderr)
+    return e0.elapsed_time(e1) * 1e3 / reps
+
+
 def time_prefill(torch, model, cfg, T: int = 512, reps: int = 3) -> dict:
     """CUDA-event time of kmr_prefill of a T-token prompt (one chunk) into cache row 0: every
     layer's int4 projections over T rows (16-row passes), the q/k norm + M-RoPE + KV write of
@@ -341,24 +369,16 @@ def time_cascade(torch, kmr, cfg, B: int = 16, P: int = 400, own: int = 100, cop
     nbytes = {"cascade": (P + B * own) * row, "plain": B * (P + own) * row}
     res = {"rows": B, "prefix": P, "own": own}
     for name, fn in runs.items():
-        for i in range(3):
-            fn(caches[i % copies])
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(reps):
-            fn(caches[i % copies])
-        e1.record(stream)
-        torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / reps
+        us = launch_time_us(torch, lambda i: fn(caches[i]), copies, reps)
         res[name] = {"us": us, "kv_bytes": nbytes[name], "gbs": nbytes[name] / (us * 1e3)}
     assert kmr.kmr_last_device_error() == 0
     return res
 
 
 def time_gemv(torch, kmr, syn, cfg, M: int) -> dict:
-    """Average CUDA-event duration of one int4 GEMV launch per projection shape, rotating
-    through distinct packed copies (> 2x L2 in total) so every launch streams from HBM."""
+    """Average CUDA-event duration of one int4 GEMV launch per projection shape (launches queued
+    behind a hold, see launch_time_us), rotating through distinct packed copies (> 2x L2 in
+    total) so every launch streams from HBM."""
     res = {}
     stream = torch.cuda.current_stream()
     for name, (N, K) in cfg.linear_shapes().items():
@@ -373,17 +393,8 @@ def time_gemv(torch, kmr, syn, cfg, M: int) -> dict:
         x = torch.randn((M, K), device="cuda")
         epi = kmr.KMR_EPI_SILU_MUL if name == "gate_up" else kmr.KMR_EPI_NONE
         y = torch.zeros((M, N), device="cuda")
-        for i in range(copies):
-            kmr.kmr_int4_gemv(bufs[i], N, K, 128, flags, x, M, y, epi, stream)
-        torch.cuda.synchronize()
-        reps = 200
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(reps):
-            kmr.kmr_int4_gemv(bufs[i % copies], N, K, 128, flags, x, M, y, epi, stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) * 1000.0 / reps
+        us = launch_time_us(torch, lambda i: kmr.kmr_int4_gemv(bufs[i], N, K, 128, flags, x, M, y, epi, stream),
+                            copies, 200)
         nbytes = size
         res[name] = {"us": us, "bytes": nbytes, "gbs": nbytes / us / 1e3, "copies": copies}
         del bufs, one
@@ -490,6 +501,71 @@ def run_reference(args) -> dict:
             "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ------------------------------------------------------------------ kernel sweeps
+GEMV_SWEEP_SHAPES = [(4096, 2048), (2048, 2048), (12288, 2048), (2048, 6144), (151936, 2048)]   # (N out, K in)
+ATTN_SWEEP = [(B, L) for B in (1, 4, 16) for L in (256, 1024, 4096, 8192)]
+
+
+def sweep() -> None:
+    """Standalone kernel sweeps of the measurement plan: kmr_int4_gemv at M in {1,2,4,8,16}
+    over the decoder's projection shapes and the int4 vocabulary shape, and kmr_decode_attn
+    (16 q / 8 kv heads x 128) at B in {1,4,16} rows x {256,1024,4096,8192} cached positions
+    (every row full).  Each point rotates through enough distinct weight / cache copies to
+    exceed L2 by 2x, so every launch streams from HBM.  Prints one JSON line: per point the
+    algorithmic bytes, mean launch time and achieved GB/s against the measured copy bandwidth."""
+    import math
+    import torch
+    import int4_weight_only_group_gb300 as kmr
+    peak = measured_peaks()
+    hbm = peak["hbm_gbs"]
+    stream = torch.cuda.current_stream()
+    g = torch.Generator(device="cuda").manual_seed(0)
+    gemv = []
+    for N, K in GEMV_SWEEP_SHAPES:
+        size = kmr.kmr_packed_size(N, K, 128)
+        q = torch.randint(0, 16, (N, K), generator=g, device="cuda", dtype=torch.uint8)
+        sc = (torch.rand((N, K // 128), generator=g, device="cuda") * 0.018 + 0.002).to(torch.bfloat16).view(torch.int16)
+        z = (torch.randn((N, K // 128), generator=g, device="cuda") * 0.005).to(torch.bfloat16).view(torch.int16)
+        one = torch.empty(size, dtype=torch.uint8, device="cuda")
+        kmr.kmr_pack_int4(q, sc, z, N, K, 128, 0, one, size, 1, stream)
+        del q, sc, z
+        copies = max(4, math.ceil(300e6 / size))
+        bufs = [one] + [one.clone() for _ in range(copies - 1)]
+        for M in (1, 2, 4, 8, 16):
+            x = torch.randn((M, K), generator=g, device="cuda")
+            y = torch.zeros((M, N), device="cuda")
+            us = launch_time_us(torch, lambda i: kmr.kmr_int4_gemv(bufs[i], N, K, 128, 0, x, M, y, kmr.KMR_EPI_NONE,
+                                                                   stream), copies, 100)
+            nbytes = size + M * K * 4 + M * N * 4
+            gemv.append({"N": N, "K": K, "M": M, "bytes": nbytes, "us": round(us, 2),
+                         "gbs": round(nbytes / (us * 1e3), 1), "frac": round(nbytes / (us * 1e3) / hbm, 3)})
+        del bufs, one
+    attn = []
+    nq, nkv, d = 16, 8, 128
+    for B, L in ATTN_SWEEP:
+        per = B * nkv * L * d * 2
+        copies = max(2, math.ceil(300e6 / (2 * per)))
+        caches = [(torch.randn((B, nkv, L, d), generator=g, device="cuda").to(torch.bfloat16).view(torch.int16),
+                   torch.randn((B, nkv, L, d), generator=g, device="cuda").to(torch.bfloat16).view(torch.int16))
+                  for _ in range(copies)]
+        qv = torch.randn((B, nq, d), generator=g, device="cuda")
+        out = torch.empty((B, nq, d), device="cuda")
+        slot_ids = torch.arange(B, dtype=torch.int32, device="cuda")
+        cpos = torch.full((B,), L - 1, dtype=torch.int32, device="cuda")
+        ws = kmr.kmr_decode_attn_workspace_size(B, nq, nkv, d)
+        wsb = torch.zeros(max(ws, 1), dtype=torch.uint8, device="cuda")
+        us = launch_time_us(torch, lambda i: kmr.kmr_decode_attn(qv, caches[i][0], caches[i][1], slot_ids, cpos, B, nq,
+                                                                 nkv, d, L, B, 1.0 / math.sqrt(d), out, wsb, ws,
+                                                                 stream), copies, 50)
+        nbytes = 2 * per
+        attn.append({"B": B, "cached": L, "bytes": nbytes, "us": round(us, 2),
+                     "gbs": round(nbytes / (us * 1e3), 1), "frac": round(nbytes / (us * 1e3) / hbm, 3)})
+        del caches
+    assert kmr.kmr_last_device_error() == 0
+    print(json.dumps({"sweep": {"int4_gemv": gemv, "decode_attn": attn, "peak_gbs": hbm,
+                                "peak_source": peak["source"], "l2": "rotating copies > 2x L2"}}))
+
+
 # ------------------------------------------------------------------ main
 def prefill_only(T: int) -> None:
     """Two kmr_prefill calls of T seeded tokens into slot 0 of the batch-1 model (a fixed
@@ -529,7 +605,12 @@ def main():
                     help="time only the decode steps (no standalone GEMV timing, e2e or CPU legs; for launch lists)")
     ap.add_argument("--prefill-only", type=int, default=0, metavar="T",
                     help="only run two T-token prefills on the batch-1 model and exit (for profiling)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="only run the standalone int4 GEMV and decode-attention sweeps and exit")
     args = ap.parse_args()
+    if args.sweep:
+        sweep()
+        return
     if args.prefill_only:
         prefill_only(args.prefill_only)
         return
