@@ -610,17 +610,34 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
         __syncthreads();
         if (!flag[0]) return;
         const float* parts = p.part + (size_t(b) * p.nkv + h) * p.tsplit * REP * (D + 2);
+        // Every split's (m, l) in one round of independent loads and the merge weights once,
+        // in shared memory (the warp states in wo are consumed); then each output sums its
+        // splits with its own loads in flight together.  Same operations in the same order
+        // as a per-output loop over the splits, so the same bits.
+        float* mq = wo;                                   // [split][head]
+        float* lq = wo + ns * REP;
+        float* wq = wo + 2 * ns * REP;
+        for (int i = tid; i < ns * REP; i += kThreads) {
+            const float* pq = parts + size_t(i) * (D + 2);
+            mq[i] = __ldcg(&pq[0]);
+            lq[i] = __ldcg(&pq[1]);
+        }
+        __syncthreads();
+        for (int i = tid; i < ns * REP; i += kThreads) {
+            const int hh = i % REP;
+            float mx = -INFINITY;
+            for (int q = 0; q < ns; ++q) mx = fmaxf(mx, mq[q * REP + hh]);
+            wq[i] = (mq[i] == -INFINITY) ? 0.f : exp2f(__fsub_rn(mq[i], mx));
+        }
+        __syncthreads();
         for (int i = tid; i < REP * D; i += kThreads) {
             const int hh = i / D, dim = i % D;
-            float mx = -INFINITY;
-            for (int q = 0; q < ns; ++q) mx = fmaxf(mx, __ldcg(&parts[(size_t(q) * REP + hh) * (D + 2)]));
             float num = 0.f, den = 0.f;
+#pragma unroll 8
             for (int q = 0; q < ns; ++q) {
-                const float* pq = parts + (size_t(q) * REP + hh) * (D + 2);
-                const float mq = __ldcg(&pq[0]);
-                const float wt = (mq == -INFINITY) ? 0.f : exp2f(__fsub_rn(mq, mx));
-                den = __fmaf_rn(wt, __ldcg(&pq[1]), den);
-                num = __fmaf_rn(wt, __ldcg(&pq[2 + dim]), num);
+                const float wt = wq[q * REP + hh];
+                den = __fmaf_rn(wt, lq[q * REP + hh], den);
+                num = __fmaf_rn(wt, __ldcg(&parts[(size_t(q) * REP + hh) * (D + 2) + 2 + dim]), num);
             }
             outrow[i] = __fdiv_rn(num, den);
         }
