@@ -129,7 +129,10 @@ size_t kmr_decode_attn_workspace_size(int B, int n_q_heads, int n_kv_heads, int 
  * out = softmax(q K^T / sqrt(d)) V, and the LSE-weighted merge of partial
  * results; "kaminari", §03 StaticKVCache).  Split-KV: each (row, KV head)
  * is cut into position chunks whose partial softmax states are merged in a
- * fixed order; the split plan depends only on the row's own length.
+ * fixed order; the split plan depends only on the row's own length and on
+ * n_kv_heads and max_len (which choose between 8 splits merged inside a
+ * thread-block cluster and up to 32 splits merged through the workspace),
+ * never on B: a row's result does not depend on the other rows.
  *   q        device fp32 [B, n_q, d]
  *   k_cache, v_cache  device bf16 [slots, n_kv, max_len, d] (one layer)
  *   slot_ids device int32 [B]; cache_position device int32 [B]: row b attends

@@ -222,6 +222,11 @@ extern "C" int kmr_decode_attn(const float* q, const uint16_t* k_cache, const ui
     p.slots = slots;
     p.scale = scale;
     p.tsplit = attn_default_tsplit(nkv);
+    // The 8-CTA cluster form (splits merged through distributed shared memory, no global
+    // partials) unless one row's grid would leave most SMs idle on long rows, where the
+    // wider split (one CTA per SM) streams the cache faster.  Chosen from n_kv and max_len
+    // only, never from B, so a row's result does not depend on the batch it is in.
+    p.cluster = (nkv * kAttnClusterSplits >= num_sms() / 2 || max_len <= 4096) ? 1 : 0;
     p.out = out;
     p.part = static_cast<float*>(workspace);
     p.counters = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) +

@@ -238,7 +238,7 @@ def test_decode_attn_single_token_and_determinism(torch):
     assert np.array_equal(out, again)
 
 
-@pytest.mark.parametrize("nkv,S", [(4, 1024), (8, 4096)])   # 8- and 16-position scoring chunks
+@pytest.mark.parametrize("nkv,S", [(4, 1024), (8, 4096), (8, 8192)])   # 8-/16-position chunks; 8192: global merge
 def test_decode_attn_ignores_stale_shared_memory(torch, nkv, S):
     cpos = [0, 6, 15, 16, 70, 127, 1000, S - 1]   # lone last positions, exact splits, ragged tails
     args = (torch, len(cpos), 16, nkv, 128, S, len(cpos), cpos, list(range(len(cpos))))
@@ -247,6 +247,37 @@ def test_decode_attn_ignores_stale_shared_memory(torch, nkv, S):
     for pat in POISON_PATTERNS:
         out, _, err = _attn_case(*args, seed=11, poison=pat)
         assert err == 0 and np.array_equal(out, clean), hex(pat)
+
+
+@pytest.mark.parametrize("S", [1024, 8192])        # cluster-merged splits; workspace-merged splits
+def test_decode_attn_batch_invariant(torch, S):
+    """A row's output is bitwise the same alone (B = 1) and inside a batch of 5, whatever the
+    other rows hold: the split plan depends on the row's length, n_kv and max_len only."""
+    nq, nkv, d, B = 16, 8, 128, 5
+    r = np.random.default_rng(S)
+    cpos = [S - 1, 3, S // 2 + 5, 70, S - 300]
+    kc = f32_to_bf16_bits(r.standard_normal((B, nkv, S, d)).astype(np.float32))
+    vc = f32_to_bf16_bits(r.standard_normal((B, nkv, S, d)).astype(np.float32))
+    q = torch.from_numpy(r.standard_normal((B, nq, d)).astype(np.float32)).cuda()
+    dk = torch.from_numpy(kc.view(np.int16)).cuda()
+    dv = torch.from_numpy(vc.view(np.int16)).cuda()
+
+    def run(rows):
+        n = len(rows)
+        ws_bytes = kmr.kmr_decode_attn_workspace_size(n, nq, nkv, d)
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+        out = torch.zeros((n, nq, d), dtype=torch.float32, device="cuda")
+        kmr.kmr_decode_attn(q[rows].contiguous(), dk, dv, torch.tensor(rows, dtype=torch.int32, device="cuda"),
+                            torch.tensor([cpos[i] for i in rows], dtype=torch.int32, device="cuda"), n, nq, nkv, d,
+                            S, B, 1.0 / math.sqrt(d), out, ws, ws_bytes, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        assert kmr.kmr_last_device_error() == 0
+        return out.cpu().numpy()
+
+    full = run(list(range(B)))
+    for i in range(B):
+        assert np.array_equal(run([i])[0], full[i]), i
+    assert np.array_equal(run([3, 0])[1], full[0])
 
 
 def test_decode_attn_bad_rows_flag_errors(torch):
