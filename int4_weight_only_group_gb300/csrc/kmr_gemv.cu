@@ -102,10 +102,9 @@ __device__ __forceinline__ float norm_factor(const GemvParams& p, const float* s
 }
 
 // Epilogue of one tile: fixed-order sum of the warp partials, RMSNorm factor, store / add / SiLU-mul.
-template <int MB>
+template <int MB, int WS = 16 * MB>                // WS: floats from one warp's partial to the next
 __device__ __forceinline__ void tile_epilogue(const GemvParams& p, const float* ps, int tile, int idx,
                                               const float* ssw, bool have_res = false, float res = 0.f) {
-    constexpr int WS = 16 * MB;                     // floats per warp partial
     if (p.epi == EPI_SILU) {
         if (idx >= 8 * MB) return;
         const int j = idx / MB, m = idx % MB;
@@ -127,27 +126,17 @@ __device__ __forceinline__ void tile_epilogue(const GemvParams& p, const float* 
     }
 }
 
-// Two CTAs per SM (so the next GEMV of the step can be resident and prefetching) where the
-// staging registers allow it.
-// Everything after griddepcontrol.wait for up to MB rows of x: stage x, run the tile products
-// on the resident weight tiles, reduce and apply the epilogue.  Called once per group of MB
-// rows (two calls let a CTA serve 16 rows from one weight fill).
-template <int MB, int GPW>
-__device__ __forceinline__ void gemv_rows(const GemvParams p, uint8_t* smem, const GemvSmem& L, const uint2 (&nwv)[GPW],
-                                          int t0, int nt, int c) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int K = p.K, G = K >> 7, tb = p.tile_bytes, nst = p.nstage;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
-    __half* xw = reinterpret_cast<__half*>(smem + L.xw) + size_t(warp) * GPW * MB * 128;
-    float* xst = reinterpret_cast<float*>(smem + L.xst) + size_t(warp) * GPW * 16;
-    float* ssw = reinterpret_cast<float*>(smem + L.ssw);
-    float* part = reinterpret_cast<float*>(smem + L.part);
-    uint8_t* stages = smem + L.stage;
+// Stage x for this warp's groups: lane l holds inputs 4l..4l+3 of each group.  Loads
+// first, then `pre` (a caller's early global load), then every (group, row)'s arithmetic,
+// then all warp reductions together (independent, so their latencies overlap), then the
+// stores: fp16 halves in B-fragment order (xw), (X', 1/sigma) per (group, row) (xst) and
+// each row's sum of squares (ssw, for the RMSNorm factor).
+template <int MB, int GPW, typename Pre>
+__device__ __forceinline__ void stage_x(const GemvParams& p, __half* xw, float* xst, float* ssw,
+                                        const uint2 (&nwv)[GPW], int c, Pre&& pre) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int K = p.K, G = K >> 7;
     const bool norm = p.in_kind != IN_F32;
-
-    // ---- stage x for this warp's groups: lane l holds inputs 4l..4l+3 of each group.
-    // Loads first, then every (group, row)'s arithmetic, then all warp reductions
-    // together (independent, so their latencies overlap), then the stores.
     float4 xv[GPW][MB];
 #pragma unroll
     for (int j = 0; j < GPW; ++j) {
@@ -171,21 +160,7 @@ __device__ __forceinline__ void gemv_rows(const GemvParams p, uint8_t* smem, con
             }
         }
     }
-    // All tiles fit (the usual case): an EPI_RESID thread fetches its first residual value
-    // (written by an earlier kernel of the step) now, so the epilogue does not wait on L2.
-    const bool fast = nt <= nst;
-    const int per = (p.epi == EPI_SILU ? 8 : 16) * MB;
-    float res0 = 0.f;
-    bool have_res0 = false;
-    if (fast) {
-        if (p.epi == EPI_RESID && tid < nt * per) {
-            const int tl = tid / per, e = tid - tl * per, rr = e / MB, m = e % MB, n = (t0 + tl) * 16 + rr;
-            if (m < p.M && n < p.N) {
-                res0 = p.y[size_t(m) * p.ldy + n];
-                have_res0 = true;
-            }
-        }
-    }
+    pre();
     float ss[MB];
 #pragma unroll
     for (int m = 0; m < MB; ++m) ss[m] = 0.f;
@@ -266,6 +241,41 @@ __device__ __forceinline__ void gemv_rows(const GemvParams p, uint8_t* smem, con
         for (int m = MB; m < 8; ++m) ssw[warp * 8 + m] = 0.f;
     }
     __syncwarp();
+}
+
+// Two CTAs per SM (so the next GEMV of the step can be resident and prefetching) where the
+// staging registers allow it.
+// Everything after griddepcontrol.wait for up to MB rows of x: stage x, run the tile products
+// on the resident weight tiles, reduce and apply the epilogue.  Called once per group of MB
+// rows (two calls let a CTA serve 16 rows from one weight fill).
+template <int MB, int GPW>
+__device__ __forceinline__ void gemv_rows(const GemvParams p, uint8_t* smem, const GemvSmem& L, const uint2 (&nwv)[GPW],
+                                          int t0, int nt, int c) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int K = p.K, G = K >> 7, tb = p.tile_bytes, nst = p.nstage;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
+    __half* xw = reinterpret_cast<__half*>(smem + L.xw) + size_t(warp) * GPW * MB * 128;
+    float* xst = reinterpret_cast<float*>(smem + L.xst) + size_t(warp) * GPW * 16;
+    float* ssw = reinterpret_cast<float*>(smem + L.ssw);
+    float* part = reinterpret_cast<float*>(smem + L.part);
+    uint8_t* stages = smem + L.stage;
+
+    // All tiles fit (the usual case): an EPI_RESID thread fetches its first residual value
+    // (written by an earlier kernel of the step) while x is staged, so the epilogue does not
+    // wait on L2.
+    const bool fast = nt <= nst;
+    const int per = (p.epi == EPI_SILU ? 8 : 16) * MB;
+    float res0 = 0.f;
+    bool have_res0 = false;
+    stage_x<MB, GPW>(p, xw, xst, ssw, nwv, c, [&] {
+        if (fast && p.epi == EPI_RESID && tid < nt * per) {
+            const int tl = tid / per, e = tid - tl * per, rr = e / MB, m = e % MB, n = (t0 + tl) * 16 + rr;
+            if (m < p.M && n < p.N) {
+                res0 = p.y[size_t(m) * p.ldy + n];
+                have_res0 = true;
+            }
+        }
+    });
 
     // ---- products: every warp runs its groups of every tile, no block barrier until the end
     const int g = lane >> 2;
@@ -327,6 +337,72 @@ __device__ __forceinline__ void gemv_rows(const GemvParams p, uint8_t* smem, con
     }
 }
 
+// 16 rows (two halves of 8) on resident tiles when every warp owns exactly one group
+// (K = 2048): both halves are staged and held as x fragments, every weight block is
+// unpacked once for both (group_product2), and each warp leaves its two partials in the
+// block it has just consumed (only that warp reads a block).  Per row the same operations
+// in the same order as one half at a time, so the same bits.
+__device__ __forceinline__ void gemv_rows16(const GemvParams p, uint8_t* smem, const GemvSmem& L,
+                                            const uint2 (&nwv)[1], int t0, int nt, int c) {
+    constexpr int MB = 8;
+    constexpr int PWS = kGroupBytes / 4;           // floats from one warp's partials to the next
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int K = p.K, tb = p.tile_bytes;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
+    __half* xw = reinterpret_cast<__half*>(smem + L.xw) + size_t(warp) * MB * 128;
+    float* xst = reinterpret_cast<float*>(smem + L.xst) + size_t(warp) * 16;
+    float* ssw[2] = {reinterpret_cast<float*>(smem + L.ssw),
+                     reinterpret_cast<float*>(smem + L.part)};     // the partial ring is unused here
+    uint8_t* stages = smem + L.stage;
+    GemvParams h[2] = {p, p};
+    h[0].M = MB;
+    h[1].M = p.M - MB;
+    h[1].x = p.x ? p.x + size_t(MB) * K : nullptr;
+    h[1].tokens = p.tokens ? p.tokens + MB : nullptr;
+    h[1].x_out = p.x_out ? p.x_out + size_t(MB) * K : nullptr;
+    h[1].y = p.y + size_t(MB) * p.ldy;
+    const int per = (p.epi == EPI_SILU ? 8 : 16) * MB;
+    float res0[2] = {0.f, 0.f};
+    bool have_res0[2] = {false, false};
+    const int g = lane >> 2;
+    XFrag xf[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const GemvParams& q = h[hh];
+        stage_x<MB, 1>(q, xw, xst, ssw[hh], nwv, c, [&] {
+            if (q.epi == EPI_RESID && tid < nt * per) {
+                const int tl = tid / per, e = tid - tl * per, rr = e / MB, m = e % MB, n = (t0 + tl) * 16 + rr;
+                if (m < q.M && n < q.N) {
+                    res0[hh] = q.y[size_t(m) * q.ldy + n];
+                    have_res0[hh] = true;
+                }
+            }
+        });
+        const bool bload = g < q.M;
+        load_xfrag(xf[hh], xw + size_t(bload ? g : 0) * 128, bload, lane, xst);
+        __syncwarp();                              // xw / xst are restaged for the second half
+    }
+    mbar_wait(&bar[0], 0u, p.err);
+#pragma unroll 1
+    for (int tl = 0; tl < nt; ++tl) {
+        float acca[4] = {0.f, 0.f, 0.f, 0.f}, accb[4] = {0.f, 0.f, 0.f, 0.f};
+        uint8_t* blk = stages + size_t(tl) * tb + size_t(warp) * kGroupBytes;
+        group_product2(blk, xf[0], xf[1], lane, acca, accb);
+        __syncwarp();                              // every lane's reads of the block are done
+        float* wp = reinterpret_cast<float*>(blk);
+        store_part<MB>(wp, lane, acca);
+        store_part<MB>(wp + 16 * MB, lane, accb);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+        for (int idx = tid; idx < nt * per; idx += kGemvThreads) {
+            const int tl = idx / per;
+            tile_epilogue<MB, PWS>(h[hh], reinterpret_cast<const float*>(stages + size_t(tl) * tb) + hh * 16 * MB,
+                                   t0 + tl, idx - tl * per, ssw[hh], idx == tid && have_res0[hh], res0[hh]);
+        }
+}
+
 template <int MB, int GPW, int NH>
 __global__ void __launch_bounds__(kGemvThreads, (MB * GPW * NH <= 8) ? 2 : 1) gemv_kernel(const GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -373,6 +449,8 @@ __global__ void __launch_bounds__(kGemvThreads, (MB * GPW * NH <= 8) ? 2 : 1) ge
 
     if constexpr (NH == 1) {
         gemv_rows<MB, GPW>(p, smem, L, nwv, t0, nt, c);
+    } else if (GPW == 1 && (K >> 7) == kGemvWarps) {
+        if constexpr (GPW == 1) gemv_rows16(p, smem, L, nwv, t0, nt, c);
     } else {
         // rows [0, MB), then [MB, M) on the same resident weight tiles
         GemvParams q = p;

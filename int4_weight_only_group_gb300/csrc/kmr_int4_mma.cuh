@@ -70,6 +70,30 @@ __device__ __forceinline__ void load_xfrag(XFrag& f, const __half* xb, bool bloa
     f.X = *reinterpret_cast<const float4*>(st + 4 * t);
 }
 
+// Sum of the four k-step chains, then the fold of the group's offset, -8 and zero point for
+// rows g (x1) and g+8 (x16) and batch columns 2t, 2t+1 (ODD = false: column 2t only).
+template <bool ODD>
+__device__ __forceinline__ void fold_group(const uint8_t* gb, int g, const float (&d)[4][4], const float4 X,
+                                           float (&acc)[4]) {
+    float D[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        if (ODD || (i & 1) == 0) D[i] = __fadd_rn(__fadd_rn(d[0][i], d[1][i]), __fadd_rn(d[2][i], d[3][i]));
+    const uint32_t sz0 = *reinterpret_cast<const uint32_t*>(gb + 1024 + g * 4);
+    const uint32_t sz1 = *reinterpret_cast<const uint32_t*>(gb + 1024 + (g + 8) * 4);
+    // X = (X'_{2t}, is_{2t}, X'_{2t+1}, is_{2t+1})
+    const float s0 = bf16_lo(sz0), z0 = bf16_hi(sz0), s1 = bf16_lo(sz1), z1 = bf16_hi(sz1);
+    const float s1c = __fmul_rn(s1, 0.0625f);
+    const float zz0 = __fmaf_rn(-8.f, s0, z0), zz1 = __fmaf_rn(-8.f, s1, z1);
+    const float x0 = 1024.f * X.x, x1 = ODD ? 1024.f * X.z : 0.f;
+    acc[0] = __fmaf_rn(__fmaf_rn(s0, __fsub_rn(D[0], x0), __fmul_rn(zz0, X.x)), X.y, acc[0]);
+    acc[2] = __fmaf_rn(__fmaf_rn(s1c, __fsub_rn(D[2], x0), __fmul_rn(zz1, X.x)), X.y, acc[2]);
+    if (ODD) {
+        acc[1] = __fmaf_rn(__fmaf_rn(s0, __fsub_rn(D[1], x1), __fmul_rn(zz0, X.z)), X.w, acc[1]);
+        acc[3] = __fmaf_rn(__fmaf_rn(s1c, __fsub_rn(D[3], x1), __fmul_rn(zz1, X.z)), X.w, acc[3]);
+    }
+}
+
 // One (16-row tile, 128-input group) block: 8 tensor-core k-steps on four independent
 // accumulator chains, then the fold for rows g (x1) and g+8 (x16) and batch columns
 // 2t, 2t+1.  ODD = false skips the odd columns (one row of x: column 2t+1 never exists).
@@ -91,23 +115,35 @@ __device__ __forceinline__ void group_product(const uint8_t* gb, const XFrag& xf
                      xf.b[blk * 8 + 2 * ks], xf.b[blk * 8 + 2 * ks + 1]);
         }
     }
-    float D[4];
+    fold_group<ODD>(gb, g, d, xf.X, acc);
+}
+
+// The same block against two staged halves of up to 8 rows each (batch rows 0..7 in xa,
+// 8..15 in xb): every weight word is unpacked once and feeds two mma, one per half.  Each
+// half's chains, sums and fold are those of group_product, so each row gets the same bits.
+__device__ __forceinline__ void group_product2(const uint8_t* gb, const XFrag& xa, const XFrag& xb, int lane,
+                                               float (&acca)[4], float (&accb)[4]) {
+    const int g = lane >> 2;
+    float da[4][4], db[4][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        if (ODD || (i & 1) == 0) D[i] = __fadd_rn(__fadd_rn(d[0][i], d[1][i]), __fadd_rn(d[2][i], d[3][i]));
-    const uint32_t sz0 = *reinterpret_cast<const uint32_t*>(gb + 1024 + g * 4);
-    const uint32_t sz1 = *reinterpret_cast<const uint32_t*>(gb + 1024 + (g + 8) * 4);
-    const float4 X = xf.X;                                                // (X'_{2t}, is_{2t}, X'_{2t+1}, is_{2t+1})
-    const float s0 = bf16_lo(sz0), z0 = bf16_hi(sz0), s1 = bf16_lo(sz1), z1 = bf16_hi(sz1);
-    const float s1c = __fmul_rn(s1, 0.0625f);
-    const float zz0 = __fmaf_rn(-8.f, s0, z0), zz1 = __fmaf_rn(-8.f, s1, z1);
-    const float x0 = 1024.f * X.x, x1 = ODD ? 1024.f * X.z : 0.f;
-    acc[0] = __fmaf_rn(__fmaf_rn(s0, __fsub_rn(D[0], x0), __fmul_rn(zz0, X.x)), X.y, acc[0]);
-    acc[2] = __fmaf_rn(__fmaf_rn(s1c, __fsub_rn(D[2], x0), __fmul_rn(zz1, X.x)), X.y, acc[2]);
-    if (ODD) {
-        acc[1] = __fmaf_rn(__fmaf_rn(s0, __fsub_rn(D[1], x1), __fmul_rn(zz0, X.z)), X.w, acc[1]);
-        acc[3] = __fmaf_rn(__fmaf_rn(s1c, __fsub_rn(D[3], x1), __fmul_rn(zz1, X.z)), X.w, acc[3]);
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) da[c][i] = db[c][i] = 0.f;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+        const uint4 wq = *reinterpret_cast<const uint4*>(gb + blk * 512 + lane * 16);
+        const uint32_t w4[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t w = w4[ks], w2 = w >> 8;
+            const uint32_t a0 = and_or(w, 0x000F000Fu, 0x64006400u), a1 = and_or(w, 0x00F000F0u, 0x64006400u);
+            const uint32_t a2 = and_or(w2, 0x000F000Fu, 0x64006400u), a3 = and_or(w2, 0x00F000F0u, 0x64006400u);
+            mma16816(da[ks], a0, a1, a2, a3, xa.b[blk * 8 + 2 * ks], xa.b[blk * 8 + 2 * ks + 1]);
+            mma16816(db[ks], a0, a1, a2, a3, xb.b[blk * 8 + 2 * ks], xb.b[blk * 8 + 2 * ks + 1]);
+        }
     }
+    fold_group<true>(gb, g, da, xa.X, acca);
+    fold_group<true>(gb, g, db, xb.X, accb);
 }
 
 }  // namespace kmr
