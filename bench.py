@@ -96,18 +96,24 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def profile_traffic(kernel_file: str, summary: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current kernel source."""
+def profile_traffic(summary: str):
+    """DRAM bytes per launch from a committed ncu summary, if every source file it names
+    (`kernel_source_sha256: <sha> (<file>), ...`) is unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", summary)
-    src = os.path.join(ROOT, "int4_weight_only_group_gb300", "csrc", kernel_file)
-    if not (os.path.exists(path) and os.path.exists(src)):
+    if not os.path.exists(path):
         return None
     text = open(path).read()
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    m_sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    line = re.search(r"kernel_source_sha256:(.*)", text)
     m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_sha or not m_tr or m_sha.group(1) != sha:
+    if not line or not m_tr:
         return None
+    pairs = re.findall(r"([0-9a-f]{64})\s*\(([\w.]+)\)", line.group(1))
+    if not pairs:
+        return None
+    for sha, name in pairs:
+        src = os.path.join(ROOT, "int4_weight_only_group_gb300", "csrc", name)
+        if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != sha:
+            return None
     return float(m_tr.group(1))
 
 
@@ -647,7 +653,7 @@ def main():
     step_weight_bytes = cfg.n_layers * (wb["qkv"] + wb["o"] + wb["gate_up"] + wb["down"]) + wb["lm_head"] + wb["norms"]
     step_bytes = step_weight_bytes + r["kv_gen"] / wl.steps
     g = r["gemv"]["gate_up"]
-    traffic = profile_traffic("kmr_gemv.cu", "int4_gemv_gate_up.md")
+    traffic = profile_traffic("int4_gemv_gate_up.md")
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
