@@ -290,7 +290,7 @@ def test_head_layouts(torch, nq, nkv, B):
 
 
 def test_sixteen_rows_one_weight_fill(torch):
-    """B = 16 (SURVEY f1): each int4 GEMV serves all 16 rows from one weight fill and the LM head
+    """B = 16: each int4 GEMV serves all 16 rows from one weight fill and the LM head
     takes them in one pass; 2 teacher-forced steps match the oracle and rows 0 and 13 equal
     their batch-1 results bit for bit."""
     from workloads import Workload
