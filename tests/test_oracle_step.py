@@ -145,3 +145,70 @@ def test_oracle_prefill_is_causal_and_chunkable():
     c.prefill(toks[:-1] + [1], pos, 1, 3)                      # only the last token differs
     for l in range(cfg.n_layers):
         assert np.array_equal(a.K[l][1, :, :8], c.K[l][1, :, :8]) and not np.array_equal(a.K[l][1, :, 8], c.K[l][1, :, 8])
+
+
+def _one_layer_with(cfg, edit):
+    """Oracle over layer 0 only, with its int4 linears replaced by edit(name, (q, s, z))."""
+    o = od.OracleDecoder(cfg, seed=0, layers=1)
+    lin = {n: edit(n, tuple(a.copy() for a in o.syn.linear(0, n))) for n in cfg.linear_shapes()}
+    o.syn.linear = lambda layer, name: lin[name]
+    return o, {n: od.dequant_int4(*lin[n], cfg.group) for n in lin}
+
+
+def _zero_rows(qsz, rows):
+    q, s, z = qsz
+    q[rows] = 8                          # (8 - 8) s + 0 = 0 exactly
+    z[rows] = 0
+    return q, s, z
+
+
+def _rms(x, w_bits, eps):
+    return x / np.sqrt(np.mean(x * x) + eps) * od.bf16_to_f64(w_bits)
+
+
+def test_layer_with_zero_q_and_k_attends_uniformly():
+    """W_q = W_k = 0 make every score 0, so each query head's attention is the plain mean of
+    its KV head's cached V rows and the new token's v (bf16, as the cache holds it); with
+    gate_up = 0 the MLP adds nothing.  The layer then has a closed form that fixes how the
+    pieces compose: v from the normed input, the new position included, the query-to-KV-head
+    map, the O projection's head order and the residual."""
+    cfg = tiny_config()
+    qd, kvd, d = cfg.q_dim, cfg.kv_dim, cfg.head_dim
+    rep = cfg.n_q_heads // cfg.n_kv_heads
+    o, W = _one_layer_with(cfg, lambda n, qsz: _zero_rows(qsz, slice(0, qd + kvd)) if n == "qkv"
+                           else (_zero_rows(qsz, slice(None)) if n == "gate_up" else qsz))
+    t, tok = 20, 41
+    o.prefill_cache(0, t)
+    res = o.step(*_state(cpos=t, tok=tok))
+    syn = o.syn
+    E = od.bf16_to_f64(syn.embedding())
+    x0 = E[tok]
+    h = _rms(x0, syn.norm(0, "in"), cfg.eps)
+    v_new = od.bf16_to_f64(od.f64_to_bf16_bits((W["qkv"][qd + kvd:] @ h).reshape(cfg.n_kv_heads, d)))
+    V = np.concatenate([od.bf16_to_f64(syn.kv_prefill(0, 0, t, "v")[:, :t]), v_new[:, None, :]], axis=1)
+    per_kv = V.sum(axis=1) / (t + 1)
+    attn = np.concatenate([per_kv[i // rep] for i in range(cfg.n_q_heads)])
+    x1 = x0 + W["o"] @ attn
+    logits = E @ _rms(x1, syn.norm(-1, "final"), cfg.eps)
+    assert np.allclose(res.logits[0], logits, rtol=1e-11, atol=1e-14)
+    assert np.array_equal(od.bf16_to_f64(o.V[0][0][:, t]), v_new)
+    assert not od.bf16_to_f64(o.K[0][0][:, t]).any()
+
+
+def test_layer_with_zero_attention_is_the_mlp_block():
+    """W_qkv = 0 on an empty row (cache position 0: the new token attends itself, v = 0) leaves
+    the attention block adding 0; the layer is then x + W_down (silu(gate) * up) of the
+    post-attention RMSNorm, gate the first half of gate_up's rows."""
+    cfg = tiny_config()
+    o, W = _one_layer_with(cfg, lambda n, qsz: _zero_rows(qsz, slice(None)) if n == "qkv" else qsz)
+    tok = 300
+    res = o.step(*_state(cpos=0, tok=tok))
+    syn = o.syn
+    E = od.bf16_to_f64(syn.embedding())
+    x0 = E[tok]
+    h2 = _rms(x0, syn.norm(0, "post"), cfg.eps)
+    gu = W["gate_up"] @ h2
+    g, u = gu[:cfg.intermediate], gu[cfg.intermediate:]
+    x2 = x0 + W["down"] @ (g / (1.0 + np.exp(-g)) * u)
+    logits = E @ _rms(x2, syn.norm(-1, "final"), cfg.eps)
+    assert np.allclose(res.logits[0], logits, rtol=1e-11, atol=1e-14)
