@@ -154,6 +154,15 @@ def weight_bytes(cfg) -> dict:
 
 
 # ------------------------------------------------------------------ GPU arm
+def aggregate_ranks(torch, elapsed_ms: float, tokens: float, world: int, device: str):
+    """Whole-job figures of N replicas: the slowest rank's time and the sum of every rank's
+    tokens (each rank decodes its own batch on its own model; no data-path collective)."""
+    t = torch.tensor([elapsed_ms, tokens], dtype=torch.float64, device=device)
+    ts = [torch.zeros_like(t) for _ in range(world)]
+    torch.distributed.all_gather(ts, t)
+    return max(float(x[0]) for x in ts), sum(float(x[1]) for x in ts)
+
+
 def run_kmr(args, rank: int, world: int) -> dict:
     import torch
     import int4_weight_only_group_gb300 as kmr
@@ -235,11 +244,7 @@ def run_kmr(args, rank: int, world: int) -> dict:
     kv_gen = kv_bytes_per_generation(wl)
 
     if world > 1:
-        t = torch.tensor([elapsed_ms, tokens], dtype=torch.float64, device="cuda")
-        ts = [torch.zeros_like(t) for _ in range(world)]
-        torch.distributed.all_gather(ts, t)
-        elapsed_ms = max(float(x[0]) for x in ts)
-        tokens = sum(float(x[1]) for x in ts)
+        elapsed_ms, tokens = aggregate_ranks(torch, elapsed_ms, tokens, world, "cuda")
     if rank != 0:
         return {}
 
