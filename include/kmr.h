@@ -377,6 +377,14 @@ int kmr_model_sync_status(kmr_model* m, void* stream);
  * model's captured step graphs.  Off by default; costs one extra launch per
  * kernel.  Returns KMR_OK, KMR_ERR_INVALID_ARG (null model) or KMR_ERR_CUDA. */
 int kmr_smem_poison(uint32_t pattern, void* stream);
+
+/* Self-test of the bounded device waits (failure detection without a fault):
+ * launches one warp that waits on a shared-memory mbarrier nothing completes.
+ * The wait gives up after limit_ns nanoseconds (1 us .. 2 s), the kernel
+ * returns, and kmr_last_device_error() then reads KMR_ERR_DEVICE_TIMEOUT; the
+ * context stays usable.  Asynchronous on `stream`.  Returns KMR_OK,
+ * KMR_ERR_INVALID_ARG (limit out of range) or KMR_ERR_CUDA. */
+int kmr_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
 int kmr_model_set_smem_poison(kmr_model* m, int enable, uint32_t pattern);
 
 /* Launches one step makes (kernels per step) for the given B, for accounting

@@ -25,7 +25,7 @@ __all__ = [
     "ModelConfig", "kmr_status_string", "kmr_layout_version", "kmr_packed_size", "kmr_pack_int4",
     "kmr_unpack_int4", "kmr_int4_gemv", "kmr_decode_attn_workspace_size",
     "kmr_decode_attn", "kmr_decode_attn_noalloc", "kmr_decode_attn_cascade_workspace_size",
-    "kmr_decode_attn_cascade", "kmr_last_device_error", "kmr_smem_poison", "Model",
+    "kmr_decode_attn_cascade", "kmr_last_device_error", "kmr_smem_poison", "kmr_selftest_wait_timeout", "Model",
 ]
 
 KMR_OK = 0
@@ -105,6 +105,7 @@ _SIGNATURES = {
     "kmr_model_sync_status": (_I, [_P, _P]),
     "kmr_model_kernels_per_step": (_I, [_P, _I]),
     "kmr_smem_poison": (_I, [ctypes.c_uint32, _P]),
+    "kmr_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
     "kmr_model_set_smem_poison": (_I, [_P, _I, ctypes.c_uint32]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
@@ -225,6 +226,12 @@ def kmr_decode_attn_cascade(q, k_cache, v_cache, slot_ids, cache_position, prefi
 
 def kmr_last_device_error() -> int:
     return lib().kmr_last_device_error()
+
+
+def kmr_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Launch the bounded-wait self-test (a wait nothing completes gives up after limit_ns);
+    kmr_last_device_error() then reads KMR_ERR_DEVICE_TIMEOUT."""
+    _check(lib().kmr_selftest_wait_timeout(int(limit_ns), _stream(stream)), "kmr_selftest_wait_timeout")
 
 
 def kmr_smem_poison(pattern: int, stream=None) -> None:

@@ -1083,6 +1083,18 @@ extern "C" int kmr_smem_poison(uint32_t pattern, void* stream) {
                                                                                                  : KMR_ERR_CUDA;
 }
 
+namespace kmr {
+cudaError_t launch_wait_timeout(int* err, unsigned long long limit_ns, cudaStream_t st);   // kmr_poison.cu
+}
+
+extern "C" int kmr_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
+    if (limit_ns < 1000ull || limit_ns > 2000000000ull) return KMR_ERR_INVALID_ARG;
+    int* err = standalone_error_word();
+    if (!err) return KMR_ERR_CUDA;
+    return launch_wait_timeout(err, limit_ns, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KMR_OK
+                                                                                                : KMR_ERR_CUDA;
+}
+
 extern "C" int kmr_model_set_smem_poison(kmr_model* m, int enable, uint32_t pattern) {
     if (!m) return KMR_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(m->mu);

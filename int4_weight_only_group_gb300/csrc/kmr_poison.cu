@@ -5,6 +5,9 @@
 // test that compares a poisoned run with a clean one bitwise turns such a
 // read into a deterministic failure.  Nothing on the decode path depends on
 // it; the model enables it with kmr_model_set_smem_poison.
+//
+// Also here: a self-test of the bounded device waits, which waits on an
+// mbarrier that nothing completes and must give up with a status, not hang.
 #include "kmr_internal.cuh"
 
 namespace kmr {
@@ -25,7 +28,25 @@ __global__ void __launch_bounds__(kPoisonThreads, 1) poison_kernel(uint32_t patt
     __syncthreads();
 }
 
+// One warp waits on a freshly initialised mbarrier that expects one arrival which never
+// comes (no copy is in flight, so nothing is left pending when the kernel exits).  Every
+// lane's bounded wait gives up after limit_ns and records KMR_ERR_DEVICE_TIMEOUT.
+__global__ void __launch_bounds__(32, 1) wait_timeout_kernel(int* err, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    mbar_wait(&bar, 0u, err, limit_ns);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout(int* err, unsigned long long limit_ns, cudaStream_t st) {
+    wait_timeout_kernel<<<1, 32, 0, st>>>(err, limit_ns);
+    return cudaGetLastError();
+}
 
 cudaError_t poison_set_attributes() {
     return cudaFuncSetAttribute(poison_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kPoisonBytes));

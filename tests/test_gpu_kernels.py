@@ -295,3 +295,23 @@ def test_decode_attn_bad_rows_flag_errors(torch):
                             ws, ws_bytes)
         assert kmr.kmr_last_device_error() == code
         assert float(res[1].abs().sum()) == 0.0         # the bad row is zeroed, not read
+
+
+def test_bounded_wait_gives_up_with_a_status(torch):
+    """Failure detection without a fault: a device wait that nothing completes gives up after
+    its limit and reports KMR_ERR_DEVICE_TIMEOUT through the error word; the context stays
+    usable (a GEMV afterwards still matches the oracle)."""
+    import time
+    assert kmr.kmr_last_device_error() == 0
+    t0 = time.perf_counter()
+    kmr.kmr_selftest_wait_timeout(2_000_000)                       # 2 ms
+    assert kmr.kmr_last_device_error() == kmr.KMR_ERR_DEVICE_TIMEOUT
+    assert time.perf_counter() - t0 < 10.0
+    assert kmr.kmr_last_device_error() == 0                        # reading clears the word
+    with pytest.raises(kmr.KmrError):
+        kmr.kmr_selftest_wait_timeout(10)                          # limit below 1 us: refused on the host
+    q, s, z = _canon(3, 64, 256)
+    x = np.random.default_rng(3).standard_normal((2, 256)).astype(np.float32)
+    y = _gemv(torch, _device_pack(torch, q, s, z), 64, 256, x)
+    assert rel_l2(y, od.int4_linear(x.astype(np.float64), q, s, z, 128)) <= REL_L2_TOL
+    assert kmr.kmr_last_device_error() == 0
