@@ -163,6 +163,11 @@ def generate_continuous(model: Model, requests: Sequence[Request], n_slots: int,
     the steps and the reads are ordered on it."""
     import contextlib
     import torch
+    for req in requests:
+        if req.prompt is not None and len(req.prompt) == 0:
+            raise ValueError(f"request {req.rid!r}: empty prompt")
+        if req.prompt is None and req.load_kv is None and req.max_new_tokens > 0:
+            raise ValueError(f"request {req.rid!r}: needs a prompt or a load_kv callback")
     with torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext():
         return _continuous(model, requests, n_slots, eos_id, stream, device)
 

@@ -133,3 +133,12 @@ def test_continuous_prefills_prompts_on_admission():
     assert out == {"p": [50, 10, 11], "q": [51], "r": [51], "s": [51, 10]}
     assert m.prefilled[0] == (0, 3, [7, 8, 9], [4, 4, 4])      # ids = position + rope_delta
     assert [x[0] for x in m.prefilled] == [0, 1, 1, 1]
+
+
+def test_continuous_rejects_requests_without_a_kv_source():
+    m = FakePrefillModel({0: (lambda a: 10)}, 99, 0, 64)
+    with pytest.raises(ValueError, match="empty prompt"):
+        generate_continuous(m, [Request("e", 0, 0, 0, 2, prompt=[])], n_slots=1, device="cpu")
+    with pytest.raises(ValueError, match="prompt or a load_kv"):
+        generate_continuous(m, [Request("n", 0, 0, 0, 2)], n_slots=1, device="cpu")
+    assert m.prefilled == [] and m.ticks == 0                 # nothing ran
