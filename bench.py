@@ -261,6 +261,9 @@ def run_kmr(args, rank: int, world: int) -> dict:
     out["kv_copy"] = time_kv_copy(torch, model, cfg)
     # ---- text prefill of a 512-token prompt into slot 0 (after the timed decode region)
     out["prefill"] = time_prefill(torch, model, cfg)
+    model.set_prefill_tcgen05(True)                 # the tensor-core (tcgen05) projections, for comparison
+    out["prefill_tcgen05"] = time_prefill(torch, model, cfg)
+    model.set_prefill_tcgen05(False)
     # ---- shared-prefix attention vs plain attention on the same contexts
     out["cascade"] = time_cascade(torch, kmr, cfg)
     model.close()
@@ -682,7 +685,8 @@ def main():
                          "cascade_kv_bytes": r["cascade"]["cascade"]["kv_bytes"],
                          "plain_kv_bytes": r["cascade"]["plain"]["kv_bytes"]},
         "prefill": {"tokens": r["prefill"]["tokens"], "ms": round(r["prefill"]["ms"], 3),
-                    "tok_s": round(r["prefill"]["tok_s"], 1)},
+                    "tok_s": round(r["prefill"]["tok_s"], 1),
+                    "tcgen05_ms": round(r["prefill_tcgen05"]["ms"], 3)},
         "kv_row_copy": {"us": round(r["kv_copy"]["us"], 2), "gbs": round(r["kv_copy"]["gbs"], 1),
                         "frac": round(r["kv_copy"]["gbs"] / peaks["hbm_gbs"], 3), "bytes": r["kv_copy"]["bytes"]},
         "gpu_launches": r["kernels_per_step"] * args.steps,

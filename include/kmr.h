@@ -387,6 +387,17 @@ int kmr_smem_poison(uint32_t pattern, void* stream);
 int kmr_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
 int kmr_model_set_smem_poison(kmr_model* m, int enable, uint32_t pattern);
 
+/* Prefill projections on the 5th-generation tensor cores.  With enable = 1,
+ * kmr_prefill runs every projection whose output rows are a multiple of 128
+ * as a tcgen05.mma kernel: the group's int4 weights dequantised to fp16 in
+ * shared memory, the staged tokens as fp16 scaled by a per-row power of two,
+ * fp32 accumulation in tensor memory across all of K.  Results agree with the
+ * default (legacy warp-level mma) prefill within rounding and are
+ * parity-tested against the oracle the same way; the default stays the
+ * warp-level kernel, which is faster today.  Takes effect from the next
+ * kmr_prefill call.  Returns KMR_OK or KMR_ERR_INVALID_ARG (null model). */
+int kmr_model_set_prefill_tcgen05(kmr_model* m, int enable);
+
 /* Launches one step makes (kernels per step) for the given B, for accounting
  * (twice as many while shared-memory poisoning is on). */
 int kmr_model_kernels_per_step(const kmr_model* m, int B);

@@ -107,6 +107,7 @@ _SIGNATURES = {
     "kmr_smem_poison": (_I, [ctypes.c_uint32, _P]),
     "kmr_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
     "kmr_model_set_smem_poison": (_I, [_P, _I, ctypes.c_uint32]),
+    "kmr_model_set_prefill_tcgen05": (_I, [_P, _I]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
 
@@ -336,6 +337,10 @@ class Model:
 
     def kernels_per_step(self, B: int) -> int:
         return lib().kmr_model_kernels_per_step(self._h, B)
+
+    def set_prefill_tcgen05(self, enable: bool) -> None:
+        """kmr_model_set_prefill_tcgen05: run prefill projections on the tcgen05 kernel."""
+        _check(lib().kmr_model_set_prefill_tcgen05(self._h, int(bool(enable))), "kmr_model_set_prefill_tcgen05")
 
     def set_smem_poison(self, enable: bool, pattern: int = 0xFFFFFFFF) -> None:
         """Precede every kernel of the step with a shared-memory fill of `pattern` (diagnostic)."""

@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "kmr_internal.cuh"
+#include "kmr_tcgemm.cuh"
 
 namespace kmr {
 int pack_run(const uint8_t* q, const uint16_t* s, const uint16_t* z, int N, int K, int group, int flags,
@@ -58,6 +59,7 @@ cudaError_t ensure_kernel_attributes() {
     if ((e = attn_set_attributes()) != cudaSuccess) return e;
     if ((e = poison_set_attributes()) != cudaSuccess) return e;
     if ((e = gemm_set_attributes()) != cudaSuccess) return e;
+    if ((e = tc_gemm_set_attributes()) != cudaSuccess) return e;
     done[dev] = true;
     return cudaSuccess;
 }
@@ -353,6 +355,7 @@ struct kmr_model {
     std::vector<GraphEntry> graphs;
     unsigned long long tick = 0;
     bool poison = false;           // diagnostic: fill shared memory before every kernel of the step
+    bool prefill_tc = false;       // prefill projections on tcgen05 (kmr_model_set_prefill_tcgen05)
     // prefill scratch for chunks of up to prefill_cap positions (kmr_model_reserve_prefill)
     int prefill_cap = 0;
     float* px = nullptr;           // residual rows [cap][H]
@@ -608,6 +611,39 @@ struct PrefillArgs {
 // One int4 projection of all T rows of a prefill chunk: stage the rows once, then the
 // weight-stationary GEMM (each unpacked weight fragment serves 64 rows).
 int enqueue_projection(kmr_model* m, const GemvLaunch& g, int T, cudaStream_t st) {
+    if (m->prefill_tc && tc_gemm_supported(g.g.N, g.g.K)) {
+        // 5th-generation tensor cores: staged tokens (fp16, per-row power of two) x dequantised
+        // fp16 weights, fp32 accumulators in tensor memory
+        TcStageParams tp = {};
+        tp.in_kind = g.in_kind;
+        tp.x = g.x;
+        tp.embed = g.embed;
+        tp.tokens = g.tokens;
+        tp.vocab = g.vocab;
+        tp.x_out = g.x_out;
+        tp.norm_w = g.norm_w;
+        tp.eps = g.eps;
+        tp.M = T;
+        tp.K = g.g.K;
+        tp.nt = tc_gemm_pick_nt(g.g.N, T, m->sms);
+        tp.xs = m->pxs;
+        tp.rs = m->prn;
+        tp.err = m->err;
+        if (launch_tc_stage(tp, st) != cudaSuccess) return KMR_ERR_CUDA;
+        TcGemmParams tg = {};
+        tg.w = g.w;
+        tg.N = g.g.N;
+        tg.K = g.g.K;
+        tg.xs = m->pxs;
+        tg.rs = m->prn;
+        tg.M = T;
+        tg.nt = tp.nt;
+        tg.epi = g.epi;
+        tg.y = g.y;
+        tg.ldy = g.ldy;
+        tg.err = m->err;
+        return launch_tc_gemm(tg, st) == cudaSuccess ? KMR_OK : KMR_ERR_CUDA;
+    }
     StageParams sp = {};
     sp.in_kind = g.in_kind;
     sp.x = g.x;
@@ -1093,6 +1129,13 @@ extern "C" int kmr_selftest_wait_timeout(unsigned long long limit_ns, void* stre
     if (!err) return KMR_ERR_CUDA;
     return launch_wait_timeout(err, limit_ns, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KMR_OK
                                                                                                 : KMR_ERR_CUDA;
+}
+
+extern "C" int kmr_model_set_prefill_tcgen05(kmr_model* m, int enable) {
+    if (!m) return KMR_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(m->mu);
+    m->prefill_tc = enable != 0;
+    return KMR_OK;
 }
 
 extern "C" int kmr_model_set_smem_poison(kmr_model* m, int enable, uint32_t pattern) {

@@ -23,10 +23,11 @@ def torch():
     return require_gpu()
 
 
-def _model(cfg, seed=0, cap=None, max_batch=1):
+def _model(cfg, seed=0, cap=None, max_batch=1, tc=False):
     syn = SyntheticModel(cfg, seed)
     m = kmr.Model.from_config(cfg, max_batch=max_batch)
     driver.load_weights(m, syn, cfg.n_layers, cfg.qk_norm)
+    m.set_prefill_tcgen05(tc)
     if cap:
         m.reserve_prefill(cap)
     return m, syn
@@ -68,10 +69,14 @@ def _cache(m, cfg, slot):
     return out
 
 
+TC = pytest.mark.parametrize("tc", [False, True], ids=["mma", "tcgen05"])
+
+
+@TC
 @pytest.mark.parametrize("T,start,slot", [(40, 0, 1), (1, 0, 0), (23, 17, 1), (128, 0, 0), (16, 112, 1)])
-def test_tiny_prefill_matches_oracle(torch, T, start, slot):
+def test_tiny_prefill_matches_oracle(torch, T, start, slot, tc):
     cfg = tiny_config(slots=2)
-    m, syn = _model(cfg, cap=128)
+    m, syn = _model(cfg, cap=128, tc=tc)
     o = od.OracleDecoder(cfg, 0)
     if start:
         # earlier chunk already in the row (same on both sides)
@@ -101,11 +106,12 @@ def test_tiny_prefill_matches_oracle(torch, T, start, slot):
     m.close()
 
 
-def test_chunked_prefill_equals_one_chunk_bitwise(torch):
+@TC
+def test_chunked_prefill_equals_one_chunk_bitwise(torch, tc):
     cfg = tiny_config(slots=2)
     toks, pos = _prompt(cfg, 70, seed=9)
-    a, _ = _model(cfg, cap=70)
-    b, _ = _model(cfg, cap=32)
+    a, _ = _model(cfg, cap=70, tc=tc)
+    b, _ = _model(cfg, cap=32, tc=tc)
     sa, sb = State(torch, cfg.vocab), State(torch, cfg.vocab)
     _prefill(torch, a, toks, pos, 1, 0, sa)
     for c0, c1 in ((0, 32), (32, 40), (40, 70)):
@@ -162,10 +168,11 @@ def test_prefill_agrees_with_decode_steps_and_decoding_continues(torch):
     b.close()
 
 
-def test_prefill_single_2b_layer_matches_oracle(torch):
+@TC
+def test_prefill_single_2b_layer_matches_oracle(torch, tc):
     cfg = layer2b_config(slots=1)
     T = 48
-    m, _ = _model(cfg, cap=64)
+    m, _ = _model(cfg, cap=64, tc=tc)
     o = od.OracleDecoder(cfg, 0)
     toks, pos = _prompt(cfg, T, seed=2, delta=-40)
     st = State(torch, cfg.vocab)
@@ -177,6 +184,30 @@ def test_prefill_single_2b_layer_matches_oracle(torch):
     assert rel_l2(od.bf16_to_f64(gpu[0][:, :T]), od.bf16_to_f64(o.K[0][0][:, :T])) <= REL_L2_TOL
     assert rel_l2(od.bf16_to_f64(gpu[1][:, :T]), od.bf16_to_f64(o.V[0][0][:, :T])) <= REL_L2_TOL
     m.close()
+
+
+def test_tcgen05_prefill_agrees_with_the_default_kernel(torch):
+    """The tensor-core (tcgen05) projections against the default ones on the same prompt:
+    logits and every cached K/V within the parity bar (fp16-dequantised weights and per-row
+    scaled fp16 tokens against per-group folded integer products), the same greedy token
+    unless the logits have a near tie, the same row state."""
+    cfg = layer2b_config(slots=1, n_layers=2)
+    T = 200
+    toks, pos = _prompt(cfg, T, seed=12, delta=3)
+    outs = []
+    for tc in (False, True):
+        m, _ = _model(cfg, cap=T, tc=tc)
+        st = State(torch, cfg.vocab)
+        _prefill(torch, m, toks, pos, 0, 0, st)
+        outs.append((st.logits.cpu().numpy(), int(st.tok.cpu()[0]), st.pos.cpu().numpy(), int(st.cpos.cpu()[0]),
+                     _cache(m, cfg, 0)))
+        m.close()
+    (la, ta, pa, ca, ka), (lb, tb, pb, cb, kb) = outs
+    assert rel_l2(lb, la) <= REL_L2_TOL
+    assert ta == tb or greedy_agrees(tb, la.astype(np.float64))
+    assert np.array_equal(pa, pb) and ca == cb == T
+    for x, y in zip(ka, kb):
+        assert rel_l2(od.bf16_to_f64(y[:, :T]), od.bf16_to_f64(x[:, :T])) <= REL_L2_TOL
 
 
 def test_prefill_argument_errors(torch):
