@@ -607,6 +607,31 @@ def prefill_only(T: int) -> None:
     print(json.dumps({"prefill_tokens": T, "calls": 2, "status": "ok"}))
 
 
+def device_info(torch) -> dict:
+    """Name and SM count of the current CUDA device and the host's core count (None when a
+    value cannot be read; never raises)."""
+    info = {"gpu": None, "sms": None, "host_cores": os.cpu_count()}
+    try:
+        prop = torch.cuda.get_device_properties(torch.cuda.current_device())
+        info["gpu"], info["sms"] = prop.name, int(prop.multi_processor_count)
+    except Exception:
+        pass
+    return info
+
+
+def start_watchdog(seconds: float, on_timeout=None) -> threading.Timer:
+    """A host-side watchdog: if the run has not finished after `seconds`, report it on stderr
+    and end the process with status 3 instead of leaving it hanging (device waits are bounded
+    already; this covers the host).  Cancel the returned timer when the run is done."""
+    def fire():
+        print(json.dumps({"error": f"bench watchdog: no result after {seconds:.0f} s"}), file=sys.stderr, flush=True)
+        (on_timeout or (lambda: os._exit(3)))()
+    t = threading.Timer(seconds, fire)
+    t.daemon = True
+    t.start()
+    return t
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -621,7 +646,17 @@ def main():
                     help="only run two T-token prefills on the batch-1 model and exit (for profiling)")
     ap.add_argument("--sweep", action="store_true",
                     help="only run the standalone int4 GEMV and decode-attention sweeps and exit")
+    ap.add_argument("--watchdog-s", type=float, default=1800.0,
+                    help="end the run with status 3 if it has not finished after this many seconds")
     args = ap.parse_args()
+    watchdog = start_watchdog(args.watchdog_s)
+    try:
+        _main(args)
+    finally:
+        watchdog.cancel()
+
+
+def _main(args):
     if args.sweep:
         sweep()
         return
@@ -691,6 +726,7 @@ def main():
                         "frac": round(r["kv_copy"]["gbs"] / peaks["hbm_gbs"], 3), "bytes": r["kv_copy"]["bytes"]},
         "gpu_launches": r["kernels_per_step"] * args.steps,
         "clocks": r["clocks"],
+        "device": device_info(torch),
         "setup_s": round(r["setup_s"], 1),
     }
     if "cpu" in r:
