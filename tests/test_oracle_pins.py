@@ -244,3 +244,33 @@ def test_argmax_lowest_index_and_nan():
 def test_silu_closed_form():
     x = np.array([-3.0, 0.0, 2.0])
     assert np.allclose(od.silu(x), x * scipy.special.expit(x), rtol=1e-15)
+
+
+def test_attention_is_invariant_to_permuting_cached_positions_and_linear_in_v():
+    """softmax(q K^T / sqrt(d)) V does not depend on the order of the cached positions (K and V
+    permuted together) and is linear in V — a K/V index mix-up or a stray nonlinearity breaks
+    one of them."""
+    r = np.random.default_rng(21)
+    nq, nkv, d, T = 4, 2, 16, 37
+    q = r.standard_normal((nq, d))
+    K = r.standard_normal((nkv, T, d))
+    V = r.standard_normal((nkv, T, d))
+    V2 = r.standard_normal((nkv, T, d))
+    out = od.decode_attention(q, K, V)
+    perm = r.permutation(T)
+    assert np.allclose(od.decode_attention(q, K[:, perm], V[:, perm]), out, rtol=1e-12, atol=1e-14)
+    assert not np.allclose(od.decode_attention(q, K[:, perm], V), out)          # permuting V alone matters
+    lin = od.decode_attention(q, K, 2.5 * V - 0.75 * V2)
+    assert np.allclose(lin, 2.5 * out - 0.75 * od.decode_attention(q, K, V2), rtol=1e-12, atol=1e-13)
+
+
+def test_int4_linear_is_linear_in_x():
+    r = np.random.default_rng(22)
+    N, K = 24, 256
+    q = r.integers(0, 16, (N, K), dtype=np.uint8)
+    s = od.f64_to_bf16_bits(r.uniform(0.002, 0.02, (N, K // 128)))
+    z = od.f64_to_bf16_bits(r.normal(0, 0.005, (N, K // 128)))
+    x1, x2 = r.standard_normal((2, K)), r.standard_normal((2, K))
+    y = od.int4_linear(1.5 * x1 - 2.0 * x2, q, s, z, 128)
+    assert np.allclose(y, 1.5 * od.int4_linear(x1, q, s, z, 128) - 2.0 * od.int4_linear(x2, q, s, z, 128),
+                       rtol=1e-12, atol=1e-12)
