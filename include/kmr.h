@@ -387,7 +387,8 @@ int kmr_smem_poison(uint32_t pattern, void* stream);
 int kmr_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
 int kmr_model_set_smem_poison(kmr_model* m, int enable, uint32_t pattern);
 
-/* Prefill projections on the 5th-generation tensor cores.  With enable = 1,
+/* Prefill projections on the 5th-generation tensor cores (the prefill of
+ * "kaminari", §04 Request lifecycle; the projections of §07).  With enable = 1,
  * kmr_prefill runs every projection whose output rows are a multiple of 128
  * as a tcgen05.mma kernel: the group's int4 weights dequantised to fp16 in
  * shared memory, the staged tokens as fp16 scaled by a per-row power of two,

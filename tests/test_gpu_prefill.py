@@ -5,7 +5,10 @@ static cache and yields the first token from the last position's logits).
 Besides the oracle: chunked prefill must equal one-chunk prefill bit for bit (a row's result
 depends only on that row), and prefill must agree with the GPU's own decode step run token by
 token (the prefill GEMM sums the 128-input groups in order where the decode GEMV uses a
-pairwise tree, so the two differ by rounding only)."""
+pairwise tree, so the two differ by rounding only).
+
+The oracle cases run on both projection kernels: the default warp-level one and the opt-in
+tcgen05 one (fp16-dequantised weights, fp32 accumulation in tensor memory)."""
 import numpy as np
 import pytest
 
