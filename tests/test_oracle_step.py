@@ -212,3 +212,80 @@ def test_layer_with_zero_attention_is_the_mlp_block():
     x2 = x0 + W["down"] @ (g / (1.0 + np.exp(-g)) * u)
     logits = E @ _rms(x2, syn.norm(-1, "final"), cfg.eps)
     assert np.allclose(res.logits[0], logits, rtol=1e-11, atol=1e-14)
+
+
+def _rot_complex(x, pos3, d, theta, sections):
+    """M-RoPE written independently of the oracle: the pair (x_i, x_{i+d/2}) as one complex
+    number turned by exp(j * pos[axis(i)] * theta^(-2i/d)), axis(i) from contiguous sections."""
+    axes = [0] * sections[0] + [1] * sections[1] + [2] * sections[2]
+    out = np.empty(d)
+    for i in range(d // 2):
+        zc = complex(x[i], x[i + d // 2]) * np.exp(1j * pos3[axes[i]] * theta ** (-2.0 * i / d))
+        out[i], out[i + d // 2] = zc.real, zc.imag
+    return out
+
+
+def _two_position_layer(cfg, syn, W, tok, pos3, cpos, norm_after_rope=False, swap_qk_norm=False,
+                        rotate_at_cache_position=False):
+    """Closed form of one layer on a row holding one cached position (cache position 1): q and k
+    from the normed input, per-head RMSNorm with the q and k weights, the rotation at the row's
+    positions, then a two-way softmax per query head over the cached k and the new (bf16) k.
+    The keyword flags build the same closed form with one plausible mistake in it."""
+    d, qd, kvd = cfg.head_dim, cfg.q_dim, cfg.kv_dim
+    rep = cfg.n_q_heads // cfg.n_kv_heads
+    E = od.bf16_to_f64(syn.embedding())
+    x0 = E[tok]
+    h = _rms(x0, syn.norm(0, "in"), cfg.eps)
+    qkv = W["qkv"] @ h
+    q = qkv[:qd].reshape(cfg.n_q_heads, d)
+    k = qkv[qd:qd + kvd].reshape(cfg.n_kv_heads, d)
+    v = qkv[qd + kvd:].reshape(cfg.n_kv_heads, d)
+    wq, wk = syn.norm(0, "q"), syn.norm(0, "k")
+    if swap_qk_norm:
+        wq, wk = wk, wq
+    p = [cpos] * 3 if rotate_at_cache_position else list(pos3)
+    rot = lambda a: _rot_complex(a, p, d, cfg.rope_theta, cfg.mrope_sections)
+    if norm_after_rope:
+        qr = np.stack([_rms(rot(a), wq, cfg.eps) for a in q])
+        kr = np.stack([_rms(rot(a), wk, cfg.eps) for a in k])
+    else:
+        qr = np.stack([rot(_rms(a, wq, cfg.eps)) for a in q])
+        kr = np.stack([rot(_rms(a, wk, cfg.eps)) for a in k])
+    k_new = od.bf16_to_f64(od.f64_to_bf16_bits(kr))
+    v_new = od.bf16_to_f64(od.f64_to_bf16_bits(v))
+    K0 = od.bf16_to_f64(syn.kv_prefill(0, 0, 1, "k")[:, 0])
+    V0 = od.bf16_to_f64(syn.kv_prefill(0, 0, 1, "v")[:, 0])
+    attn = np.empty((cfg.n_q_heads, d))
+    for i in range(cfg.n_q_heads):
+        hk = i // rep
+        s0 = qr[i] @ K0[hk] / np.sqrt(d)
+        s1 = qr[i] @ k_new[hk] / np.sqrt(d)
+        p1 = 1.0 / (1.0 + np.exp(s0 - s1))           # softmax over the two positions
+        attn[i] = (1.0 - p1) * V0[hk] + p1 * v_new[hk]
+    x1 = x0 + W["o"] @ attn.reshape(-1)
+    return E @ _rms(x1, syn.norm(-1, "final"), cfg.eps), k_new
+
+
+def test_layer_qk_norm_then_mrope_at_positions_closed_form():
+    """How the attention prologue composes ("kaminari", §03 Architecture overview: TextAttention
+    with fused QKV and Mrope; §04 Request lifecycle: positions (3, B, 1) and cache_position):
+    per-head RMSNorm of q and k with their own weights, then the 3-section rotation at the row's
+    positions (distinct T/H/W ids, none equal to the cache position), then attention over the
+    cached position and the new one.  Non-zero W_q and W_k, gate_up = 0 (the MLP adds nothing).
+    The same closed form built with the norm after the rotation, with the q and k norm weights
+    swapped, or with the rotation at cache_position differs from the correct one by far more than
+    the tolerance, so an oracle making any of those mistakes fails this test."""
+    cfg = tiny_config()
+    o, W = _one_layer_with(cfg, lambda n, qsz: _zero_rows(qsz, slice(None)) if n == "gate_up" else qsz)
+    tok, cp, pos3 = 211, 1, (57, 23, 9)
+    o.prefill_cache(0, cp)
+    state = (np.array([tok], np.int32), np.array(pos3, np.int32).reshape(3, 1), np.array([cp], np.int32),
+             np.array([0], np.int32), np.zeros(1, np.uint8))
+    res = o.step(*state)
+    want, k_new = _two_position_layer(cfg, o.syn, W, tok, pos3, cp)
+    assert np.allclose(res.logits[0], want, rtol=1e-11, atol=1e-14)
+    assert np.array_equal(od.bf16_to_f64(o.K[0][0][:, cp]), k_new)     # the cache holds the rotated k
+    scale = np.linalg.norm(want)
+    for mistake in ("norm_after_rope", "swap_qk_norm", "rotate_at_cache_position"):
+        wrong, _ = _two_position_layer(cfg, o.syn, W, tok, pos3, cp, **{mistake: True})
+        assert np.linalg.norm(wrong - want) > 1e-6 * scale, mistake
