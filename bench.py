@@ -163,7 +163,32 @@ def aggregate_ranks(torch, elapsed_ms: float, tokens: float, world: int, device:
     return max(float(x[0]) for x in ts), sum(float(x[1]) for x in ts)
 
 
-def run_kmr(args, rank: int, world: int) -> dict:
+def percentiles(ms) -> dict:
+    a = np.asarray(ms, dtype=np.float64)
+    return {"mean": float(a.mean()), "p10": float(np.percentile(a, 10)), "p50": float(np.percentile(a, 50)),
+            "p90": float(np.percentile(a, 90)), "n": int(a.size)}
+
+
+def timed_steps_accounting(wl, steps: int):
+    """Tokens emitted and KV bytes read (positions 0..cache_position of every active row, all
+    layers, K and V) over the `steps` timed steps, generation by generation from the start."""
+    c = wl.cfg
+    per_pos = c.n_layers * 2 * c.n_kv_heads * c.head_dim * 2
+    tokens = kv = 0
+    for i in range(steps):
+        t = i % wl.steps
+        for b in range(wl.batch):
+            n = min(wl.finish_at.get(b, wl.steps), c.max_len - wl.prefill[b], wl.steps)
+            if t < n:
+                tokens += 1
+                kv += per_pos * (wl.prefill[b] + t + 1)
+    return tokens, kv
+
+
+def run_kmr(args, batch: int, rank: int, world: int, extras: bool) -> dict:
+    """Decode `args.steps` timed steps of the workload of `batch` rows (after the warm-up),
+    one CUDA event per step on the launching stream.  With `extras` (rank 0 of the headline
+    batch) also the standalone kernel timings, prefill, slot migration and cascade attention."""
     import torch
     import int4_weight_only_group_gb300 as kmr
     from int4_weight_only_group_gb300 import driver
@@ -172,15 +197,20 @@ def run_kmr(args, rank: int, world: int) -> dict:
 
     dev_index = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(dev_index)
-    wl = workload(args.batch)
+    wl = workload(batch)
     cfg = wl.cfg
     B = wl.batch
     t_setup = time.time()
-    syn = SyntheticModel(cfg, wl.seed, memo=(rank == 0 and not args.no_cpu_baseline))
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    syn = SyntheticModel(cfg, wl.seed, memo=(rank == 0 and extras and not args.no_cpu_baseline))
     model = kmr.Model.from_config(cfg, max_batch=B)
     driver.load_weights(model, syn, cfg.n_layers, cfg.qk_norm)
     for b in range(B):
         driver.load_kv(model, syn, cfg.n_layers, wl.slot_ids[b], wl.prefill[b])
+    torch.cuda.synchronize()
+    memory = model.device_bytes()
+    memory["mem_get_info_delta"] = int(free0 - torch.cuda.mem_get_info()[0])
     setup_s = time.time() - t_setup
 
     st0 = initial_state(wl)
@@ -211,52 +241,48 @@ def run_kmr(args, rank: int, world: int) -> dict:
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     t0 = time.time()
-    e0.record(stream)
-    gens = 0
+    ev[0].record(stream)
     for i in range(args.steps):
         t = i % wl.steps
         if t == 0 and i > 0:
-            rewind()
-            gens += 1
+            rewind()                      # back to the generation's start (a device copy, inside the timing)
         step(t)
-    e1.record(stream)
+        ev[i + 1].record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
     if world > 1:
         torch.distributed.barrier()
-    elapsed_ms = e0.elapsed_time(e1)
+    elapsed_ms = ev[0].elapsed_time(ev[-1])
+    per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
     clk = None
     if clocks:
         time.sleep(0.1)
         clocks.stop()
         clk = clocks.summary(t0, t1)
     assert model.sync_status(stream) == 0, "device error during the timed region"
-    full_gens, rem = divmod(args.steps, wl.steps)
-    tok_gen = tokens_per_generation(wl)
-    # tokens emitted in the timed steps (partial last generation counted exactly)
-    partial = 0
-    for b in range(B):
-        n = min(wl.finish_at.get(b, wl.steps), cfg.max_len - wl.prefill[b], wl.steps)
-        partial += min(n, rem)
-    tokens = full_gens * tok_gen + partial
-    kv_gen = kv_bytes_per_generation(wl)
+    tokens, kv_timed = timed_steps_accounting(wl, args.steps)
 
     if world > 1:
         elapsed_ms, tokens = aggregate_ranks(torch, elapsed_ms, tokens, world, "cuda")
     if rank != 0:
+        model.close()
         return {}
 
-    out = {"elapsed_ms": elapsed_ms, "tokens": tokens, "setup_s": setup_s, "clocks": clk,
-           "kernels_per_step": model.kernels_per_step(B), "kv_gen": kv_gen}
+    out = {"wl": wl, "elapsed_ms": elapsed_ms, "tokens": tokens, "setup_s": setup_s, "clocks": clk,
+           "kernels_per_step": model.kernels_per_step(B), "kv_timed": kv_timed, "step_ms": percentiles(per_step),
+           "memory": memory}
     if args.skip_extras:
+        model.close()
+        return out
+    # ---- end to end through the host-buffer C ABI call
+    out["e2e"] = time_e2e(torch, model, wl, st0, args.steps)
+    if not extras:
         model.close()
         return out
     # ---- dominant kernel: the int4 GEMV, timed alone on rotating copies larger than L2
     out["gemv"] = time_gemv(torch, kmr, syn, cfg, B)
-    # ---- end to end through the host-buffer C ABI call
-    out["e2e"] = time_e2e(torch, model, wl, st0, args.steps)
     # ---- slot migration: one whole cache row (every layer, K and V) per copy_row_from
     out["kv_copy"] = time_kv_copy(torch, model, cfg)
     # ---- text prefill of a 512-token prompt into slot 0 (after the timed decode region)
@@ -268,7 +294,7 @@ def run_kmr(args, rank: int, world: int) -> dict:
     out["cascade"] = time_cascade(torch, kmr, cfg)
     model.close()
     if not args.no_cpu_baseline:
-        out["cpu"] = cpu_baseline(wl, syn)
+        out["cpu"] = cpu_baseline(wl, syn, args)
     return out
 
 
@@ -449,70 +475,143 @@ def time_e2e(torch, model, wl, st0, steps: int) -> dict:
 
 
 # ------------------------------------------------------------------ CPU oracle legs
-def oracle_sample_time(wl, syn, layer_rows_frac: float, head_frac: float):
-    """Time one oracle layer (all of its math, on a row fraction of each linear) and a
-    vocab slice of the LM head; returns (s for the full step estimate, detail)."""
+ORACLE_LEGS = {
+    "tiny": "tiny_workload",
+    "layer": "layer2b_workload",
+    "b1": "full2b_b1_workload",
+    "b4": "full2b_b4_workload",
+}
+
+
+def oracle_leg_workload(leg: str):
+    import workloads
+    return getattr(workloads, ORACLE_LEGS[leg])()
+
+
+def warm_weights(syn, cfg) -> None:
+    """Draw (and memoise) every tensor the oracle reads, outside any timed step."""
+    for l in range(cfg.n_layers):
+        for name in cfg.linear_shapes():
+            syn.linear(l, name)
+        for nm in ("in", "post", "q", "k"):
+            syn.norm(l, nm)
+    syn.norm(-1, "final")
+    syn.embedding()
+
+
+def oracle_steps(wl, syn, max_steps: int, budget_s: float) -> dict:
+    """Whole oracle decode steps of `wl` from its initial state (free-running on the oracle's
+    own tokens, with the workload's row retirements), each timed on its own; stops after
+    `max_steps` or once `budget_s` has passed (at least one step).  Nothing is sampled or
+    scaled: every timed step is the full decode step of every row."""
     from oracle import decoder as od
-    cfg = wl.cfg
-    B = wl.batch
-    o = od.OracleDecoder(cfg, wl.seed, layers=1, syn=syn)
-    st = od.initial_state(wl)
-    for b in range(B):
-        o.prefill_cache(wl.slot_ids[b], wl.prefill[b])
-    x = od.bf16_to_f64(syn.embedding()[np.asarray(st[0])])
-    # weights drawn outside the timed region
-    for name in ("qkv", "o", "gate_up", "down"):
-        syn.linear(0, name)
-    t0 = time.perf_counter()
-    o._layer(0, x, st[1], st[2], st[3], st[4] == 0)
-    t_layer = time.perf_counter() - t0
-    nv = max(1, int(cfg.vocab * head_frac))
-    o.head_rows = slice(0, nv)
-    t0 = time.perf_counter()
-    o.logits_of(x)
-    t_head = time.perf_counter() - t0
-    full = t_layer * cfg.n_layers + t_head * cfg.vocab / nv
-    return full, {"t_layer_s": t_layer, "t_head_slice_s": t_head, "head_rows": nv}
+    o = od.OracleDecoder.for_workload(wl, syn=syn)
+    tok, pos, cpos, slot, fin = od.initial_state(wl)
+    times, toks = [], []
+    t_start = time.perf_counter()
+    for t in range(max_steps):
+        fin = np.array(fin, copy=True)
+        for row, at in wl.finish_at.items():
+            if at == t:
+                fin[row] = 1
+        active = int((fin == 0).sum())
+        t0 = time.perf_counter()
+        res = o.step(tok, pos, cpos, slot, fin)
+        times.append(time.perf_counter() - t0)
+        toks.append(active)
+        tok, pos, cpos, fin = res.next_ids, res.positions, res.cache_position, res.finished
+        if time.perf_counter() - t_start > budget_s:
+            break
+    med = statistics.median(times)
+    return {"workload": wl.name, "steps": len(times), "s_per_step": times, "median_s": med,
+            "tok_per_s": statistics.median(toks) / med, "extrapolated": False}
 
 
-def cpu_baseline(wl, syn) -> dict:
-    full, det = oracle_sample_time(wl, syn, 1.0, 1.0 / 16)
-    tokens_per_step = tokens_per_generation(wl) / wl.steps
-    return {"value": tokens_per_step / full, "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"one full oracle layer (layer 0, all rows, attention included) x {wl.cfg.n_layers} "
-                      f"+ LM head on {det['head_rows']} of {wl.cfg.vocab} vocab rows scaled to the full vocab; "
-                      f"numpy float64 (BLAS threads = host cores); t_layer={det['t_layer_s']:.2f}s "
-                      f"t_head_slice={det['t_head_slice_s']:.2f}s",
-            "est_s_per_step": full}
+def oracle_leg(leg: str, max_steps: int, budget_s: float, syn=None) -> dict:
+    from workloads import SyntheticModel
+    wl = oracle_leg_workload(leg)
+    if syn is None:
+        syn = SyntheticModel(wl.cfg, wl.seed, memo=True)
+    warm_weights(syn, wl.cfg)
+    return oracle_steps(wl, syn, max_steps, budget_s)
+
+
+def oracle_leg_subprocess(leg: str, threads: int, max_steps: int, budget_s: float) -> dict:
+    """One oracle leg in a child process with its BLAS / OpenMP pools set to `threads`."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = str(threads)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-leg", leg, "--oracle-steps",
+                        str(max_steps), "--oracle-budget-s", str(budget_s)], env=env, capture_output=True,
+                       text=True, timeout=budget_s * 4 + 600)
+    if r.returncode != 0:
+        return {"error": (r.stderr or r.stdout).strip().splitlines()[-1:] or ["failed"]}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    d["threads"] = threads
+    return d
+
+
+def cpu_baseline(wl, syn, args) -> dict:
+    """The oracle as it stands on the host cores: whole 28-layer steps of the headline workload
+    (all cores, weights drawn before the timing), plus the smaller legs of the measurement plan
+    on all cores and on one thread (--cpu-suite adds the 28-layer legs on one thread and
+    batch 4 on all cores)."""
+    cores = os.cpu_count()
+    main = oracle_steps(wl, syn, 3, 20.0)
+    main["threads"] = cores
+    suite = {}
+    for leg in ("tiny", "layer"):
+        suite[f"{leg}_all_cores"] = oracle_leg_subprocess(leg, cores, 3, 10.0)
+        suite[f"{leg}_1_thread"] = oracle_leg_subprocess(leg, 1, 3, 10.0)
+    if args.cpu_suite:
+        suite["b4_all_cores"] = oracle_leg_subprocess("b4", cores, 3, 60.0)
+        suite["b1_1_thread"] = oracle_leg_subprocess("b1", 1, 3, 60.0)
+        suite["b4_1_thread"] = oracle_leg_subprocess("b4", 1, 3, 60.0)
+    tps = tokens_per_generation(wl) / wl.steps
+    value = tps / main["median_s"]
+    return {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "sample": f"{main['steps']} whole oracle decode steps of the headline workload ({wl.name}), "
+                      f"median {main['median_s']:.2f} s per step; numpy float64 with BLAS threads = host cores; "
+                      "weights drawn before the timing; nothing extrapolated",
+            "steps": main["steps"], "s_per_step": main["s_per_step"], "extrapolated": False, "suite": suite}
 
 
 def run_reference(args) -> dict:
-    """The oracle as it stands, on the host cores, on this benchmark's workload: each step
-    is a bounded sample (one layer + a vocab slice of the head) scaled to a full step."""
+    """The oracle as it stands, on the host cores, on this benchmark's workloads: every timed
+    step is one whole oracle decode step (all 28 layers and the full vocabulary) of the batch-1
+    workload, until `--steps` are done or the time budget is spent (the line's `steps` is the
+    count actually run); `bs4` times whole steps of the batch-4 workload the same way."""
     from workloads import SyntheticModel
-    wl = workload(args.batch)
-    syn = SyntheticModel(wl.cfg, wl.seed, memo=True)
-    for i in range(args.warmup):
-        oracle_sample_time(wl, syn, 1.0, 1.0 / 64)
-    fulls = []
-    t0 = time.perf_counter()
-    budget_s = 150.0
-    for i in range(args.steps):
-        f, _ = oracle_sample_time(wl, syn, 1.0, 1.0 / 64)
-        fulls.append(f)
-        if time.perf_counter() - t0 > budget_s:
-            break
-    est = statistics.median(fulls)
-    tps = tokens_per_generation(wl) / wl.steps
-    value = tps / est
-    return {"metric": METRIC, "value": value, "unit": "tok/s", "impl": "reference", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": est * 1000.0, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+    batches = [args.batch] if args.batch else [1, 4]
+    res = {}
+    for B in batches:
+        wl = workload(B)
+        syn = SyntheticModel(wl.cfg, wl.seed, memo=True)
+        warm_weights(syn, wl.cfg)
+        if args.warmup:
+            oracle_steps(wl, syn, 1, 0.0)          # one whole warm-up step (numpy / BLAS first-touch)
+        budget = 120.0 if B == batches[0] else 60.0
+        r = oracle_steps(wl, syn, args.steps, budget)
+        r["tokens_per_step"] = tokens_per_generation(wl) / wl.steps
+        res[B] = (wl, r)
+        del syn
+    wl, r = res[batches[0]]
+    value = r["tokens_per_step"] / r["median_s"]
+    line = {"metric": METRIC, "value": value, "unit": "tok/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": r["steps"], "warmup": 1 if args.warmup else 0, "ms_per_step": r["median_s"] * 1000.0,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl.name, "batch": wl.batch, "kv_max_len": wl.cfg.max_len},
             "cpu_baseline": {"value": value, "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": f"per step: one oracle layer (all rows) x {wl.cfg.n_layers} + 1/64 of the "
-                                       f"LM head x 64; {len(fulls)} sampled steps (median), budget {budget_s:.0f}s"},
+                             "sample": f"{r['steps']} whole oracle decode steps (median; requested {args.steps}, "
+                                       "120 s budget), numpy float64, BLAS threads = host cores; nothing "
+                                       "extrapolated", "extrapolated": False},
             "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    if 4 in res and batches[0] != 4:
+        wl4, r4 = res[4]
+        v4 = r4["tokens_per_step"] / r4["median_s"]
+        line["bs4"] = {"value": v4, "unit": "tok/s", "steps": r4["steps"], "ms_per_step": r4["median_s"] * 1000.0,
+                       "config": {"workload": wl4.name, "batch": 4}}
+    return line
 
 
 # ------------------------------------------------------------------ kernel sweeps
@@ -632,20 +731,47 @@ def start_watchdog(seconds: float, on_timeout=None) -> threading.Timer:
     return t
 
 
+def step_figures(r, args, peaks) -> dict:
+    """tok/s, per-step times and the step's algorithmic bytes against the measured peak, from
+    the KV the timed steps actually read."""
+    wl = r["wl"]
+    cfg = wl.cfg
+    ms = r["elapsed_ms"] / args.steps
+    wb = weight_bytes(cfg)
+    step_weight_bytes = cfg.n_layers * (wb["qkv"] + wb["o"] + wb["gate_up"] + wb["down"]) + wb["lm_head"] + wb["norms"]
+    step_bytes = step_weight_bytes + r["kv_timed"] / args.steps
+    return {
+        "value": r["tokens"] / (r["elapsed_ms"] / 1000.0), "ms_per_step": ms,
+        "step_ms": {k: (round(v, 5) if isinstance(v, float) else v) for k, v in r["step_ms"].items()},
+        "step_roofline": {"bytes_per_step": step_bytes, "weight_bytes_per_step": step_weight_bytes,
+                          "kv_bytes_per_step": r["kv_timed"] / args.steps, "achieved_gbs": step_bytes / (ms * 1e6),
+                          "frac": step_bytes / (ms * 1e6) / peaks["hbm_gbs"],
+                          "roofline_ms_per_step": step_bytes / (peaks["hbm_gbs"] * 1e6),
+                          "kv": "positions 0..cache_position of every active row in the timed steps"},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=256)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--batch", type=int, default=1, choices=(1, 4, 16))
+    ap.add_argument("--batch", type=int, default=None, choices=(1, 4, 16),
+                    help="time only this batch (default: batch 1 headline plus a batch-4 'bs4' object)")
     ap.add_argument("--impl", default="kmr", choices=("kmr", "reference"))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-suite", action="store_true",
+                    help="also time the 28-layer oracle legs on one thread and batch 4 on all cores")
     ap.add_argument("--skip-extras", action="store_true",
                     help="time only the decode steps (no standalone GEMV timing, e2e or CPU legs; for launch lists)")
     ap.add_argument("--prefill-only", type=int, default=0, metavar="T",
                     help="only run two T-token prefills on the batch-1 model and exit (for profiling)")
     ap.add_argument("--sweep", action="store_true",
                     help="only run the standalone int4 GEMV and decode-attention sweeps and exit")
+    ap.add_argument("--oracle-leg", choices=tuple(ORACLE_LEGS), default=None,
+                    help="(internal) time whole oracle steps of one workload and print one JSON line")
+    ap.add_argument("--oracle-steps", type=int, default=3)
+    ap.add_argument("--oracle-budget-s", type=float, default=30.0)
     ap.add_argument("--watchdog-s", type=float, default=1800.0,
                     help="end the run with status 3 if it has not finished after this many seconds")
     args = ap.parse_args()
@@ -657,6 +783,9 @@ def main():
 
 
 def _main(args):
+    if args.oracle_leg:
+        print(json.dumps(oracle_leg(args.oracle_leg, args.oracle_steps, args.oracle_budget_s)))
+        return
     if args.sweep:
         sweep()
         return
@@ -678,42 +807,44 @@ def _main(args):
     import torch
     if world > 1:
         torch.distributed.init_process_group("nccl")
-    r = run_kmr(args, rank, world)
+    head_b = args.batch or 1
+    r = run_kmr(args, head_b, rank, world, extras=True)
+    r4 = run_kmr(args, 4, rank, world, extras=False) if args.batch is None else None
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank != 0:
         return
-    if args.skip_extras:
-        print(json.dumps({"ms_per_step": r["elapsed_ms"] / args.steps, "steps": args.steps,
-                          "kernels_per_step": r["kernels_per_step"]}))
-        return
-    wl = workload(args.batch)
-    cfg = wl.cfg
     peaks = measured_peaks()
-    ms = r["elapsed_ms"] / args.steps
-    value = r["tokens"] / (r["elapsed_ms"] / 1000.0)
-    wb = weight_bytes(cfg)
-    step_weight_bytes = cfg.n_layers * (wb["qkv"] + wb["o"] + wb["gate_up"] + wb["down"]) + wb["lm_head"] + wb["norms"]
-    step_bytes = step_weight_bytes + r["kv_gen"] / wl.steps
+    if args.skip_extras:
+        out = {"ms_per_step": r["elapsed_ms"] / args.steps, "steps": args.steps,
+               "kernels_per_step": r["kernels_per_step"], "step_ms": r["step_ms"]}
+        if r4:
+            out["bs4_ms_per_step"] = r4["elapsed_ms"] / args.steps
+        print(json.dumps(out))
+        return
+    wl = r["wl"]
+    cfg = wl.cfg
+    f = step_figures(r, args, peaks)
     g = r["gemv"]["gate_up"]
     traffic = profile_traffic("int4_gemv_gate_up.md")
     line = {
-        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int4w/bf16->f32", "data": "synthetic (seeded; shapes and distributions of the workload recipe)",
+        "metric": METRIC, "value": f["value"], "unit": "tok/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": f["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4w/bf16->f32",
+        "data": "synthetic (seeded; shapes and distributions of the workload recipe)",
         "config": {"workload": wl.name, "batch": wl.batch, "kv_max_len": cfg.max_len, "prefill": wl.prefill,
                    "steps_per_generation": wl.steps, "l2": "inputs larger than L2 (1.4 GB of weights per step)",
                    "parallelism": "replicas" if args.gpus > 1 else "single-gpu"},
+        "step_ms": f["step_ms"],
         "roofline": {"bound": "hbm", "kernel": "int4_gemv (gate_up shape, M=%d)" % wl.batch,
                      "achieved": g["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": g["gbs"] / peaks["hbm_gbs"], "traffic": traffic,
                      "peak_source": peaks["source"]},
-        "step_roofline": {"bytes_per_step": step_bytes, "achieved_gbs": step_bytes / (ms * 1e6),
-                          "frac": step_bytes / (ms * 1e6) / peaks["hbm_gbs"],
-                          "roofline_ms_per_step": step_bytes / (peaks["hbm_gbs"] * 1e6)},
+        "step_roofline": f["step_roofline"],
         "gemv_us": {k: round(v["us"], 2) for k, v in r["gemv"].items()},
         "gemv_gbs": {k: round(v["gbs"], 1) for k, v in r["gemv"].items()},
         "e2e": r["e2e"],
+        "memory": r["memory"],
         "cascade_attn": {"rows": r["cascade"]["rows"], "prefix": r["cascade"]["prefix"], "own": r["cascade"]["own"],
                          "cascade_us": round(r["cascade"]["cascade"]["us"], 2),
                          "plain_us": round(r["cascade"]["plain"]["us"], 2),
@@ -728,9 +859,21 @@ def _main(args):
         "clocks": r["clocks"],
         "device": device_info(torch),
         "setup_s": round(r["setup_s"], 1),
+        "context": {"pages_decode_tok_s": 100.6, "pages_peak_vram_gb": 2.3,
+                    "note": "the pages' own figures (RTX 3050 6 GB, torch.compile + torchao, real Qwen3-VL-2B): "
+                            "context only, another machine and model; vs_baseline stays null"},
     }
+    if r4:
+        f4 = step_figures(r4, args, peaks)
+        line["bs4"] = {"value": f4["value"], "unit": "tok/s", "ms_per_step": f4["ms_per_step"],
+                       "step_ms": f4["step_ms"], "step_roofline": f4["step_roofline"], "e2e": r4["e2e"],
+                       "memory": r4["memory"], "clocks": r4["clocks"],
+                       "gpu_launches": r4["kernels_per_step"] * args.steps,
+                       "config": {"workload": r4["wl"].name, "batch": 4, "prefill": r4["wl"].prefill,
+                                  "steps_per_generation": r4["wl"].steps}}
     if "cpu" in r:
         line["cpu_baseline"] = r["cpu"]
+        line["cpu_baseline"]["gpu_over_cpu"] = f["value"] / r["cpu"]["value"]
     print(json.dumps(line))
 
 

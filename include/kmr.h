@@ -188,8 +188,14 @@ int kmr_decode_attn_cascade(const float* q, const uint16_t* k_cache, const uint1
  * latency-critical loops that cannot afford cudaMalloc's implicit device
  * synchronisation.  The pages this library follows have no counterpart of
  * this entry point; it exists only for such callers.
- *   Same arguments, layouts and results as kmr_decode_attn, minus the
- *   workspace.  The split partials live in one fixed array inside the
+ *   Same arguments and layouts as kmr_decode_attn, minus the workspace.  It
+ *   always runs the global-merge form (splits = ceil(SM count / n_kv_heads),
+ *   capped at 32, each writing its partial state to the array, the last CTA
+ *   of a (row, KV head) to arrive merging them in split order), whereas
+ *   kmr_decode_attn takes the cluster-merged form for most shapes: the two
+ *   agree within the attention tolerance, not bit for bit, and both match the
+ *   plain definition (relative L2 <= 1e-4 in the tests).  The split partials
+ *   live in one fixed array inside the
  *   library's device image (KMR_NOALLOC_ATTN_SCRATCH_BYTES, held by every GPU
  *   that loads the library until the process exits); the call allocates
  *   nothing, and clears the array's arrival counters with cudaMemsetAsync on
@@ -402,6 +408,17 @@ int kmr_model_set_prefill_tcgen05(kmr_model* m, int enable);
 /* Launches one step makes (kernels per step) for the given B, for accounting
  * (twice as many while shared-memory poisoning is on). */
 int kmr_model_kernels_per_step(const kmr_model* m, int B);
+
+/* Device memory the model holds ("kaminari — a single-GPU Qwen3-VL inference
+ * engine, explained", §01 TL;DR and §02: int4 weights with a static
+ * 1024-token cache brought peak VRAM from 4.2 GB to 2.3 GB).  Returns the
+ * bytes of every device allocation the handle owns (packed int4 weights,
+ * bf16 embedding and norms, the static KV cache, step and prefill scratch,
+ * the host-state step's logits buffer once allocated) and, where the pointers
+ * are not null, splits it into weights (packed linears, embedding, norms),
+ * kv_cache (K and V of every layer and slot) and scratch (the rest).  No
+ * CUDA call; 0 for a null model. */
+size_t kmr_model_device_bytes(const kmr_model* m, size_t* weights, size_t* kv_cache, size_t* scratch);
 
 #ifdef __cplusplus
 }

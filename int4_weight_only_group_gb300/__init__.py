@@ -104,6 +104,7 @@ _SIGNATURES = {
     "kmr_decode_step_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P]),
     "kmr_model_sync_status": (_I, [_P, _P]),
     "kmr_model_kernels_per_step": (_I, [_P, _I]),
+    "kmr_model_device_bytes": (_SZ, [_P, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
     "kmr_smem_poison": (_I, [ctypes.c_uint32, _P]),
     "kmr_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
     "kmr_model_set_smem_poison": (_I, [_P, _I, ctypes.c_uint32]),
@@ -337,6 +338,12 @@ class Model:
 
     def kernels_per_step(self, B: int) -> int:
         return lib().kmr_model_kernels_per_step(self._h, B)
+
+    def device_bytes(self) -> dict:
+        """kmr_model_device_bytes: device memory the model holds, total and split."""
+        w, kv, sc = _SZ(0), _SZ(0), _SZ(0)
+        total = lib().kmr_model_device_bytes(self._h, ctypes.byref(w), ctypes.byref(kv), ctypes.byref(sc))
+        return {"total": int(total), "weights": int(w.value), "kv_cache": int(kv.value), "scratch": int(sc.value)}
 
     def set_prefill_tcgen05(self, enable: bool) -> None:
         """kmr_model_set_prefill_tcgen05: run prefill projections on the tcgen05 kernel."""

@@ -370,6 +370,7 @@ struct kmr_model {
     float* prn = nullptr;          // [Mpad] RMSNorm factors
     uint32_t poison_pattern = 0;
     std::vector<void*> allocs;
+    std::vector<size_t> alloc_bytes;   // device bytes of allocs[i]
     std::mutex mu;
 };
 
@@ -381,6 +382,7 @@ cudaError_t dalloc(kmr_model* m, T** p, size_t bytes) {
     cudaError_t e = cudaMalloc(&q, bytes ? bytes : 16);
     if (e != cudaSuccess) return e;
     m->allocs.push_back(q);
+    m->alloc_bytes.push_back(bytes ? bytes : 16);
     *p = static_cast<T*>(q);
     return cudaMemset(q, 0, bytes ? bytes : 16);
 }
@@ -1058,7 +1060,12 @@ extern "C" int kmr_model_reserve_prefill(kmr_model* m, int max_tokens) {
     void* old[10] = {m->px, m->pqkv, m->pq, m->pattn, m->pact, m->pslot, m->pcpos, m->pxs, m->pxst, m->prn};
     for (void* p : old) {
         if (!p) continue;
-        m->allocs.erase(std::remove(m->allocs.begin(), m->allocs.end(), p), m->allocs.end());
+        for (size_t i = 0; i < m->allocs.size(); ++i)
+            if (m->allocs[i] == p) {
+                m->allocs.erase(m->allocs.begin() + i);
+                m->alloc_bytes.erase(m->alloc_bytes.begin() + i);
+                break;
+            }
         cudaFree(p);
     }
     m->prefill_cap = 0;
@@ -1250,4 +1257,22 @@ extern "C" int kmr_model_kernels_per_step(const kmr_model* m, int B) {
     const int head_passes = (B + kMaxHeadRows - 1) / kMaxHeadRows;
     const int k = c.n_layers * (gemv_launches + 1) + head_passes;
     return m->poison ? 2 * k : k;                 // the diagnostic adds one fill per kernel
+}
+
+extern "C" size_t kmr_model_device_bytes(const kmr_model* m, size_t* weights, size_t* kv_cache, size_t* scratch) {
+    if (!m) return 0;
+    const kmr_model_config& c = m->cfg;
+    size_t total = 0;
+    for (size_t n : m->alloc_bytes) total += n;
+    if (m->d_logits) total += size_t(c.max_batch) * c.vocab * 4;
+    size_t w = size_t(c.vocab) * c.hidden * 2 + size_t(c.hidden) * 2;           // tied embedding, final norm
+    for (const LayerW& l : m->layers) {
+        for (int i = 0; i < 4; ++i) w += size_t(l.g[i].bytes);
+        w += (size_t(2) * c.hidden + size_t(2) * c.head_dim) * 2;               // input, post, q, k norms
+    }
+    const size_t kv = size_t(2) * m->kv_layer_elems * c.n_layers * 2;
+    if (weights) *weights = w;
+    if (kv_cache) *kv_cache = kv;
+    if (scratch) *scratch = total > w + kv ? total - w - kv : 0;
+    return total;
 }

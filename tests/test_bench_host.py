@@ -42,3 +42,26 @@ def test_cli_parses_without_a_gpu():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--help"], capture_output=True, text=True,
                        timeout=120)
     assert r.returncode == 0 and "--watchdog-s" in r.stdout
+
+
+def test_timed_step_accounting_counts_active_rows_and_their_kv():
+    """Batch-4 slots: row 2 retires at step 64, row 3 (900 prefilled) writes its last position at
+    step 123; tokens and KV bytes of the timed steps follow that row by row."""
+    from workloads import full2b_b4_workload
+    wl = full2b_b4_workload()
+    c = wl.cfg
+    per_pos = c.n_layers * 2 * c.n_kv_heads * c.head_dim * 2
+    tok, kv = bench.timed_steps_accounting(wl, 20)
+    assert tok == 80
+    assert kv == per_pos * sum(p + t + 1 for p in wl.prefill for t in range(20))
+    tok, kv = bench.timed_steps_accounting(wl, wl.steps)
+    assert tok == bench.tokens_per_generation(wl) == 128 + 128 + 64 + 124
+
+
+def test_oracle_leg_times_whole_steps():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-leg", "tiny", "--oracle-steps", "2",
+                        "--oracle-budget-s", "30"], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    import json
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    assert d["steps"] == 2 and len(d["s_per_step"]) == 2 and d["extrapolated"] is False and d["tok_per_s"] > 0
