@@ -205,6 +205,8 @@ def run_kmr(args, batch: int, rank: int, world: int, extras: bool) -> dict:
     free0 = torch.cuda.mem_get_info()[0]
     syn = SyntheticModel(cfg, wl.seed, memo=(rank == 0 and extras and not args.no_cpu_baseline))
     model = kmr.Model.from_config(cfg, max_batch=B)
+    if args.persistent_step:
+        model.set_persistent_step(True)
     driver.load_weights(model, syn, cfg.n_layers, cfg.qk_norm)
     for b in range(B):
         driver.load_kv(model, syn, cfg.n_layers, wl.slot_ids[b], wl.prefill[b])
@@ -762,6 +764,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-suite", action="store_true",
                     help="also time the 28-layer oracle legs on one thread and batch 4 on all cores")
+    ap.add_argument("--persistent-step", action="store_true",
+                    help="run the step's layers as the persistent kernel (opt-in) instead of one kernel per phase")
     ap.add_argument("--skip-extras", action="store_true",
                     help="time only the decode steps (no standalone GEMV timing, e2e or CPU legs; for launch lists)")
     ap.add_argument("--prefill-only", type=int, default=0, metavar="T",
@@ -820,6 +824,7 @@ def _main(args):
                "kernels_per_step": r["kernels_per_step"], "step_ms": r["step_ms"]}
         if r4:
             out["bs4_ms_per_step"] = r4["elapsed_ms"] / args.steps
+            out["bs4_kernels_per_step"] = r4["kernels_per_step"]
         print(json.dumps(out))
         return
     wl = r["wl"]

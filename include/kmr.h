@@ -405,6 +405,22 @@ int kmr_model_set_smem_poison(kmr_model* m, int enable, uint32_t pattern);
  * kmr_prefill call.  Returns KMR_OK or KMR_ERR_INVALID_ARG (null model). */
 int kmr_model_set_prefill_tcgen05(kmr_model* m, int enable);
 
+/* Whether the decode step runs its layers as one persistent kernel (default
+ * on).  The persistent kernel keeps one CTA per SM for the whole step: each
+ * CTA streams its share of every layer's int4 weights and its attention
+ * splits' K/V rows through a ring of shared-memory slots (cp.async.bulk),
+ * phases (QKV, attention, O, gate_up, down of each layer) start when every CTA
+ * has finished the previous one (bounded waits on global counters; a wait that
+ * runs out records KMR_ERR_DEVICE_TIMEOUT), and the LM head follows as its own
+ * kernel.  It serves up to 4 rows for head sizes 64 and 128 with 2 query heads
+ * per KV head; other shapes and larger batches keep the multi-kernel step.
+ * Both give the same bits ("kaminari — a single-GPU Qwen3-VL inference engine,
+ * explained", §06 The optimization ladder: decode is memory-bandwidth bound
+ * and per-step launch overhead was the next cost removed).  Takes effect from
+ * the next kmr_decode_step.  Returns KMR_OK or KMR_ERR_INVALID_ARG (null
+ * model) / KMR_ERR_CUDA. */
+int kmr_model_set_persistent_step(kmr_model* m, int enable);
+
 /* Launches one step makes (kernels per step) for the given B, for accounting
  * (twice as many while shared-memory poisoning is on). */
 int kmr_model_kernels_per_step(const kmr_model* m, int B);

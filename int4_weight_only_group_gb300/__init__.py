@@ -109,6 +109,7 @@ _SIGNATURES = {
     "kmr_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
     "kmr_model_set_smem_poison": (_I, [_P, _I, ctypes.c_uint32]),
     "kmr_model_set_prefill_tcgen05": (_I, [_P, _I]),
+    "kmr_model_set_persistent_step": (_I, [_P, _I]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
 
@@ -348,6 +349,10 @@ class Model:
     def set_prefill_tcgen05(self, enable: bool) -> None:
         """kmr_model_set_prefill_tcgen05: run prefill projections on the tcgen05 kernel."""
         _check(lib().kmr_model_set_prefill_tcgen05(self._h, int(bool(enable))), "kmr_model_set_prefill_tcgen05")
+
+    def set_persistent_step(self, enable: bool) -> None:
+        """kmr_model_set_persistent_step: run the step's layers as one persistent kernel."""
+        _check(lib().kmr_model_set_persistent_step(self._h, int(bool(enable))), "kmr_model_set_persistent_step")
 
     def set_smem_poison(self, enable: bool, pattern: int = 0xFFFFFFFF) -> None:
         """Precede every kernel of the step with a shared-memory fill of `pattern` (diagnostic)."""

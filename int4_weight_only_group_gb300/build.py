@@ -40,6 +40,8 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
                     "--expt-relaxed-constexpr"]
     if ptxas_info:
         flags += ["-Xptxas", "-v"]
+    # extra nvcc flags for diagnostic builds (for instance -DKMR_STEP_TRACE)
+    flags += os.environ.get("KMR_NVCC_FLAGS", "").split()
 
     def compile_one(src: str) -> str:
         obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")

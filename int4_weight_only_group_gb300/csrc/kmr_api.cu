@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "kmr_internal.cuh"
+#include "kmr_step.cuh"
 #include "kmr_tcgemm.cuh"
 
 namespace kmr {
@@ -60,6 +61,7 @@ cudaError_t ensure_kernel_attributes() {
     if ((e = poison_set_attributes()) != cudaSuccess) return e;
     if ((e = gemm_set_attributes()) != cudaSuccess) return e;
     if ((e = tc_gemm_set_attributes()) != cudaSuccess) return e;
+    if ((e = step_set_attributes()) != cudaSuccess) return e;
     done[dev] = true;
     return cudaSuccess;
 }
@@ -356,6 +358,12 @@ struct kmr_model {
     unsigned long long tick = 0;
     bool poison = false;           // diagnostic: fill shared memory before every kernel of the step
     bool prefill_tc = false;       // prefill projections on tcgen05 (kmr_model_set_prefill_tcgen05)
+    // persistent step (kmr_step.cu): every layer in one kernel for batches it serves
+    bool persistent = false;       // kmr_model_set_persistent_step (opt-in: slower than the PDL-chained step, see header)
+    bool persistent_failed = false;    // a capture of it failed: this model uses the multi-kernel step
+    StepLayer* step_layers = nullptr;  // [L] device table
+    float* step_part = nullptr;        // split states [max rows][nkv][8][rep][d + 2]
+    unsigned* step_sync = nullptr;     // phase counters [L][5] | merge counters [rows][nkv] | done | abort
     // prefill scratch for chunks of up to prefill_cap positions (kmr_model_reserve_prefill)
     int prefill_cap = 0;
     float* px = nullptr;           // residual rows [cap][H]
@@ -450,6 +458,62 @@ bool fused_qkv(const kmr_model_config& c, int B) {
     return B <= kFuseQkvMaxRows && attn_can_fuse_qkv(c.head_dim, c.n_q_heads / c.n_kv_heads, c.hidden);
 }
 
+// Whether this model runs the layers of a B-row step as the persistent kernel (kmr_step.cu),
+// and its launch plan: every CTA must be resident at once (one per SM).
+bool persistent_plan(const kmr_model* m, int B, StepPlan* plan) {
+    if (!m->persistent || m->persistent_failed) return false;
+    const kmr_model_config& c = m->cfg;
+    if (!step_supported(B, c.n_layers, c.hidden, c.n_q_heads, c.n_kv_heads, c.head_dim, c.intermediate, c.max_len,
+                        m->sms, plan))
+        return false;
+    return step_max_active_ctas(*plan, c.head_dim) >= 1;
+}
+
+// The layers of the step as one persistent kernel; the LM head follows.
+int enqueue_persistent(kmr_model* m, const StepArgs& a, const StepPlan& plan, cudaStream_t st) {
+    const kmr_model_config& c = m->cfg;
+    const int rows = std::min(c.max_batch, kStepMaxRows);
+    StepParams p = {};
+    p.layers = m->step_layers;
+    p.L = c.n_layers;
+    p.H = c.hidden;
+    p.nq = c.n_q_heads;
+    p.nkv = c.n_kv_heads;
+    p.I = c.intermediate;
+    p.vocab = c.vocab;
+    p.S = c.max_len;
+    p.slots = c.slots;
+    p.B = a.B;
+    p.eps = c.eps;
+    p.scale = 1.0f / sqrtf(float(c.head_dim));
+    p.qk_norm = c.qk_norm;
+    p.embed = m->embed;
+    p.inv_freq = m->inv_freq;
+    p.sec0 = c.mrope_sections[0];
+    p.sec1 = c.mrope_sections[1];
+    p.tok = a.tok;
+    p.pos = a.pos;
+    p.cpos = a.cpos;
+    p.slot = a.slot;
+    p.fin = a.fin;
+    p.x = m->x_resid;
+    p.qkv = m->qkv;
+    p.attn = m->attn_out;
+    p.act = m->act;
+    p.part = m->step_part;
+    p.phase_cnt = m->step_sync;
+    p.merge_cnt = m->step_sync + size_t(c.n_layers) * 5;
+    p.done_cnt = p.merge_cnt + size_t(rows) * c.n_kv_heads;
+    p.abort_flag = p.done_cnt + 1;
+    p.err = m->err;
+    p.nslots = plan.nslots;
+    p.slot_bytes = plan.slot_bytes;
+    p.gpw_max = plan.gpw_max;
+    p.max_tiles = plan.max_tiles;
+    if (m->poison && launch_smem_poison(m->poison_pattern, m->sms, st) != cudaSuccess) return KMR_ERR_CUDA;
+    return launch_step(p, plan, c.head_dim, st) == cudaSuccess ? KMR_OK : KMR_ERR_CUDA;
+}
+
 int enqueue_step(kmr_model* m, const StepArgs& a, cudaStream_t st) {
     const kmr_model_config& c = m->cfg;
     const int B = a.B;
@@ -459,7 +523,13 @@ int enqueue_step(kmr_model* m, const StepArgs& a, cudaStream_t st) {
     bool pdl = false;   // the first kernel of the step has no kernel predecessor inside the graph
     // Small batches: the attention kernel computes each head group's QKV rows itself (no QKV launch).
     const bool fuse_qkv = fused_qkv(c, B);
-    for (int l = 0; l < c.n_layers; ++l) {
+    StepPlan plan;
+    const bool persistent = persistent_plan(m, B, &plan);
+    if (persistent) {
+        const int rc = enqueue_persistent(m, a, plan, st);
+        if (rc != KMR_OK) return rc;
+    }
+    for (int l = 0; l < c.n_layers && !persistent; ++l) {
         LayerW& L = m->layers[l];
         GemvLaunch g = {};
         if (!fuse_qkv) {
@@ -828,19 +898,27 @@ int get_graph(kmr_model* m, const StepArgs& a, cudaGraphExec_t* out) {
             return KMR_OK;
         }
     }
-    cudaGraph_t graph = nullptr;
-    if (cudaStreamBeginCapture(m->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return KMR_ERR_CUDA;
-    const int rc = enqueue_step(m, a, m->cap);
-    const cudaError_t ec = cudaStreamEndCapture(m->cap, &graph);
-    if (rc != KMR_OK || ec != cudaSuccess) {
+    cudaGraphExec_t exec = nullptr;
+    for (int attempt = 0;; ++attempt) {
+        StepPlan plan;
+        const bool persistent = persistent_plan(m, a.B, &plan);
+        cudaGraph_t graph = nullptr;
+        if (cudaStreamBeginCapture(m->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return KMR_ERR_CUDA;
+        const int rc = enqueue_step(m, a, m->cap);
+        const cudaError_t ec = cudaStreamEndCapture(m->cap, &graph);
+        cudaError_t ei = cudaErrorUnknown;
+        if (rc == KMR_OK && ec == cudaSuccess) ei = cudaGraphInstantiate(&exec, graph, 0);
         if (graph) cudaGraphDestroy(graph);
+        if (rc == KMR_OK && ec == cudaSuccess && ei == cudaSuccess) break;
         cudaGetLastError();
+        // A persistent step that cannot be captured or instantiated here: this model falls back to
+        // the multi-kernel step (kmr_model_kernels_per_step reports which one runs).
+        if (persistent && attempt == 0) {
+            m->persistent_failed = true;
+            continue;
+        }
         return rc != KMR_OK ? rc : KMR_ERR_CUDA;
     }
-    cudaGraphExec_t exec = nullptr;
-    const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
-    cudaGraphDestroy(graph);
-    if (ei != cudaSuccess) return KMR_ERR_CUDA;
     if (m->graphs.size() >= 8) {
         size_t lru = 0;
         for (size_t i = 1; i < m->graphs.size(); ++i)
@@ -912,6 +990,25 @@ extern "C" int kmr_model_create(const kmr_model_config* cfg, kmr_model** out) {
     for (int i = 0; i < c.head_dim / 2; ++i)
         inv[i] = float(pow(double(c.rope_theta), -2.0 * double(i) / double(c.head_dim)));
     if (cudaMemcpy(m->inv_freq, inv.data(), inv.size() * 4, cudaMemcpyHostToDevice)) return fail(KMR_ERR_CUDA);
+    {
+        const int rows = std::min(B, kStepMaxRows), rep = c.n_q_heads / c.n_kv_heads;
+        const size_t nsync = size_t(c.n_layers) * 5 + size_t(rows) * c.n_kv_heads + 2;
+        if (dalloc(m, &m->step_layers, sizeof(StepLayer) * c.n_layers) ||
+            dalloc(m, &m->step_part, size_t(rows) * c.n_kv_heads * kAttnClusterSplits * rep * (c.head_dim + 2) * 4) ||
+            dalloc(m, &m->step_sync, nsync * 4))
+            return fail(KMR_ERR_CUDA);
+        std::vector<StepLayer> t(c.n_layers);
+        for (int l = 0; l < c.n_layers; ++l) {
+            for (int w = 0; w < 4; ++w) {
+                t[l].w[w] = m->layers[l].w[w];
+                t[l].norm[w] = m->layers[l].norm[w];
+            }
+            t[l].kc = m->kc + size_t(l) * m->kv_layer_elems;
+            t[l].vc = m->vc + size_t(l) * m->kv_layer_elems;
+        }
+        if (cudaMemcpy(m->step_layers, t.data(), sizeof(StepLayer) * c.n_layers, cudaMemcpyHostToDevice))
+            return fail(KMR_ERR_CUDA);
+    }
     if (cudaMallocHost(&m->h_state, size_t(B) * 32) != cudaSuccess) return fail(KMR_ERR_CUDA);
     if (cudaStreamCreateWithFlags(&m->cap, cudaStreamNonBlocking) != cudaSuccess) return fail(KMR_ERR_CUDA);
     if (cudaDeviceSynchronize() != cudaSuccess) return fail(KMR_ERR_CUDA);
@@ -1145,6 +1242,17 @@ extern "C" int kmr_model_set_prefill_tcgen05(kmr_model* m, int enable) {
     return KMR_OK;
 }
 
+extern "C" int kmr_model_set_persistent_step(kmr_model* m, int enable) {
+    if (!m) return KMR_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(m->mu);
+    DeviceGuard dg(m->device);
+    if (cudaDeviceSynchronize() != cudaSuccess) return KMR_ERR_CUDA;
+    m->persistent = enable != 0;
+    for (GraphEntry& e : m->graphs) cudaGraphExecDestroy(e.exec);   // captured graphs follow the old setting
+    m->graphs.clear();
+    return KMR_OK;
+}
+
 extern "C" int kmr_model_set_smem_poison(kmr_model* m, int enable, uint32_t pattern) {
     if (!m) return KMR_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(m->mu);
@@ -1255,7 +1363,8 @@ extern "C" int kmr_model_kernels_per_step(const kmr_model* m, int B) {
     }
     if (fused_qkv(c, B)) gemv_launches -= 1;                 // QKV runs inside the attention kernel
     const int head_passes = (B + kMaxHeadRows - 1) / kMaxHeadRows;
-    const int k = c.n_layers * (gemv_launches + 1) + head_passes;
+    StepPlan plan;
+    const int k = persistent_plan(m, B, &plan) ? 1 + head_passes : c.n_layers * (gemv_launches + 1) + head_passes;
     return m->poison ? 2 * k : k;                 // the diagnostic adds one fill per kernel
 }
 

@@ -40,6 +40,7 @@
 #include <cooperative_groups.h>
 #include <math.h>
 
+#include "kmr_attn_core.cuh"
 #include "kmr_int4_mma.cuh"
 #include "kmr_internal.cuh"
 
@@ -53,8 +54,8 @@ namespace {
 // KV head serves at most 2 query heads, so that NV = heads x CH stays <= 32); a ring stage
 // holds 8 warps x CH positions.
 constexpr int kMaxStages = 4;
-constexpr int kMaxRep = 4;          // query heads per KV head supported
-constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxRep = kAttnMaxRep;
+constexpr float kLog2e = kAttnLog2e;
 
 __host__ __device__ inline size_t al16a(size_t v) { return (v + 15) & ~size_t(15); }
 
@@ -228,8 +229,6 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     constexpr int kChunk = CH;                // positions a warp scores at once
     constexpr int kSub = 8 * CH;              // positions per ring stage
     static_assert(REP * CH <= 32, "one score per lane after the reduce-scatter");
-    constexpr int NV = REP * kChunk;          // partial scores per lane before the reduce-scatter
-    constexpr int JS = 32 / NV;               // lanes sharing one score after it
     constexpr int PER = REP * D / 8;          // output slice per cluster rank
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -278,8 +277,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     }
     const int nsplit = gridDim.x;
     const int Lq = cp + 1;
-    const int chunk = (((Lq + nsplit - 1) / nsplit) + 15) & ~15;
-    const int ns = (Lq + chunk - 1) / chunk;
+    int chunk, ns;
+    attn_split_plan(cp, nsplit, chunk, ns);
     if (!CLUSTER && s >= ns) return;             // (cluster mode: empty splits still merge a slice)
     const int t0 = s * chunk, t1 = min(Lq, t0 + chunk);      // t1 <= t0 for an empty split
     const int cached_end = p.fused ? min(t1, cp) : t1;
@@ -339,17 +338,9 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     // constants of the prologue, and the RoPE angles of this row's positions, before the wait
     const bool qk_warp = p.fused && warp <= REP;
     float nw[EPL], cs[EPL], sn[EPL];
-    if (qk_warp) {
-        const uint16_t* nrm = warp < REP ? p.qn_w : p.kn_w;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-            const int dim = lane * EPL + e, f = dim % (D / 2);
-            nw[e] = nrm ? bf16_to_f32(nrm[dim]) : 1.f;
-            const int axis = f < p.sec0 ? 0 : (f < p.sec0 + p.sec1 ? 1 : 2);
-            const float pos = float(p.positions[size_t(axis) * p.pos_ld + b]);
-            sincosf(pos * p.inv_freq[f], &sn[e], &cs[e]);
-        }
-    }
+    if (qk_warp)
+        attn_rope_constants<D>(warp < REP ? p.qn_w : p.kn_w, p.positions, p.pos_ld, b, p.inv_freq, p.sec0, p.sec1,
+                               lane, nw, cs, sn);
     pdl_launch_dependents();
     pdl_wait();
 
@@ -372,25 +363,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
             float x[EPL];
 #pragma unroll
             for (int e = 0; e < EPL; ++e) x[e] = src[lane * EPL + e];
-            if (qk_warp) {
-                if (isq ? p.qn_w != nullptr : p.kn_w != nullptr) {
-                    float ss = 0.f;
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) ss = __fmaf_rn(x[e], x[e], ss);
-                    const float r = rsqrtf(warp_sum(ss) / float(D) + p.eps);
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) x[e] = __fmul_rn(__fmul_rn(x[e], r), nw[e]);
-                }
-                // 3-section M-RoPE: frequency f turns the pair (f, f + D/2); the partner
-                // dim sits 16 lanes away
-                const bool lo = lane < 16;
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) {
-                    const float other = __shfl_xor_sync(0xffffffffu, x[e], 16);
-                    x[e] = lo ? __fsub_rn(__fmul_rn(x[e], cs[e]), __fmul_rn(other, sn[e]))
-                              : __fadd_rn(__fmul_rn(x[e], cs[e]), __fmul_rn(other, sn[e]));
-                }
-            }
+            if (qk_warp)
+                attn_norm_rope<D>(x, isq ? p.qn_w != nullptr : p.kn_w != nullptr, p.eps, nw, cs, sn, lane);
             if (isq) {
 #pragma unroll
                 for (int e = 0; e < EPL; ++e) qs[warp * D + lane * EPL + e] = __fmul_rn(x[e], qscale);
@@ -424,17 +398,6 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
 #pragma unroll
         for (int e = 0; e < EPL; ++e) o[hh][e] = 0.f;
     }
-    auto load_row = [&](const uint16_t* row, float (&v)[EPL]) {
-        if constexpr (EPL == 4) {
-            const uint2 u = *reinterpret_cast<const uint2*>(row + lane * 4);
-            v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
-        } else {
-            const uint32_t u = *reinterpret_cast<const uint32_t*>(row + lane * 2);
-            v[0] = bf16_lo(u); v[1] = bf16_hi(u);
-        }
-    };
-    const int myidx = lane / JS;                 // (head, position) of the score this lane completes
-    const int myhh = myidx / kChunk, myj = myidx % kChunk;
     for (int st = 0; st < nsub; ++st) {
         const int sb = st % nst;
         mbar_wait(&bar[sb], uint32_t((st / nst) & 1), p.err);
@@ -445,63 +408,16 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
             const int nv = min(kChunk, np - c0);
             const uint16_t* ks = kst + size_t(sb) * kSub * D;
             const uint16_t* vs = vst + size_t(sb) * kSub * D;
-            // rows past the end of the chunk re-read its first row (weight 0 below)
-            auto krow = [&](int j) {
-                const int i = c0 + (j < nv ? j : 0);
+            // rows past the end of the chunk re-read its first row (weight 0 in the update)
+            auto krow = [&](int j) -> const uint16_t* {
+                const int i = c0 + j;
                 return (p.fused && pa + i == cp) ? knew : ks + size_t(i) * D;
             };
-            auto vrow = [&](int j) {
-                const int i = c0 + (j < nv ? j : 0);
+            auto vrow = [&](int j) -> const uint16_t* {
+                const int i = c0 + j;
                 return (p.fused && pa + i == cp) ? vnew : vs + size_t(i) * D;
             };
-            float sc[NV];
-#pragma unroll
-            for (int j = 0; j < kChunk; ++j) {
-                float kv[EPL];
-                load_row(krow(j), kv);
-#pragma unroll
-                for (int hh = 0; hh < REP; ++hh) {
-                    float a = 0.f;
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) a = __fmaf_rn(qreg[hh][e], kv[e], a);
-                    sc[hh * kChunk + j] = a;
-                }
-            }
-            const float mine = reduce_scatter<NV>(sc, lane);
-            const bool valid = myj < nv;
-            const float sv = valid ? mine : -INFINITY;
-            // chunk maximum per head: butterfly over the lanes of the same head
-            float cm = sv;
-#pragma unroll
-            for (int off = JS; off < JS * kChunk; off <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
-            float mn[REP], cf[REP], mymn = 0.f;
-#pragma unroll
-            for (int hh = 0; hh < REP; ++hh) {
-                const float cmh = __shfl_sync(0xffffffffu, cm, hh * kChunk * JS);
-                mn[hh] = fmaxf(m[hh], cmh);
-                cf[hh] = (m[hh] == -INFINITY) ? 0.f : exp2f(__fsub_rn(m[hh], mn[hh]));
-                if (hh == myhh) mymn = mn[hh];
-            }
-            const float pme = valid ? exp2f(__fsub_rn(sv, mymn)) : 0.f;
-#pragma unroll
-            for (int hh = 0; hh < REP; ++hh) {
-                l[hh] = __fmul_rn(l[hh], cf[hh]);
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) o[hh][e] = __fmul_rn(o[hh][e], cf[hh]);
-                m[hh] = mn[hh];
-            }
-#pragma unroll
-            for (int j = 0; j < kChunk; ++j) {
-                float vv[EPL];
-                load_row(vrow(j), vv);
-#pragma unroll
-                for (int hh = 0; hh < REP; ++hh) {
-                    const float pj = __shfl_sync(0xffffffffu, pme, (hh * kChunk + j) * JS);
-                    l[hh] = __fadd_rn(l[hh], pj);
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) o[hh][e] = __fmaf_rn(pj, vv[e], o[hh][e]);
-                }
-            }
+            attn_score_chunk<D, REP, kChunk>(nv, krow, vrow, qreg, m, l, o, lane);
         }
         if (st + nst < nsub) {
             __syncthreads();                      // every warp is done with this stage
@@ -524,19 +440,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     __syncthreads();
     for (int i = tid; i < REP * D; i += kThreads) {
         const int hh = i / D, dim = i % D;
-        float mx = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) mx = fmaxf(mx, wml[(w * kMaxRep + hh) * 2]);
-        float num = 0.f, den = 0.f;
-        if (mx != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < 8; ++w) {
-                const float mw = wml[(w * kMaxRep + hh) * 2];
-                const float wt = (mw == -INFINITY) ? 0.f : exp2f(__fsub_rn(mw, mx));
-                den = __fmaf_rn(wt, wml[(w * kMaxRep + hh) * 2 + 1], den);
-                num = __fmaf_rn(wt, wo[(size_t(w) * REP + hh) * D + dim], num);
-            }
-        }
+        float mx, num, den;
+        attn_warp_merge<D, REP>(wml, wo, hh, dim, mx, num, den);
         if constexpr (CLUSTER) {
             // push this split's state for output i to the rank that merges i's slice
             if (s < ns) {
@@ -562,7 +467,6 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
         for (int k = tid; k < PER; k += kThreads) {
             // all sources' states first (independent loads), then the fixed-order sums
             float mr[kAttnClusterSplits], lr[kAttnClusterSplits], nr[kAttnClusterSplits];
-            float mx = -INFINITY;
 #pragma unroll
             for (int r = 0; r < kAttnClusterSplits; ++r) {
                 mr[r] = -INFINITY;
@@ -572,16 +476,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
                     lr[r] = recv[r * (PER + 2) + 1];
                     nr[r] = recv[r * (PER + 2) + 2 + k];
                 }
-                mx = fmaxf(mx, mr[r]);
             }
-            float num = 0.f, den = 0.f;
-#pragma unroll
-            for (int r = 0; r < kAttnClusterSplits; ++r) {
-                const float wt = (mr[r] == -INFINITY) ? 0.f : exp2f(__fsub_rn(mr[r], mx));
-                den = __fmaf_rn(wt, lr[r], den);
-                num = __fmaf_rn(wt, nr[r], num);
-            }
-            outrow[s * PER + k] = __fdiv_rn(num, den);
+            outrow[s * PER + k] = attn_split_merge(mr, lr, nr);
         }
     } else {
         // ---- global mode: one split writes directly; otherwise the last CTA merges

@@ -151,6 +151,7 @@ def test_entry_points_reject_bad_arguments_without_a_gpu(L):
     assert L.kmr_selftest_wait_timeout(2_000_000_001, None) == kmr.KMR_ERR_INVALID_ARG  # above 2 s
     assert L.kmr_model_kernels_per_step(None, 1) == 0
     assert L.kmr_model_device_bytes(None, None, None, None) == 0
+    assert L.kmr_model_set_persistent_step(None, 1) == kmr.KMR_ERR_INVALID_ARG
 
 
 def test_model_create_rejects_bad_config_on_host(L):

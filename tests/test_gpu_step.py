@@ -264,19 +264,26 @@ def test_step_ignores_stale_shared_memory(torch, B):
     m.close()
 
 
+@pytest.mark.parametrize("persistent", [True, False])
 @pytest.mark.parametrize("B", [3, 1])
 @pytest.mark.parametrize("nq,nkv", [(4, 2), (8, 2), (4, 4), (8, 4)])
-def test_head_layouts(torch, nq, nkv, B):
+def test_head_layouts(torch, nq, nkv, B, persistent):
     """1, 2 and 4 query heads per KV head (head_dim 64) match the oracle over 3
-    teacher-forced steps at batch 3 and batch 1 (the attention kernel computes the QKV rows
-    itself at one row whenever a head group gives each cluster rank whole 16-row tiles)."""
+    teacher-forced steps at batch 3 and batch 1, on the persistent step where it serves the
+    shape (2 query heads per KV head) and on the multi-kernel step (where the attention kernel
+    computes the QKV rows itself at one row whenever a head group gives each cluster rank whole
+    16-row tiles)."""
     from workloads import Workload
     cfg = tiny_config(n_q_heads=nq, n_kv_heads=nkv, slots=3)
     wl = Workload("tiny heads", cfg, 5, batch=B, prefill=[9, 40, 77][:B], rope_delta=[0, -2, -5][:B],
                   slot_ids=[1, 2, 0][:B], first_tokens=[3, 500, 77][:B], steps=3)
     m, _ = build_model(wl, max_batch=3)
+    m.set_persistent_step(persistent)
     fused = B == 1 and ((nq // nkv + 2) * cfg.head_dim) % 128 == 0      # one row: QKV in the attention
-    assert m.kernels_per_step(B) == cfg.n_layers * (4 if fused else 5) + 1
+    if persistent and nq // nkv == 2:
+        assert m.kernels_per_step(B) == 2                                # layers kernel + LM head
+    else:
+        assert m.kernels_per_step(B) == cfg.n_layers * (4 if fused else 5) + 1
     o = od.OracleDecoder.for_workload(wl)
     st = od.initial_state(wl)
     dev = Dev(torch, *st, cfg.vocab)
