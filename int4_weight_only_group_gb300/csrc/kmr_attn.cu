@@ -52,7 +52,12 @@ namespace {
 
 // A warp scores CH positions at a time (8, or 16 when a split can exceed 64 positions and a
 // KV head serves at most 2 query heads, so that NV = heads x CH stays <= 32); a ring stage
-// holds 8 warps x CH positions.
+// holds the 8 scoring warps x CH positions.  The batch-1 kernel that also computes the QKV
+// projection runs 16 warps (one 128-input group each, as the int4 GEMV does); warps 8..15 take
+// no part in the scoring, so every path scores and merges in the same order.
+constexpr int kScoreWarps = 8;
+constexpr int kAttnThreadsPlain = kScoreWarps * 32;
+constexpr int kAttnThreadsQkv = 16 * 32;
 constexpr int kMaxStages = 4;
 constexpr int kMaxRep = kAttnMaxRep;
 constexpr float kLog2e = kAttnLog2e;
@@ -75,7 +80,7 @@ __host__ __device__ inline AttnSmem attn_layout(int D, int rep, int nstage, int 
     L.qbar = o;  o += 16;
     o = (o + 127) & ~size_t(127);
     L.qw = o;    o += qkv_tb ? size_t(tpr) * qkv_tb : 0;        // this rank's QKV weight tiles
-    L.qxw = o;   o += qkv_tb ? size_t(8) * 2 * 128 * 2 : 0;     // per warp: 2 staged groups of x
+    L.qxw = o;   o += qkv_tb ? size_t(16) * 128 * 2 : 0;          // per warp: its staged group of x
     L.qxst = o;  o += qkv_tb ? size_t(16) * 16 * 4 : 0;         // per group: (X', 1/sigma) x 8 rows
     L.qss = o;   o += qkv_tb ? 16 * 4 : 0;                       // per group: sum of x^2
     L.qpart = o; o += qkv_tb ? size_t(tpr) * 16 * 16 * 4 : 0;   // per tile, per group: 16 rows
@@ -86,8 +91,8 @@ __host__ __device__ inline AttnSmem attn_layout(int D, int rep, int nstage, int 
     L.knew = o;  o += al16a(size_t(D) * 2);
     L.vnew = o;  o += al16a(size_t(D) * 2);
     L.qs = o;    o += al16a(size_t(rep) * D * 4);
-    L.wml = o;   o += al16a(size_t(8) * kMaxRep * 2 * 4);      // per warp: (m, l) per head
-    L.wo = o;    o += al16a(size_t(8) * rep * D * 4);          // per warp: o per head
+    L.wml = o;   o += al16a(size_t(kScoreWarps) * kMaxRep * 2 * 4);   // per scoring warp: (m, l) per head
+    L.wo = o;    o += al16a(size_t(kScoreWarps) * rep * D * 4);       // per scoring warp: o per head
     L.co = o;    o += al16a(size_t(rep) * D * 4);              // CTA state (global mode)
     L.cml = o;   o += al16a(size_t(kMaxRep) * 2 * 4);
     L.recv = o;  o += al16a(size_t(8) * (per + 2) * 4);        // per source rank: (m, l, slice)
@@ -109,18 +114,18 @@ __device__ __forceinline__ float tree16(const float* v, int stride) {
 }
 
 // Fused QKV projection of one cluster rank for one row (see AttnParams): stage the row's
-// RMSNorm input (warp w: groups w and w + 8), multiply this rank's QKV tiles on the tensor
-// cores, reduce each tile's 16 group partials in the one-row GEMV's fixed order, apply the
-// RMSNorm factor and push the rank's rows into every rank's q/k/v buffer.  Every step
-// mirrors the one-row int4 GEMV (kmr_gemv.cu), so a row's q, k, v are the same bits
-// whether the step ran it fused (small batches) or through the GEMV (larger ones).
+// RMSNorm input (warp w: group w), multiply this rank's QKV tiles on the tensor cores, reduce
+// each tile's 16 group partials in the one-row GEMV's fixed order, apply the RMSNorm factor
+// and push the rank's rows into every rank's q/k/v buffer.  Every step mirrors the one-row
+// int4 GEMV (kmr_gemv.cu: one group per warp at K = 2048), so a row's q, k, v are the same
+// bits whether the step ran it fused (small batches) or through the GEMV (larger ones).
 template <int D, int REP>
 __device__ __forceinline__ void qkv_phase(const AttnParams& p, uint8_t* smem, const AttnSmem& L, int s, int h,
-                                          int b, int lane, int warp, const uint2 (&nwv)[2]) {
+                                          int b, int lane, int warp, uint2 nwv) {
     constexpr int TPR = (REP + 2) * D / 128;
     const int K = p.hidden, G = K >> 7;
     const int tid = threadIdx.x;
-    __half* xw = reinterpret_cast<__half*>(smem + L.qxw) + warp * 2 * 128;
+    __half* xw = reinterpret_cast<__half*>(smem + L.qxw) + warp * 128;
     float* xst = reinterpret_cast<float*>(smem + L.qxst);
     float* ssg = reinterpret_cast<float*>(smem + L.qss);
     float* part = reinterpret_cast<float*>(smem + L.qpart);
@@ -128,12 +133,9 @@ __device__ __forceinline__ void qkv_phase(const AttnParams& p, uint8_t* smem, co
     const uint8_t* qw = smem + L.qw;
     uint64_t* qbar = reinterpret_cast<uint64_t*>(smem + L.qbar);
     const bool embed = p.x_kind == IN_EMBED_NORM;
-    float4 xv[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int g = warp + 8 * j;
-        xv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (g >= G) continue;
+    const int g = warp;
+    float4 xv = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (g < G) {
         const size_t k = size_t(g) * 128 + lane * 4;
         if (embed) {
             int tok = p.tokens[b];
@@ -142,20 +144,18 @@ __device__ __forceinline__ void qkv_phase(const AttnParams& p, uint8_t* smem, co
                 tok = 0;
             }
             const uint2 raw = *reinterpret_cast<const uint2*>(p.embed + size_t(tok) * K + k);
-            xv[j] = make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
-            if (s == 0 && h == 0 && p.x_out) *reinterpret_cast<float4*>(p.x_out + size_t(b) * K + k) = xv[j];
+            xv = make_float4(bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y));
+            if (s == 0 && h == 0 && p.x_out) *reinterpret_cast<float4*>(p.x_out + size_t(b) * K + k) = xv;
         } else {
-            xv[j] = *reinterpret_cast<const float4*>(p.x + size_t(b) * K + k);
+            xv = *reinterpret_cast<const float4*>(p.x + size_t(b) * K + k);
         }
     }
-    // (X' of both groups, sum of squares of both groups) in one reduce-scatter: lanes
-    // 8i..8i+7 end with value i (the butterfly's bits)
-    float rv[4];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int g = warp + 8 * j;
-        const float w0 = bf16_lo(nwv[j].x), w1 = bf16_hi(nwv[j].x), w2 = bf16_lo(nwv[j].y), w3 = bf16_hi(nwv[j].y);
-        float u[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+    // (X', sum of squares) of the group in one reduce-scatter: lanes 0..15 end with X',
+    // 16..31 with the sum of squares (the butterfly's bits)
+    float rv[2];
+    {
+        const float w0 = bf16_lo(nwv.x), w1 = bf16_hi(nwv.x), w2 = bf16_lo(nwv.y), w3 = bf16_hi(nwv.y);
+        float u[4] = {xv.x, xv.y, xv.z, xv.w};
         float ss = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) ss = __fmaf_rn(u[e], u[e], ss);
@@ -169,46 +169,34 @@ __device__ __forceinline__ void qkv_phase(const AttnParams& p, uint8_t* smem, co
         const __half2 h01 = __floats2half2_rn(__fmul_rn(u[0], sig), __fmul_rn(u[1], sig));
         const __half2 h23 = __floats2half2_rn(__fmul_rn(u[2], sig), __fmul_rn(u[3], sig));
         const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-        rv[j] = __fadd_rn(__fadd_rn(f01.x, f01.y), __fadd_rn(f23.x, f23.y));
-        rv[2 + j] = ss;
-        __half* blk = xw + j * 128;
-        *reinterpret_cast<__half2*>(blk + bpos(lane * 4)) = h01;
-        *reinterpret_cast<__half2*>(blk + bpos(lane * 4 + 2)) = h23;
+        rv[0] = __fadd_rn(__fadd_rn(f01.x, f01.y), __fadd_rn(f23.x, f23.y));
+        rv[1] = ss;
+        *reinterpret_cast<__half2*>(xw + bpos(lane * 4)) = h01;
+        *reinterpret_cast<__half2*>(xw + bpos(lane * 4 + 2)) = h23;
         if (lane >= 1 && lane < 16) xst[g * 16 + lane] = (g < G && lane == 1) ? isg : 0.f;
     }
-    const float tot = reduce_scatter<4>(rv, lane);
-    if ((lane & 7) == 0) {
-        const int i = lane >> 3, g = warp + 8 * (i & 1);
-        if (i < 2) xst[g * 16] = g < G ? tot : 0.f;
-        else ssg[g] = g < G ? tot : 0.f;
-    }
+    const float tot = reduce_scatter<2>(rv, lane);
+    if (lane == 0) xst[g * 16] = g < G ? tot : 0.f;
+    if (lane == 16) ssg[g] = g < G ? tot : 0.f;
     __syncwarp();
     const int gl = lane >> 2;
-    // both groups' fragments once, then all TPR x 2 block products unrolled: independent
+    // the group's fragments once, then all TPR block products unrolled: independent
     // accumulator chains the scheduler can interleave
-    XFrag xf[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) load_xfrag(xf[j], xw + j * 128, gl == 0, lane, xst + (warp + 8 * j) * 16);
+    XFrag xf;
+    load_xfrag(xf, xw, gl == 0, lane, xst + g * 16);
     mbar_wait(qbar, 0u, p.err);
-    float acc[TPR][2][4];
+    float acc[TPR][4];
 #pragma unroll
-    for (int t = 0; t < TPR; ++t)
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            acc[t][j][0] = acc[t][j][1] = acc[t][j][2] = acc[t][j][3] = 0.f;
-            if (warp + 8 * j < G)
-                group_product<false>(qw + size_t(t) * p.qkv_tile_bytes + size_t(warp + 8 * j) * kGroupBytes, xf[j],
-                                     lane, acc[t][j]);
-        }
+    for (int t = 0; t < TPR; ++t) {
+        acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+        if (g < G) group_product<false>(qw + size_t(t) * p.qkv_tile_bytes + size_t(g) * kGroupBytes, xf, lane, acc[t]);
+    }
     if ((lane & 3) == 0) {
 #pragma unroll
-        for (int t = 0; t < TPR; ++t)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int g = warp + 8 * j;
-                part[(t * 16 + g) * 16 + gl] = acc[t][j][0];
-                part[(t * 16 + g) * 16 + gl + 8] = acc[t][j][2];
-            }
+        for (int t = 0; t < TPR; ++t) {
+            part[(t * 16 + g) * 16 + gl] = acc[t][0];
+            part[(t * 16 + g) * 16 + gl + 8] = acc[t][2];
+        }
     }
     __syncthreads();
     if (tid < TPR * 16) {
@@ -223,11 +211,12 @@ __device__ __forceinline__ void qkv_phase(const AttnParams& p, uint8_t* smem, co
 }
 
 template <int D, int REP, bool CLUSTER, int CH, bool QKVF>
-__global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(QKVF ? kAttnThreadsQkv : kAttnThreadsPlain, 1) attn_kernel(const AttnParams p) {
+    constexpr int NT = QKVF ? kAttnThreadsQkv : kAttnThreadsPlain;
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int EPL = D / 32;               // contiguous dims per lane
     constexpr int kChunk = CH;                // positions a warp scores at once
-    constexpr int kSub = 8 * CH;              // positions per ring stage
+    constexpr int kSub = kScoreWarps * CH;    // positions per ring stage
     static_assert(REP * CH <= 32, "one score per lane after the reduce-scatter");
     constexpr int PER = REP * D / 8;          // output slice per cluster rank
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -259,7 +248,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
         if (s == 0) {
             pdl_wait();
             if (!fin && h == 0 && tid == 0) set_error(p.err, bad_slot ? KMR_ERR_SLOT_RANGE : KMR_ERR_CACHE_FULL);
-            for (int i = tid; i < REP * D; i += kThreads) outrow[i] = 0.f;
+            for (int i = tid; i < REP * D; i += NT) outrow[i] = 0.f;
             if constexpr (QKVF) {
                 // the layer-0 embedding still lands in the residual, as the GEMV path stores it
                 if (h == 0 && p.x_kind == IN_EMBED_NORM && p.x_out) {
@@ -268,7 +257,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
                         if (tid == 0) set_error(p.err, KMR_ERR_INVALID_ARG);
                         tok = 0;
                     }
-                    for (int k = tid; k < p.hidden; k += kThreads)
+                    for (int k = tid; k < p.hidden; k += NT)
                         p.x_out[size_t(b) * p.hidden + k] = bf16_to_f32(p.embed[size_t(tok) * p.hidden + k]);
                 }
             }
@@ -311,7 +300,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
         const int n0 = nsub < nst ? nsub : nst;
         for (int i = 0; i < n0; ++i) issue(i);
     }
-    uint2 qnw[2] = {make_uint2(0, 0), make_uint2(0, 0)};
+    uint2 qnw = make_uint2(0, 0);
     if constexpr (QKVF) {
         constexpr int TPR = (REP + 2) * D / 128, QT = REP * D / 16, KT = D / 16;
         if (tid == 0) {
@@ -328,12 +317,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
                 bulk_g2s_stream(smem + L.qw + size_t(t) * tb, p.wqkv + size_t(gt) * tb, tb, qbar, pol);
             }
         }
-        const int G = p.hidden >> 7;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int g = warp + 8 * j;
-            if (g < G) qnw[j] = *reinterpret_cast<const uint2*>(p.in_norm_w + size_t(g) * 128 + lane * 4);
-        }
+        if (warp < (p.hidden >> 7)) qnw = *reinterpret_cast<const uint2*>(p.in_norm_w + size_t(warp) * 128 + lane * 4);
     }
     // constants of the prologue, and the RoPE angles of this row's positions, before the wait
     const bool qk_warp = p.fused && warp <= REP;
@@ -380,7 +364,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
             }
         }
     } else {
-        for (int i = tid; i < REP * D; i += kThreads) qs[i] = __fmul_rn(in[size_t(h) * REP * D + i], qscale);
+        for (int i = tid; i < REP * D; i += NT) qs[i] = __fmul_rn(in[size_t(h) * REP * D + i], qscale);
     }
     __syncthreads();
 
@@ -427,18 +411,20 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
             }
         }
     }
-    // ---- merge the 8 warps (fixed order)
+    // ---- merge the 8 scoring warps (fixed order)
+    if (warp < kScoreWarps) {
 #pragma unroll
-    for (int hh = 0; hh < REP; ++hh) {
-        if (lane == 0) {
-            wml[(warp * kMaxRep + hh) * 2] = m[hh];
-            wml[(warp * kMaxRep + hh) * 2 + 1] = l[hh];
+        for (int hh = 0; hh < REP; ++hh) {
+            if (lane == 0) {
+                wml[(warp * kMaxRep + hh) * 2] = m[hh];
+                wml[(warp * kMaxRep + hh) * 2 + 1] = l[hh];
+            }
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) wo[(size_t(warp) * REP + hh) * D + lane * EPL + e] = o[hh][e];
         }
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) wo[(size_t(warp) * REP + hh) * D + lane * EPL + e] = o[hh][e];
     }
     __syncthreads();
-    for (int i = tid; i < REP * D; i += kThreads) {
+    for (int i = tid; i < REP * D; i += NT) {
         const int hh = i / D, dim = i % D;
         float mx, num, den;
         attn_warp_merge<D, REP>(wml, wo, hh, dim, mx, num, den);
@@ -464,7 +450,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     if constexpr (CLUSTER) {
         // ---- every split's state for this rank's slice is now in local shared memory
         cg::this_cluster().sync();
-        for (int k = tid; k < PER; k += kThreads) {
+        for (int k = tid; k < PER; k += NT) {
             // all sources' states first (independent loads), then the fixed-order sums
             float mr[kAttnClusterSplits], lr[kAttnClusterSplits], nr[kAttnClusterSplits];
 #pragma unroll
@@ -483,11 +469,11 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
         // ---- global mode: one split writes directly; otherwise the last CTA merges
         __syncthreads();
         if (ns == 1) {
-            for (int i = tid; i < REP * D; i += kThreads) outrow[i] = __fdiv_rn(co[i], cml[(i / D) * 2 + 1]);
+            for (int i = tid; i < REP * D; i += NT) outrow[i] = __fdiv_rn(co[i], cml[(i / D) * 2 + 1]);
             return;
         }
         float* mypart = p.part + ((size_t(b) * p.nkv + h) * p.tsplit + s) * REP * (D + 2);
-        for (int i = tid; i < REP * D; i += kThreads) mypart[(i / D) * (D + 2) + 2 + i % D] = co[i];
+        for (int i = tid; i < REP * D; i += NT) mypart[(i / D) * (D + 2) + 2 + i % D] = co[i];
         if (tid < REP) {
             mypart[tid * (D + 2)] = cml[tid * 2];
             mypart[tid * (D + 2) + 1] = cml[tid * 2 + 1];
@@ -513,20 +499,20 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
         float* mq = wo;                                   // [split][head]
         float* lq = wo + ns * REP;
         float* wq = wo + 2 * ns * REP;
-        for (int i = tid; i < ns * REP; i += kThreads) {
+        for (int i = tid; i < ns * REP; i += NT) {
             const float* pq = parts + size_t(i) * (D + 2);
             mq[i] = __ldcg(&pq[0]);
             lq[i] = __ldcg(&pq[1]);
         }
         __syncthreads();
-        for (int i = tid; i < ns * REP; i += kThreads) {
+        for (int i = tid; i < ns * REP; i += NT) {
             const int hh = i % REP;
             float mx = -INFINITY;
             for (int q = 0; q < ns; ++q) mx = fmaxf(mx, mq[q * REP + hh]);
             wq[i] = (mq[i] == -INFINITY) ? 0.f : exp2f(__fsub_rn(mq[i], mx));
         }
         __syncthreads();
-        for (int i = tid; i < REP * D; i += kThreads) {
+        for (int i = tid; i < REP * D; i += NT) {
             const int hh = i / D, dim = i % D;
             float num = 0.f, den = 0.f;
 #pragma unroll 8
@@ -559,8 +545,7 @@ const void* attn_fn(int d, int rep, int ch, bool qkv = false) {
 
 }  // namespace
 
-// Positions a warp scores at once for a launch: 16 when the longest split the cache allows
-// exceeds 64 positions and NV = rep x 16 fits a warp, else 8.
+// Positions a warp scores at once for a launch (attn_chunk_for).
 int attn_chunk(int max_len, int splits, int rep) {
     if (splits < 1) splits = 1;
     const int chunk = (((max_len + splits - 1) / splits) + 15) & ~15;
@@ -571,14 +556,14 @@ int attn_chunk(int max_len, int splits, int rep) {
 int attn_stages(int max_len, int splits, int ch, int d) {
     if (splits < 1) splits = 1;
     const int chunk = (((max_len + splits - 1) / splits) + 15) & ~15;
-    int n = (chunk + 8 * ch - 1) / (8 * ch);
-    const int cap = int((192u * 1024u) / (unsigned(8 * ch) * unsigned(d) * 4u));
+    int n = (chunk + kScoreWarps * ch - 1) / (kScoreWarps * ch);
+    const int cap = int((192u * 1024u) / (unsigned(kScoreWarps * ch) * unsigned(d) * 4u));
     if (n > kMaxStages) n = kMaxStages;
     if (n > cap) n = cap;
     return n < 1 ? 1 : n;
 }
 size_t attn_smem_bytes(int d, int rep, int nstage, int ch, int qkv_tb) {
-    return attn_layout(d, rep, nstage, 8 * ch, qkv_tb).total;
+    return attn_layout(d, rep, nstage, kScoreWarps * ch, qkv_tb).total;
 }
 bool attn_can_fuse_qkv(int d, int rep, int hidden) {
     return ((rep + 2) * d) % 128 == 0 && hidden % 128 == 0 && hidden / 128 <= 16;
@@ -599,8 +584,8 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t st, bool pdl) {
     q.nstage = attn_stages(p.S, q.tsplit, ch, p.d);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(q.tsplit, p.nkv, p.B);
-    cfg.blockDim = dim3(kThreads);
     const bool qkv = p.cluster && p.wqkv != nullptr && attn_can_fuse_qkv(p.d, rep, p.hidden);
+    cfg.blockDim = dim3(qkv ? kAttnThreadsQkv : kAttnThreadsPlain);
     if (!qkv) q.wqkv = nullptr;
     cfg.dynamicSmemBytes = attn_smem_bytes(p.d, rep, q.nstage, ch, qkv ? p.qkv_tile_bytes : 0);
     cfg.stream = st;
