@@ -682,9 +682,10 @@ def sweep() -> None:
 
 
 # ------------------------------------------------------------------ main
-def prefill_only(T: int) -> None:
+def prefill_only(T: int, tcgen05: bool = False) -> None:
     """Two kmr_prefill calls of T seeded tokens into slot 0 of the batch-1 model (a fixed
-    command for ncu launch lists of prefill); prints one status line."""
+    command for ncu launch lists of prefill), on the tcgen05 projections if asked; prints one
+    status line."""
     import torch
     import int4_weight_only_group_gb300 as kmr
     from int4_weight_only_group_gb300 import driver
@@ -695,6 +696,7 @@ def prefill_only(T: int) -> None:
     driver.load_weights(model, SyntheticModel(cfg, wl.seed), cfg.n_layers, cfg.qk_norm)
     T = min(T, cfg.max_len)
     model.reserve_prefill(T)
+    model.set_prefill_tcgen05(tcgen05)
     g = torch.Generator(device="cuda").manual_seed(1)
     toks = torch.randint(1, cfg.vocab - 1, (T,), generator=g, device="cuda", dtype=torch.int32)
     pos = torch.arange(T, dtype=torch.int32, device="cuda").repeat(3, 1).contiguous()
@@ -770,6 +772,8 @@ def main():
                     help="time only the decode steps (no standalone GEMV timing, e2e or CPU legs; for launch lists)")
     ap.add_argument("--prefill-only", type=int, default=0, metavar="T",
                     help="only run two T-token prefills on the batch-1 model and exit (for profiling)")
+    ap.add_argument("--prefill-tcgen05", action="store_true",
+                    help="with --prefill-only: run the projections on the tcgen05 kernel")
     ap.add_argument("--sweep", action="store_true",
                     help="only run the standalone int4 GEMV and decode-attention sweeps and exit")
     ap.add_argument("--oracle-leg", choices=tuple(ORACLE_LEGS), default=None,
@@ -794,7 +798,7 @@ def _main(args):
         sweep()
         return
     if args.prefill_only:
-        prefill_only(args.prefill_only)
+        prefill_only(args.prefill_only, args.prefill_tcgen05)
         return
     if args.skip_extras:
         args.no_cpu_baseline = True

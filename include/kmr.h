@@ -405,6 +405,18 @@ int kmr_model_set_smem_poison(kmr_model* m, int enable, uint32_t pattern);
  * kmr_prefill call.  Returns KMR_OK or KMR_ERR_INVALID_ARG (null model). */
 int kmr_model_set_prefill_tcgen05(kmr_model* m, int enable);
 
+/* Tile shape of the tcgen05 prefill projections: nt tokens per CTA (64, 128
+ * or 256; the MMA's N) and the K range split over ksplit CTAs of one
+ * thread-block cluster (1, 2 or 4; a projection with fewer 128-input groups
+ * takes the largest power of two that fits), whose fp32 partials are summed
+ * in rank order through distributed shared memory.  nt = ksplit = 0 (the
+ * default) plans each projection from its shape: N x K, the prompt length and
+ * the SM count.  The result does not depend on the K split beyond fp32
+ * rounding, and the same plan always gives the same bits.  Takes effect from
+ * the next kmr_prefill call.  Returns KMR_OK or KMR_ERR_INVALID_ARG (null
+ * model, or a value outside those sets). */
+int kmr_model_set_prefill_plan(kmr_model* m, int nt, int ksplit);
+
 /* Whether the decode step runs its layers as one persistent kernel (default
  * on).  The persistent kernel keeps one CTA per SM for the whole step: each
  * CTA streams its share of every layer's int4 weights and its attention

@@ -109,6 +109,7 @@ _SIGNATURES = {
     "kmr_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
     "kmr_model_set_smem_poison": (_I, [_P, _I, ctypes.c_uint32]),
     "kmr_model_set_prefill_tcgen05": (_I, [_P, _I]),
+    "kmr_model_set_prefill_plan": (_I, [_P, _I, _I]),
     "kmr_model_set_persistent_step": (_I, [_P, _I]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
@@ -349,6 +350,10 @@ class Model:
     def set_prefill_tcgen05(self, enable: bool) -> None:
         """kmr_model_set_prefill_tcgen05: run prefill projections on the tcgen05 kernel."""
         _check(lib().kmr_model_set_prefill_tcgen05(self._h, int(bool(enable))), "kmr_model_set_prefill_tcgen05")
+
+    def set_prefill_plan(self, nt: int = 0, ksplit: int = 0) -> None:
+        """kmr_model_set_prefill_plan: force the tcgen05 tile width / K split (0, 0: planned)."""
+        _check(lib().kmr_model_set_prefill_plan(self._h, int(nt), int(ksplit)), "kmr_model_set_prefill_plan")
 
     def set_persistent_step(self, enable: bool) -> None:
         """kmr_model_set_persistent_step: run the step's layers as one persistent kernel."""

@@ -358,6 +358,7 @@ struct kmr_model {
     unsigned long long tick = 0;
     bool poison = false;           // diagnostic: fill shared memory before every kernel of the step
     bool prefill_tc = false;       // prefill projections on tcgen05 (kmr_model_set_prefill_tcgen05)
+    int pf_nt = 0, pf_ks = 0;      // forced tcgen05 tile width / K split (0: planned per projection)
     // persistent step (kmr_step.cu): every layer in one kernel for batches it serves
     bool persistent = false;       // kmr_model_set_persistent_step (opt-in: slower than the PDL-chained step, see header)
     bool persistent_failed = false;    // a capture of it failed: this model uses the multi-kernel step
@@ -697,7 +698,13 @@ int enqueue_projection(kmr_model* m, const GemvLaunch& g, int T, cudaStream_t st
         tp.eps = g.eps;
         tp.M = T;
         tp.K = g.g.K;
-        tp.nt = tc_gemm_pick_nt(g.g.N, T, m->sms);
+        TcPlan plan = tc_gemm_plan(g.g.N, g.g.K, T, m->sms);
+        if (m->pf_nt) {
+            plan.nt = m->pf_nt;
+            plan.ksplit = m->pf_ks;
+            while (plan.ksplit > g.g.K / 128) plan.ksplit >>= 1;
+        }
+        tp.nt = plan.nt;
         tp.xs = m->pxs;
         tp.rs = m->prn;
         tp.err = m->err;
@@ -710,6 +717,7 @@ int enqueue_projection(kmr_model* m, const GemvLaunch& g, int T, cudaStream_t st
         tg.rs = m->prn;
         tg.M = T;
         tg.nt = tp.nt;
+        tg.ksplit = plan.ksplit;
         tg.epi = g.epi;
         tg.y = g.y;
         tg.ldy = g.ldy;
@@ -1172,7 +1180,7 @@ extern "C" int kmr_model_reserve_prefill(kmr_model* m, int max_tokens) {
         dalloc(m, &m->pattn, T * qd * 4) || dalloc(m, &m->pact, T * c.intermediate * 4) ||
         dalloc(m, &m->pslot, T * 4) || dalloc(m, &m->pcpos, T * 4))
         return KMR_ERR_CUDA;
-    const size_t Mpad = size_t(gemm_rows_pad(max_tokens));
+    const size_t Mpad = size_t(std::max(gemm_rows_pad(max_tokens), tc_rows_pad(max_tokens)));
     const size_t Gmax = size_t(std::max(std::max(c.hidden, qd), c.intermediate) / 128);
     if (dalloc(m, &m->pxs, Gmax * Mpad * 128 * 2) || dalloc(m, &m->pxst, Gmax * Mpad * 8) ||
         dalloc(m, &m->prn, Mpad * 4))
@@ -1239,6 +1247,17 @@ extern "C" int kmr_model_set_prefill_tcgen05(kmr_model* m, int enable) {
     if (!m) return KMR_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(m->mu);
     m->prefill_tc = enable != 0;
+    return KMR_OK;
+}
+
+extern "C" int kmr_model_set_prefill_plan(kmr_model* m, int nt, int ksplit) {
+    if (!m) return KMR_ERR_INVALID_ARG;
+    const bool automatic = nt == 0 && ksplit == 0;
+    if (!automatic && !((nt == 64 || nt == 128 || nt == 256) && (ksplit == 1 || ksplit == 2 || ksplit == 4)))
+        return KMR_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(m->mu);
+    m->pf_nt = nt;
+    m->pf_ks = ksplit;
     return KMR_OK;
 }
 

@@ -9,9 +9,9 @@ namespace kmr {
 // Staging of one projection's input rows for tc_gemm: row t of x (optionally through the
 // RMSNorm weight, or the embedding of tokens[t]) as fp16 scaled by a per-row power of two
 // sigma_t, in the tensor cores' K-major core-matrix layout, one contiguous block per
-// (token tile of nt rows, 128-input group):
-//     half offset = ((t / nt) * (K / 128) + k / 128) * nt * 128
-//                   + ((t % nt) / 8) * 1024 + ((k % 128) / 8) * 64 + (t % 8) * 8 + k % 8
+// (token tile of nt rows, 128-input group, quarter of the group):
+//     half offset = ((t / nt) * (K / 128) + k / 128) * nt * 128 + ((k % 128) / 32) * nt * 32
+//                   + ((t % nt) / 8) * 256 + ((k % 32) / 8) * 64 + (t % 8) * 8 + k % 8
 // and rs[t] = r_t / sigma_t (r_t the RMSNorm factor, 1 without norm).  Rows t >= M up to
 // the tile boundary are zero with rs = 0.
 struct TcStageParams {
@@ -37,13 +37,21 @@ struct TcGemmParams {
     const uint16_t* xs;
     const float* rs;
     int M, nt, epi;
+    int ksplit;                  // CTAs along K (a thread-block cluster): 1, 2 or 4, <= K / 128
     float* y;
     int ldy;
     int* err;
 };
 
+struct TcPlan {
+    int nt;                      // tokens per CTA: 64, 128 or 256
+    int ksplit;
+};
+
 bool tc_gemm_supported(int N, int K);
-int tc_gemm_pick_nt(int N, int M, int sms);
+// Staged rows to allocate for M tokens (every tile width's padding).
+int tc_rows_pad(int M);
+TcPlan tc_gemm_plan(int N, int K, int M, int sms);
 cudaError_t tc_gemm_set_attributes();
 cudaError_t launch_tc_stage(const TcStageParams& p, cudaStream_t st);
 cudaError_t launch_tc_gemm(const TcGemmParams& p, cudaStream_t st);

@@ -147,6 +147,7 @@ def test_entry_points_reject_bad_arguments_without_a_gpu(L):
     assert L.kmr_model_destroy(None) == kmr.KMR_ERR_INVALID_ARG
     assert L.kmr_model_sync_status(None, None) == kmr.KMR_ERR_INVALID_ARG
     assert L.kmr_model_set_prefill_tcgen05(None, 1) == kmr.KMR_ERR_INVALID_ARG
+    assert L.kmr_model_set_prefill_plan(None, 0, 0) == kmr.KMR_ERR_INVALID_ARG
     assert L.kmr_selftest_wait_timeout(999, None) == kmr.KMR_ERR_INVALID_ARG          # below 1 us
     assert L.kmr_selftest_wait_timeout(2_000_000_001, None) == kmr.KMR_ERR_INVALID_ARG  # above 2 s
     assert L.kmr_model_kernels_per_step(None, 1) == 0

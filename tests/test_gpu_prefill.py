@@ -27,10 +27,13 @@ def torch():
 
 
 def _model(cfg, seed=0, cap=None, max_batch=1, tc=False):
+    """tc: False (warp-level kernel), True (tcgen05, planned tiles) or (nt, ksplit) forced."""
     syn = SyntheticModel(cfg, seed)
     m = kmr.Model.from_config(cfg, max_batch=max_batch)
     driver.load_weights(m, syn, cfg.n_layers, cfg.qk_norm)
-    m.set_prefill_tcgen05(tc)
+    m.set_prefill_tcgen05(bool(tc))
+    if isinstance(tc, tuple):
+        m.set_prefill_plan(*tc)
     if cap:
         m.reserve_prefill(cap)
     return m, syn
@@ -72,7 +75,7 @@ def _cache(m, cfg, slot):
     return out
 
 
-TC = pytest.mark.parametrize("tc", [False, True], ids=["mma", "tcgen05"])
+TC = pytest.mark.parametrize("tc", [False, True, (256, 2), (64, 4)], ids=["mma", "tcgen05", "tc256x2", "tc64x4"])
 
 
 @TC
@@ -211,6 +214,40 @@ def test_tcgen05_prefill_agrees_with_the_default_kernel(torch):
     assert np.array_equal(pa, pb) and ca == cb == T
     for x, y in zip(ka, kb):
         assert rel_l2(od.bf16_to_f64(y[:, :T]), od.bf16_to_f64(x[:, :T])) <= REL_L2_TOL
+
+
+_PLAN_REF = {}
+
+
+@pytest.mark.parametrize("plan", [(64, 1), (128, 2), (256, 1), (256, 4), (64, 4), (128, 4)],
+                         ids=lambda p: f"nt{p[0]}_ks{p[1]}")
+def test_tcgen05_tile_plans_agree(torch, plan):
+    """Every tcgen05 tile width (64, 128, 256 tokens per CTA) and K split (1, 2, 4 CTAs of one
+    cluster, partials summed in rank order) on a 200-token prompt (a ragged last tile for each
+    width) of two 2B-shaped layers: within the parity bar of the default kernel, and the same
+    plan run twice gives the same bits."""
+    cfg = layer2b_config(slots=1, n_layers=2)
+    T = 200
+    toks, pos = _prompt(cfg, T, seed=12, delta=3)
+    if "ref" not in _PLAN_REF:
+        m, _ = _model(cfg, cap=T, tc=False)
+        st = State(torch, cfg.vocab)
+        _prefill(torch, m, toks, pos, 0, 0, st)
+        _PLAN_REF["ref"] = (st.logits.cpu().numpy(), _cache(m, cfg, 0))
+        m.close()
+    la, ka = _PLAN_REF["ref"]
+    m, _ = _model(cfg, cap=T, tc=plan)
+    runs = []
+    for _ in range(2):
+        st = State(torch, cfg.vocab)
+        _prefill(torch, m, toks, pos, 0, 0, st)
+        runs.append((st.logits.cpu().numpy(), _cache(m, cfg, 0)))
+    m.close()
+    (lb, kb), (lc, kc) = runs
+    assert rel_l2(lb, la) <= REL_L2_TOL
+    for x, y in zip(ka, kb):
+        assert rel_l2(od.bf16_to_f64(y[:, :T]), od.bf16_to_f64(x[:, :T])) <= REL_L2_TOL
+    assert np.array_equal(lb, lc) and all(np.array_equal(x, y) for x, y in zip(kb, kc))
 
 
 def test_prefill_argument_errors(torch):
