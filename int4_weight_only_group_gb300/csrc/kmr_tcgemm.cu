@@ -97,6 +97,26 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
 }
+// Issue of a 32x32b.x16 load (thread i: TMEM lane base + i, 16 consecutive columns); the
+// registers are valid after tc_wait_ld16 on the same array.
+__device__ __forceinline__ void tc_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+// Waits for this thread's TMEM loads; the registers pass through so that no use of them can be
+// scheduled before the wait.
+__device__ __forceinline__ void tc_wait_ld16(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15])
+                 :
+                 : "memory");
+}
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
     asm volatile(
@@ -460,9 +480,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcGemmPara
         const uint32_t lane_base = taddr + (uint32_t(q * 32) << 16);
         const int cbeg = chalf * (NT / 2), cend = cbeg + NT / 2;
         if (have_acc && nsplit == 1) {
-            // residual rows of the next 16 tokens are loaded while this chunk is processed
+            // chunks of 16 token columns: the TMEM load and the residual rows of chunk c + 1 are in
+            // flight while chunk c is processed
+            constexpr int kChunks = NT / 32;
+            static_assert(kChunks % 2 == 0, "chunk pairs");
             const bool resid = p.epi == EPI_RESID && n < p.N;
-            float res_next[16];
             auto load_res = [&](int c0, float (&r)[16]) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
@@ -470,28 +492,52 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcGemmPara
                     r[j] = (resid && t < p.M) ? p.y[size_t(t) * p.ldy + n] : 0.f;
                 }
             };
-            load_res(cbeg, res_next);
-#pragma unroll 1
-            for (int c0 = cbeg; c0 < cend; c0 += 16) {
-                float v[16], res[16];
+            auto process = [&](int c0, const uint32_t (&v)[16], const float (&res)[16]) {
+                if (p.epi == EPI_SILU) {
+                    // tokens in pairs: the gate lanes (tile rows 0..7) finish token j, the up lanes
+                    // (rows 8..15) token j + 1, each with the partner row's value by shuffle
+                    const bool lo = (lane & 15) < 8;
+                    const int jj = (n >> 4) * 8 + (lane & 7);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) res[j] = res_next[j];
-                if (c0 + 16 < cend) load_res(c0 + 16, res_next);
-                tc_ld16(lane_base + uint32_t(c0), v);
+                    for (int j = 0; j < 16; j += 2) {
+                        const float xa = __fmul_rn(__uint_as_float(v[j]), rs_s[c0 + j]);
+                        const float xb = __fmul_rn(__uint_as_float(v[j + 1]), rs_s[c0 + j + 1]);
+                        const float dn = __shfl_down_sync(0xffffffffu, xa, 8);
+                        const float upb = __shfl_up_sync(0xffffffffu, xb, 8);
+                        const float gate = lo ? xa : upb, up = lo ? dn : xb;
+                        const int t = ttile * NT + c0 + j + (lo ? 0 : 1);
+                        if (t < p.M && jj < p.N / 2) p.y[size_t(t) * p.ldy + jj] = tc_silu_mul(gate, up);
+                    }
+                } else {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int t = ttile * NT + c0 + j;
-                    const float x = __fmul_rn(v[j], rs_s[c0 + j]);
-                    if (p.epi == EPI_SILU) {
-                        const float up = __shfl_down_sync(0xffffffffu, x, 8);
-                        if ((lane & 15) < 8 && t < p.M) {
-                            const int jj = (n >> 4) * 8 + (lane & 7);
-                            if (jj < p.N / 2) p.y[size_t(t) * p.ldy + jj] = tc_silu_mul(x, up);
-                        }
-                    } else if (t < p.M && n < p.N) {
-                        p.y[size_t(t) * p.ldy + n] = p.epi == EPI_RESID ? __fadd_rn(res[j], x) : x;
+                    for (int j = 0; j < 16; ++j) {
+                        const int t = ttile * NT + c0 + j;
+                        const float x = __fmul_rn(__uint_as_float(v[j]), rs_s[c0 + j]);
+                        if (t < p.M && n < p.N) p.y[size_t(t) * p.ldy + n] = p.epi == EPI_RESID ? __fadd_rn(res[j], x) : x;
                     }
                 }
+            };
+            uint32_t va[16], vb[16];
+            float ra[16], rb[16];
+            tc_ld16_issue(lane_base + uint32_t(cbeg), va);
+            load_res(cbeg, ra);
+            tc_wait_ld16(va);
+            // chunk pairs (kChunks is even): va / ra hold the even chunk, vb / rb the odd one
+#pragma unroll 1
+            for (int ci = 0; ci < kChunks; ci += 2) {
+                const int c0 = cbeg + ci * 16;
+                tc_ld16_issue(lane_base + uint32_t(c0 + 16), vb);
+                load_res(c0 + 16, rb);
+                process(c0, va, ra);
+                tc_wait_ld16(vb);
+                const bool more = ci + 2 < kChunks;
+                if (more) {
+                    tc_ld16_issue(lane_base + uint32_t(c0 + 32), va);
+                    load_res(c0 + 32, ra);
+                }
+                process(c0 + 16, vb, rb);
+                if (more) tc_wait_ld16(va);
+                if (warp == 2 && lane == 0) TC_MARK(40 + ci / 2, 1);
             }
         } else if (nsplit > 1) {
             // park the partial: part[c][r] = accumulator of weight row r, token column c (the
