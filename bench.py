@@ -92,8 +92,11 @@ def measured_peaks() -> dict:
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured (MEASURED_PEAKS.json)"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        out = {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured (MEASURED_PEAKS.json)"}
+        if "bf16_tflops" in d:
+            out["bf16_tflops"] = float(d["bf16_tflops"])
+        return out
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
 def profile_traffic(summary: str):
@@ -288,10 +291,10 @@ def run_kmr(args, batch: int, rank: int, world: int, extras: bool) -> dict:
     # ---- slot migration: one whole cache row (every layer, K and V) per copy_row_from
     out["kv_copy"] = time_kv_copy(torch, model, cfg)
     # ---- text prefill of a 512-token prompt into slot 0 (after the timed decode region)
-    out["prefill"] = time_prefill(torch, model, cfg)
-    model.set_prefill_tcgen05(True)                 # the tensor-core (tcgen05) projections, for comparison
-    out["prefill_tcgen05"] = time_prefill(torch, model, cfg)
-    model.set_prefill_tcgen05(False)
+    out["prefill"] = time_prefill(torch, model, cfg)          # the default tcgen05 projections
+    model.set_prefill_tcgen05(False)                # the warp-level mma projections, for comparison
+    out["prefill_mma"] = time_prefill(torch, model, cfg)
+    model.set_prefill_tcgen05(True)
     # ---- shared-prefix attention vs plain attention on the same contexts
     out["cascade"] = time_cascade(torch, kmr, cfg)
     model.close()
@@ -682,7 +685,27 @@ def sweep() -> None:
 
 
 # ------------------------------------------------------------------ main
-def prefill_only(T: int, tcgen05: bool = False) -> None:
+def projection_flop(cfg, T: int) -> float:
+    """Multiply-add flops (2 per weight and token) of every layer's int4 projections over T tokens."""
+    per_token = sum(n * k for n, k in cfg.linear_shapes().values())
+    return 2.0 * per_token * T * cfg.n_layers
+
+
+def prefill_record(r: dict, cfg, peaks: dict) -> dict:
+    """The prefill object of the JSON line: the default (tcgen05) path, its projections' achieved
+    flop rate against the measured bf16 dense peak (fp16 has the same nominal tensor rate), and the
+    warp-level mma path beside it."""
+    pf = r["prefill"]
+    flop = projection_flop(cfg, pf["tokens"])
+    tflops = flop / (pf["ms"] * 1e-3) / 1e12
+    return {"tokens": pf["tokens"], "ms": round(pf["ms"], 3), "tok_s": round(pf["tok_s"], 1), "kernel": "tcgen05",
+            "projection_tflop": round(flop / 1e12, 4), "projection_tflops_whole_prefill": round(tflops, 1),
+            "frac_of_bf16_peak": round(tflops / peaks["bf16_tflops"], 3) if peaks.get("bf16_tflops") else None,
+            "warp_mma_ms": round(r["prefill_mma"]["ms"], 3),
+            "speedup_over_warp_mma": round(r["prefill_mma"]["ms"] / pf["ms"], 3)}
+
+
+def prefill_only(T: int, mma: bool = False) -> None:
     """Two kmr_prefill calls of T seeded tokens into slot 0 of the batch-1 model (a fixed
     command for ncu launch lists of prefill), on the tcgen05 projections if asked; prints one
     status line."""
@@ -696,7 +719,7 @@ def prefill_only(T: int, tcgen05: bool = False) -> None:
     driver.load_weights(model, SyntheticModel(cfg, wl.seed), cfg.n_layers, cfg.qk_norm)
     T = min(T, cfg.max_len)
     model.reserve_prefill(T)
-    model.set_prefill_tcgen05(tcgen05)
+    model.set_prefill_tcgen05(not mma)
     g = torch.Generator(device="cuda").manual_seed(1)
     toks = torch.randint(1, cfg.vocab - 1, (T,), generator=g, device="cuda", dtype=torch.int32)
     pos = torch.arange(T, dtype=torch.int32, device="cuda").repeat(3, 1).contiguous()
@@ -772,8 +795,8 @@ def main():
                     help="time only the decode steps (no standalone GEMV timing, e2e or CPU legs; for launch lists)")
     ap.add_argument("--prefill-only", type=int, default=0, metavar="T",
                     help="only run two T-token prefills on the batch-1 model and exit (for profiling)")
-    ap.add_argument("--prefill-tcgen05", action="store_true",
-                    help="with --prefill-only: run the projections on the tcgen05 kernel")
+    ap.add_argument("--prefill-mma", action="store_true",
+                    help="with --prefill-only: run the projections on the warp-level mma kernel")
     ap.add_argument("--sweep", action="store_true",
                     help="only run the standalone int4 GEMV and decode-attention sweeps and exit")
     ap.add_argument("--oracle-leg", choices=tuple(ORACLE_LEGS), default=None,
@@ -798,7 +821,7 @@ def _main(args):
         sweep()
         return
     if args.prefill_only:
-        prefill_only(args.prefill_only, args.prefill_tcgen05)
+        prefill_only(args.prefill_only, args.prefill_mma)
         return
     if args.skip_extras:
         args.no_cpu_baseline = True
@@ -859,9 +882,7 @@ def _main(args):
                          "plain_us": round(r["cascade"]["plain"]["us"], 2),
                          "cascade_kv_bytes": r["cascade"]["cascade"]["kv_bytes"],
                          "plain_kv_bytes": r["cascade"]["plain"]["kv_bytes"]},
-        "prefill": {"tokens": r["prefill"]["tokens"], "ms": round(r["prefill"]["ms"], 3),
-                    "tok_s": round(r["prefill"]["tok_s"], 1),
-                    "tcgen05_ms": round(r["prefill_tcgen05"]["ms"], 3)},
+        "prefill": prefill_record(r, cfg, peaks),
         "kv_row_copy": {"us": round(r["kv_copy"]["us"], 2), "gbs": round(r["kv_copy"]["gbs"], 1),
                         "frac": round(r["kv_copy"]["gbs"] / peaks["hbm_gbs"], 3), "bytes": r["kv_copy"]["bytes"]},
         "gpu_launches": r["kernels_per_step"] * args.steps,

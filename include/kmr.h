@@ -394,15 +394,16 @@ int kmr_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
 int kmr_model_set_smem_poison(kmr_model* m, int enable, uint32_t pattern);
 
 /* Prefill projections on the 5th-generation tensor cores (the prefill of
- * "kaminari", §04 Request lifecycle; the projections of §07).  With enable = 1,
- * kmr_prefill runs every projection whose output rows are a multiple of 128
- * as a tcgen05.mma kernel: the group's int4 weights dequantised to fp16 in
- * shared memory, the staged tokens as fp16 scaled by a per-row power of two,
- * fp32 accumulation in tensor memory across all of K.  Results agree with the
- * default (legacy warp-level mma) prefill within rounding and are
- * parity-tested against the oracle the same way; the default stays the
- * warp-level kernel, which is faster today.  Takes effect from the next
- * kmr_prefill call.  Returns KMR_OK or KMR_ERR_INVALID_ARG (null model). */
+ * "kaminari", §04 Request lifecycle; the projections of §07).  With enable = 1
+ * (the default), kmr_prefill runs every projection whose output rows are a
+ * multiple of 128 as a tcgen05.mma kernel: each 128-input group's int4 weights
+ * dequantised to fp16 in tensor memory, the staged tokens as fp16 scaled by a
+ * per-row power of two, fp32 accumulation in tensor memory across the CTA's K
+ * range.  enable = 0 selects the warp-level mma kernel.  The two agree within
+ * rounding and are parity-tested against the oracle the same way; on either,
+ * a token's result does not depend on the prompt length or chunking.  Takes
+ * effect from the next kmr_prefill call.  Returns KMR_OK or
+ * KMR_ERR_INVALID_ARG (null model). */
 int kmr_model_set_prefill_tcgen05(kmr_model* m, int enable);
 
 /* Tile shape of the tcgen05 prefill projections: nt tokens per CTA (64, 128
@@ -418,7 +419,10 @@ int kmr_model_set_prefill_tcgen05(kmr_model* m, int enable);
 int kmr_model_set_prefill_plan(kmr_model* m, int nt, int ksplit);
 
 /* Whether the decode step runs its layers as one persistent kernel (default
- * on).  The persistent kernel keeps one CTA per SM for the whole step: each
+ * off: on GB300 it measured slower than the multi-kernel step, whose
+ * programmatic-dependent-launch hand-off between kernels costs less than the
+ * persistent kernel's grid-wide phase barriers; it stays selectable and is
+ * parity-tested).  The persistent kernel keeps one CTA per SM for the whole step: each
  * CTA streams its share of every layer's int4 weights and its attention
  * splits' K/V rows through a ring of shared-memory slots (cp.async.bulk),
  * phases (QKV, attention, O, gate_up, down of each layer) start when every CTA

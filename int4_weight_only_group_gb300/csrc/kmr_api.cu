@@ -357,7 +357,7 @@ struct kmr_model {
     std::vector<GraphEntry> graphs;
     unsigned long long tick = 0;
     bool poison = false;           // diagnostic: fill shared memory before every kernel of the step
-    bool prefill_tc = false;       // prefill projections on tcgen05 (kmr_model_set_prefill_tcgen05)
+    bool prefill_tc = true;        // prefill projections on tcgen05 (kmr_model_set_prefill_tcgen05)
     int pf_nt = 0, pf_ks = 0;      // forced tcgen05 tile width / K split (0: planned per projection)
     // persistent step (kmr_step.cu): every layer in one kernel for batches it serves
     bool persistent = false;       // kmr_model_set_persistent_step (opt-in: slower than the PDL-chained step, see header)

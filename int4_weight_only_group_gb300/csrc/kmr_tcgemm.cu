@@ -678,27 +678,46 @@ bool tc_gemm_supported(int N, int K) { return N > 0 && N % kTcRows == 0 && K > 0
 
 int tc_rows_pad(int M) { return (M + 255) / 256 * 256; }
 
-// Tile width (tokens per CTA) and K split for an N x K projection of M tokens: the modelled
-// time of each choice is waves x (groups per CTA x group time + fixed cost), with the group
-// times measured for M = 128 MMAs (a 128 x N x 16 MMA costs the same for any N <= 128; N = 256
-// runs at the full rate) and the fixed cost of a CTA (prologue, epilogue, and the split merge).
-TcPlan tc_gemm_plan(int N, int K, int M, int sms) {
+// Tile width (tokens per CTA) and K split for an N x K projection of M tokens.  The modelled time
+// of a choice is waves x (groups per CTA x group time + fixed cost), with group times measured for
+// M = 128 MMAs (a 128 x N x 16 MMA costs about the same for any N <= 128; N = 256 runs at the full
+// rate) and the fixed cost of a CTA (prologue, epilogue, and the split merge).  The K split fixes
+// the order of each output's fp32 sums, so it depends on the projection's shape only (chosen for a
+// 512-token chunk): a token's result is then the same whatever the prompt length or chunking.
+// The tile width follows M; it does not change any output's arithmetic.
+namespace {
+double tc_model_us(int nt, int ks, int N, int K, int M, int sms) {
     const int G = K / 128, tiles = N / kTcRows;
-    TcPlan best = {64, 1};
-    double best_t = 1e30;
+    const long long ctas = (long long)tiles * ((M + nt - 1) / nt) * ks;
+    const long long waves = (ctas + sms - 1) / sms;
+    const double group_us = nt == 256 ? 0.55 : 0.33;
+    const double fixed_us = 2.0 + (ks > 1 ? 0.5 + nt * 0.006 : 0.0);
+    return double(waves) * (double((G + ks - 1) / ks) * group_us + fixed_us);
+}
+}  // namespace
+
+TcPlan tc_gemm_plan(int N, int K, int M, int sms) {
+    const int G = K / 128;
     const int nts[3] = {256, 128, 64};
-    for (int nt : nts) {
-        for (int ks = 1; ks <= kTcMaxSplit; ks *= 2) {
-            if (ks > G) break;
-            const long long ctas = (long long)tiles * ((M + nt - 1) / nt) * ks;
-            const long long waves = (ctas + sms - 1) / sms;
-            const double group_us = nt == 256 ? 0.55 : 0.33;
-            const double fixed_us = 2.0 + (ks > 1 ? 0.5 + nt * 0.006 : 0.0);
-            const double t = double(waves) * (double((G + ks - 1) / ks) * group_us + fixed_us);
-            if (t < best_t * 0.999) {
-                best_t = t;
-                best = {nt, ks};
+    // the split: best at the reference chunk
+    int ks_best = 1;
+    double t_ref = 1e30;
+    for (int nt : nts)
+        for (int ks = 1; ks <= kTcMaxSplit && ks <= G; ks *= 2) {
+            const double t = tc_model_us(nt, ks, N, K, 512, sms);
+            if (t < t_ref * 0.999) {
+                t_ref = t;
+                ks_best = ks;
             }
+        }
+    // the tile width: best for this M with that split
+    TcPlan best = {64, ks_best};
+    double bt = 1e30;
+    for (int nt : nts) {
+        const double t = tc_model_us(nt, ks_best, N, K, M, sms);
+        if (t < bt * 0.999) {
+            bt = t;
+            best.nt = nt;
         }
     }
     return best;

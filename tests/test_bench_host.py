@@ -65,3 +65,14 @@ def test_oracle_leg_times_whole_steps():
     import json
     d = json.loads(r.stdout.strip().splitlines()[-1])
     assert d["steps"] == 2 and len(d["s_per_step"]) == 2 and d["extrapolated"] is False and d["tok_per_s"] > 0
+
+
+def test_projection_flop_counts_every_layer_projection():
+    """2 flops per weight and token over QKV, O, gate_up and down of every layer (2B shapes:
+    4096 x 2048 + 2048 x 2048 + 12288 x 2048 + 2048 x 6144 weights per layer)."""
+    import bench
+    from workloads import layer2b_config
+    cfg = layer2b_config(slots=1, n_layers=28)
+    per_layer = 4096 * 2048 + 2048 * 2048 + 12288 * 2048 + 2048 * 6144
+    assert bench.projection_flop(cfg, 512) == 2.0 * per_layer * 512 * 28
+    assert bench.projection_flop(cfg, 0) == 0.0

@@ -216,6 +216,28 @@ def test_tcgen05_prefill_agrees_with_the_default_kernel(torch):
         assert rel_l2(od.bf16_to_f64(y[:, :T]), od.bf16_to_f64(x[:, :T])) <= REL_L2_TOL
 
 
+def test_tcgen05_chunked_prefill_2b_bitwise(torch):
+    """On 2B-shaped projections, where the chunk sizes take different tcgen05 tile widths, a
+    chunked prefill equals the one-chunk prefill bit for bit: the K split (the only plan choice
+    that changes an output's sums) depends on the projection's shape alone."""
+    cfg = layer2b_config(slots=1, n_layers=2)
+    T = 300
+    toks, pos = _prompt(cfg, T, seed=21)
+    a, _ = _model(cfg, cap=T, tc=True)
+    sa = State(torch, cfg.vocab)
+    _prefill(torch, a, toks, pos, 0, 0, sa)
+    la, ka = sa.logits.cpu().numpy(), _cache(a, cfg, 0)
+    a.close()
+    b, _ = _model(cfg, cap=256, tc=True)
+    sb = State(torch, cfg.vocab)
+    for c0, c1 in ((0, 256), (256, 264), (264, T)):
+        _prefill(torch, b, toks[c0:c1], pos[:, c0:c1], 0, c0, sb)
+    assert np.array_equal(la, sb.logits.cpu().numpy())
+    for x, y in zip(ka, _cache(b, cfg, 0)):
+        assert np.array_equal(x[:, :T], y[:, :T])
+    b.close()
+
+
 _PLAN_REF = {}
 
 
