@@ -6,21 +6,22 @@
 // At a few hundred tokens the projection is a dense contraction, so it goes to tcgen05.mma
 // (kind::f16, fp32 accumulators in tensor memory) instead of the warp-level mma the decode
 // GEMV uses:
-//   * CTA tile: 128 packed weight rows (the MMA's M, one TMEM lane each) x nt tokens (the
-//     MMA's N, 64 or 128 TMEM columns).
+//   * CTA tile: 128 packed weight rows (the MMA's M, one TMEM lane each) x nt = 64, 128 or 256
+//     tokens (the MMA's N, nt TMEM columns).
 //   * Warp-specialised pipeline with a full and an empty mbarrier per stage and no block-wide
-//     barrier inside the K loop: warp 0 fills a 4-deep ring with each 128-input group's eight
-//     1088-byte KMR4 blocks and a ring with the group's staged tokens (cp.async.bulk);
-//     warps 2..9 turn one block each into fp16 w = (q - 8) s + z (the nibble OR-ed into the
-//     mantissa of 1024.0 gives 1024 + q, or 1024 + 16 q for tile rows 8..15, exactly; one
-//     HFMA2 applies s and z) in the K-major core-matrix layout (8 rows x 16 bytes per core
-//     matrix) of a double-buffered A operand; warp 1 issues the group's 8 MMAs (K = 16 each)
-//     and commits them to the A and B stages' empty barriers.
-//   * The accumulator stays in tensor memory across all K; the epilogue reads it once
-//     (tcgen05.ld 32x32b), applies the row's RMSNorm factor / sigma and stores, adds to the
-//     residual, or applies SiLU(gate) * up across the gate / up rows of a tile.
-//   * Every wait is bounded (mbar_wait); a timeout records KMR_ERR_DEVICE_TIMEOUT, skips
-//     the remaining work, drains the copies in flight and frees tensor memory.
+//     barrier inside the K loop: a weight producer warp and a token producer warp copy each
+//     128-input group's eight 1088-byte KMR4 blocks and the group's staged tokens into their
+//     rings (cp.async.bulk, all of a group's copies in one instruction); eight warps turn the
+//     blocks into fp16 w = (q - 8) s + z (the nibble OR-ed into the mantissa of 1024.0 gives
+//     1024 + q, or 1024 + 16 q for tile rows 8..15, exactly; one HFMA2 applies s and z) and store
+//     them to tensor memory with tcgen05.st; one thread issues the group's 8 MMAs (A in TMEM, B
+//     in shared memory) and commits them to the stages' empty barriers.
+//   * The accumulator stays in tensor memory across the CTA's K range; the epilogue reads it
+//     (tcgen05.ld 32x32b), applies the token's RMSNorm factor / sigma and stores, adds to the
+//     residual, or applies SiLU(gate) * up across the gate / up rows of a tile.  A K split over
+//     a thread-block cluster merges the CTAs' partials through distributed shared memory.
+//   * Every wait is bounded; a timeout records KMR_ERR_DEVICE_TIMEOUT, skips the remaining work,
+//     drains the copies in flight and frees tensor memory.
 #include <cooperative_groups.h>
 #include <cuda_fp16.h>
 
