@@ -136,6 +136,10 @@ constexpr int kTcStageThreads = 256;
 constexpr int kTcStageMaxK = 8192;
 
 __global__ void __launch_bounds__(kTcStageThreads) tc_stage_kernel(const TcStageParams p) {
+    // launched as a programmatic dependent: the projection that consumes this staging may start
+    // its set-up and weight stream now; every global access here waits for the previous kernel
+    pdl_launch_dependents();
+    pdl_wait();
     const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K = p.K, G = K >> 7, K4 = K >> 2;
     __half* xs = reinterpret_cast<__half*>(p.xs);
@@ -385,7 +389,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcGemmPara
             ++issued_w;
         }
     } else if (warp == kTcTokenWarp) {
-        // ---- token producer: lanes 0..3 copy the group's four quarter blocks
+        // ---- token producer: lanes 0..3 copy the group's four quarter blocks, once the staging
+        // kernel has finished (the weight producer does not wait: the weights are constant)
+        pdl_wait();
         for (int gi = 0; gi < ng; ++gi) {
             const int g = g0 + gi, s = gi % kBS;
             int go = 0;
@@ -428,7 +434,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcGemmPara
         // ---- unpack: warp w dequantises the two tiles of its tensor-memory lane quarter
         // (rows 32 (w % 4) .. + 31), k-steps 4 (w - 2) / 4 .. + 3 of each group
         const int ut = warp - 2, lq = warp & 3, kj = ut >> 2;
-        // the row factors of the tile's tokens, for the epilogue (published by tc_epilogue_bar)
+        // the row factors of the tile's tokens, for the epilogue (published by tc_epilogue_bar);
+        // they and the residuals come from the previous kernels (programmatic dependent launch)
+        pdl_wait();
         for (int i = ut * 32 + lane; i < NT; i += kTcUnpackWarps * 32) {
             const int t = ttile * NT + i;
             rs_s[i] = t < p.M ? p.rs[t] : 0.f;
@@ -471,6 +479,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const TcGemmPara
         int acc_ok = 0;
         if (lane == 0) acc_ok = !*abort_flag && mbar_wait(acc_done, 0u, p.err);
         have_acc = __shfl_sync(0xffffffffu, acc_ok, 0) != 0;
+        pdl_launch_dependents();                      // the next kernel may launch during the epilogue
         tc_fence_after();
         tc_epilogue_bar();                             // rs_s complete
         if (warp == 2 && lane == 0) TC_MARK(63, 0);
@@ -663,13 +672,15 @@ cudaError_t tc_gemm_launch(const TcGemmParams& p, cudaStream_t st) {
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = tc_layout(NT).total;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = p.ksplit;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<NT>, p);
 }
 
@@ -733,8 +744,16 @@ cudaError_t tc_gemm_set_attributes() {
 
 cudaError_t launch_tc_stage(const TcStageParams& p, cudaStream_t st) {
     const int rows = (p.M + p.nt - 1) / p.nt * p.nt;
-    tc_stage_kernel<<<rows, kTcStageThreads, 0, st>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(rows);
+    cfg.blockDim = dim3(kTcStageThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_stage_kernel, p);
 }
 
 cudaError_t launch_tc_gemm(const TcGemmParams& p, cudaStream_t st) {
