@@ -19,6 +19,10 @@ namespace {
 
 template <int D>
 __global__ void __launch_bounds__(192) prefill_rope_kernel(const PrefillRopeParams p) {
+    // a programmatic dependent of the QKV projection: release the attention launch, then wait
+    // for the projection's rows before reading anything
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int EPL = D / 32;
     const int i = blockIdx.x, h = blockIdx.y;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -81,11 +85,17 @@ __global__ void __launch_bounds__(192) prefill_rope_kernel(const PrefillRopePara
 
 cudaError_t launch_prefill_rope(const PrefillRopeParams& p, cudaStream_t st) {
     const int threads = (p.nq / p.nkv + 2) * 32;
-    if (p.d == 128)
-        prefill_rope_kernel<128><<<dim3(p.T, p.nkv), threads, 0, st>>>(p);
-    else
-        prefill_rope_kernel<64><<<dim3(p.T, p.nkv), threads, 0, st>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.T, p.nkv);
+    cfg.blockDim = dim3(threads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (p.d == 128) return cudaLaunchKernelEx(&cfg, prefill_rope_kernel<128>, p);
+    return cudaLaunchKernelEx(&cfg, prefill_rope_kernel<64>, p);
 }
 
 }  // namespace kmr
@@ -120,6 +130,10 @@ __host__ __device__ constexpr int pa_pitch() { return D + 8; }  // halves per st
 template <int D, int REP>
 __global__ void __launch_bounds__(128) prefill_attn_kernel(const PrefillAttnParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
+    // a programmatic dependent of the q/k norm + RoPE kernel: release the next launch, then wait
+    // for the rotated queries and the cache rows before reading anything
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int PPT = 16 / REP, BQ = 4 * PPT, KT = D / 16, NT = D / 8, P = pa_pitch<D>();
     uint16_t* ks = reinterpret_cast<uint16_t*>(smem);                       // [2][64][P]
     uint16_t* vs = ks + 2 * kPaBK * P;                                        // [2][64][P]
@@ -282,8 +296,17 @@ cudaError_t launch_pa(const PrefillAttnParams& p, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    prefill_attn_kernel<D, REP><<<dim3((p.T + BQ - 1) / BQ, p.nkv), 128, smem, st>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.T + BQ - 1) / BQ, p.nkv);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = la;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_attn_kernel<D, REP>, p);
 }
 
 }  // namespace
