@@ -272,6 +272,19 @@ def test_tcgen05_tile_plans_agree(torch, plan):
     assert np.array_equal(lb, lc) and all(np.array_equal(x, y) for x, y in zip(kb, kc))
 
 
+def test_prefill_plan_argument_errors(torch):
+    """kmr_model_set_prefill_plan takes nt in {64, 128, 256} with ksplit in {1, 2, 4}, or (0, 0)
+    for the planned tiles; anything else is rejected and leaves the plan as it was."""
+    cfg = tiny_config(slots=2)
+    m, _ = _model(cfg)
+    L, h = kmr.lib(), m.handle
+    for nt, ks in ((32, 1), (256, 3), (0, 1), (128, 0), (512, 2), (-64, 1)):
+        assert L.kmr_model_set_prefill_plan(h, nt, ks) == kmr.KMR_ERR_INVALID_ARG, (nt, ks)
+    for nt, ks in ((64, 1), (128, 2), (256, 4), (0, 0)):
+        assert L.kmr_model_set_prefill_plan(h, nt, ks) == kmr.KMR_OK, (nt, ks)
+    m.close()
+
+
 def test_prefill_argument_errors(torch):
     cfg = tiny_config(slots=2)
     m, _ = _model(cfg)
