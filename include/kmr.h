@@ -418,6 +418,15 @@ int kmr_model_set_prefill_tcgen05(kmr_model* m, int enable);
  * model, or a value outside those sets). */
 int kmr_model_set_prefill_plan(kmr_model* m, int nt, int ksplit);
 
+/* The tile plan kmr_prefill chooses for a tcgen05 projection with N output
+ * rows (a multiple of 128), K inputs (a multiple of 128, at most 8192) and M
+ * prompt tokens on a GPU with `sms` SMs: *nt tokens per CTA and *ksplit CTAs
+ * along K.  The split depends on (N, K, sms) only, never on M, so a token's
+ * result does not change with the prompt length or chunking.  Host-only (no
+ * GPU needed).  Returns KMR_OK or KMR_ERR_INVALID_ARG (unsupported shape, M or
+ * sms < 1, null output). */
+int kmr_prefill_plan(int N, int K, int M, int sms, int* nt, int* ksplit);
+
 /* Whether the decode step runs its layers as one persistent kernel (default
  * off: on GB300 it measured slower than the multi-kernel step, whose
  * programmatic-dependent-launch hand-off between kernels costs less than the

@@ -14,7 +14,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from typing import Optional, Sequence
+from typing import Optional, Sequence, Tuple
 
 __all__ = [
     "KmrError", "KmrLibraryMissing", "lib", "library_path", "EXPORTED_SYMBOLS",
@@ -110,6 +110,7 @@ _SIGNATURES = {
     "kmr_model_set_smem_poison": (_I, [_P, _I, ctypes.c_uint32]),
     "kmr_model_set_prefill_tcgen05": (_I, [_P, _I]),
     "kmr_model_set_prefill_plan": (_I, [_P, _I, _I]),
+    "kmr_prefill_plan": (_I, [_I, _I, _I, _I, _P, _P]),
     "kmr_model_set_persistent_step": (_I, [_P, _I]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
@@ -226,6 +227,14 @@ def kmr_decode_attn_cascade(q, k_cache, v_cache, slot_ids, cache_position, prefi
                                          _ptr(cache_position), prefix_slot, prefix_len, B, nq, nkv, d, max_len,
                                          slots, float(scale), _ptr(out), _ptr(workspace), workspace_bytes,
                                          _stream(stream)), "kmr_decode_attn_cascade")
+
+
+def kmr_prefill_plan(N: int, K: int, M: int, sms: int) -> Tuple[int, int]:
+    """kmr_prefill_plan: (tokens per CTA, K split) of a tcgen05 prefill projection (host only)."""
+    nt, ks = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().kmr_prefill_plan(int(N), int(K), int(M), int(sms), ctypes.byref(nt), ctypes.byref(ks)),
+           "kmr_prefill_plan")
+    return nt.value, ks.value
 
 
 def kmr_last_device_error() -> int:

@@ -1250,6 +1250,14 @@ extern "C" int kmr_model_set_prefill_tcgen05(kmr_model* m, int enable) {
     return KMR_OK;
 }
 
+extern "C" int kmr_prefill_plan(int N, int K, int M, int sms, int* nt, int* ksplit) {
+    if (!nt || !ksplit || M < 1 || sms < 1 || !tc_gemm_supported(N, K)) return KMR_ERR_INVALID_ARG;
+    const TcPlan plan = tc_gemm_plan(N, K, M, sms);
+    *nt = plan.nt;
+    *ksplit = plan.ksplit;
+    return KMR_OK;
+}
+
 extern "C" int kmr_model_set_prefill_plan(kmr_model* m, int nt, int ksplit) {
     if (!m) return KMR_ERR_INVALID_ARG;
     const bool automatic = nt == 0 && ksplit == 0;

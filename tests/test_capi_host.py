@@ -176,3 +176,28 @@ def test_model_create_rejects_bad_config_on_host(L):
         h = ctypes.c_void_p()
         assert L.kmr_model_create(ctypes.byref(c), ctypes.byref(h)) == kmr.KMR_ERR_SHAPE, kw
         assert not h.value
+
+
+def test_prefill_plan_split_depends_on_the_shape_only(L):
+    """The tcgen05 prefill plan on the host: the K split of each 2B projection is the same for
+    every prompt length (so chunked and one-chunk prefill sum each output in the same order), the
+    tile width is one of 64/128/256, the split never exceeds K / 128, and at 512 tokens on 152 SMs
+    the plans are the fastest ones a GB300 sweep measured for each projection."""
+    shapes = {"qkv": (4096, 2048), "o": (2048, 2048), "gate_up": (12288, 2048), "down": (2048, 6144),
+              "tiny_qkv": (512, 256), "tiny_down": (256, 768)}
+    for name, (N, K) in shapes.items():
+        splits = set()
+        for M in (1, 7, 16, 100, 128, 200, 256, 300, 512, 777, 1024, 2048):
+            nt, ks = kmr.kmr_prefill_plan(N, K, M, 152)
+            assert nt in (64, 128, 256) and ks in (1, 2, 4) and ks <= K // 128, (name, M, nt, ks)
+            splits.add(ks)
+        assert len(splits) == 1, (name, splits)
+    assert kmr.kmr_prefill_plan(4096, 2048, 512, 152) == (128, 1)
+    assert kmr.kmr_prefill_plan(2048, 2048, 512, 152) == (128, 2)
+    assert kmr.kmr_prefill_plan(12288, 2048, 512, 152) == (256, 1)
+    assert kmr.kmr_prefill_plan(2048, 6144, 512, 152) == (256, 4)
+    nt, ks = ctypes.c_int(), ctypes.c_int()
+    for args in ((100, 2048, 512, 152), (4096, 100, 512, 152), (4096, 16384, 512, 152), (4096, 2048, 0, 152),
+                 (4096, 2048, 512, 0)):
+        assert L.kmr_prefill_plan(*args, ctypes.byref(nt), ctypes.byref(ks)) == kmr.KMR_ERR_INVALID_ARG, args
+    assert L.kmr_prefill_plan(4096, 2048, 512, 152, None, None) == kmr.KMR_ERR_INVALID_ARG
