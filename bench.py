@@ -4,7 +4,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--batch 1|4|16] [--impl kmr|reference]
     python bench.py --sweep          # standalone int4 GEMV / decode-attention sweeps
-    python bench.py --prefill-only T # two T-token prefills (a fixed command for launch lists)
+    python bench.py --prefill-only T [--prefill-mma]  # two T-token prefills (a fixed command for launch lists)
 
 A step is one pass of the whole decode path (every layer's int4 QKV / O /
 gate_up / down GEMVs, q/k norm, M-RoPE, KV write and GQA attention, final
