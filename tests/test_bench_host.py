@@ -76,3 +76,19 @@ def test_projection_flop_counts_every_layer_projection():
     per_layer = 4096 * 2048 + 2048 * 2048 + 12288 * 2048 + 2048 * 6144
     assert bench.projection_flop(cfg, 512) == 2.0 * per_layer * 512 * 28
     assert bench.projection_flop(cfg, 0) == 0.0
+
+
+def test_prefill_record_reports_flop_rate_and_speedup():
+    """The prefill object: the projections' flops over the default path's time, its fraction of
+    the measured bf16 peak, and the warp-level path's time and the speedup over it."""
+    import bench
+    from workloads import layer2b_config
+    cfg = layer2b_config(slots=1, n_layers=28)
+    r = {"prefill": {"tokens": 512, "ms": 4.0, "tok_s": 128000.0}, "prefill_mma": {"ms": 8.0}}
+    rec = bench.prefill_record(r, cfg, {"bf16_tflops": 1854.8})
+    flop = bench.projection_flop(cfg, 512)
+    assert rec["kernel"] == "tcgen05" and rec["tokens"] == 512 and rec["ms"] == 4.0
+    assert abs(rec["projection_tflops_whole_prefill"] - round(flop / 4e-3 / 1e12, 1)) < 1e-9
+    assert abs(rec["frac_of_bf16_peak"] - round(flop / 4e-3 / 1e12 / 1854.8, 3)) < 1e-9
+    assert rec["warp_mma_ms"] == 8.0 and rec["speedup_over_warp_mma"] == 2.0
+    assert bench.prefill_record(r, cfg, {})["frac_of_bf16_peak"] is None
